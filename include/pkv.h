@@ -1,0 +1,206 @@
+/*
+ * pkv.h - C ABI of libpkv.so: attention over a paged KV cache addressed through an int32 block
+ * table, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title, then the part of the page that defines the operation):
+ *   [P109]  HyperQwen PR #109 - int64 cast in the int8 prefill attention (prefill_attn_hd256.py):
+ *           description items 1-2 and the review (three kernels _k_stats_kernel,
+ *           _k_quant_kernel, _prefill_attn_kernel; exact-QK and int8-QK arms; chunk 2048,
+ *           head_dim 256, block 880; top-vs-bottom placement in a 2,600-block pool).
+ *   [P91]   HyperQwen PR #91 - int64 cast in the speculative-decode verify kernel
+ *           _spec_attn_partial: description and review (kernel excerpt: blk = table[req][pos //
+ *           BLOCK_SIZE], slot = pos % BLOCK_SIZE, K address blk * stride_kb + ...; int8
+ *           per-token-head scales addressed by the same blk; split-KV partials).
+ *   [P3360] vllm.cpp PR #3360 - serve fp8 KV prefill through the bf16 dense dequant, "What
+ *           changed": dequantize ONCE per layer into a dense bf16 scratch, one block per request
+ *           with block_size = max_seq and an identity block table, then run the bf16 kernel.
+ *
+ * Conventions shared by every call
+ *   - Caches are [num_blocks][block_size][num_kv_heads][head_dim] with explicit element strides
+ *     (stride_blk, stride_tok, stride_head; the head_dim axis is contiguous). The element
+ *     offset of (block blk, slot s, head h, d) is blk*stride_blk + s*stride_tok + h*stride_head + d,
+ *     and every block-id x stride product is formed in 64-bit arithmetic, so pools of any size
+ *     (past 2^31 elements) are addressed correctly [P109 item 1, P91 description].
+ *   - Key position pos of request r lives in block block_table[r*bt_stride + pos/block_size],
+ *     slot pos % block_size. Table entries past ceil(seq_len/block_size) are never read.
+ *   - Query head qh reads KV head qh / (num_q_heads / num_kv_heads).
+ *   - Request r's queries are its last q_len positions (seq_len - q_len .. seq_len - 1); a query
+ *     at position p attends keys 0..p (causal).
+ *   - head_dim must be 256 (the pages' geometry); other values return PKV_ERR_UNSUPPORTED.
+ *   - Ownership: the caller allocates every buffer (caches, tables, scratch, partials, outputs).
+ *     The library allocates no device memory and keeps no state beyond a thread-local error
+ *     message. All pointers except `stream` are device pointers unless stated otherwise.
+ *   - Streams: every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and returns without synchronising. Results are ready when the stream is.
+ *   - Errors: arguments are validated on the host before anything is launched; a failed check
+ *     returns a non-zero pkv_status, launches nothing and leaves a message for pkv_last_error().
+ *     `dev_err` (nullable, device int32, caller-zeroed) receives a device-side status when a
+ *     kernel meets a block id outside [0, num_blocks) or a position past the table
+ *     (PKV_ERR_DEVICE_BOUNDS; the access is skipped and reads as zero) or a bounded internal
+ *     wait expires (PKV_ERR_TIMEOUT). Kernels never trap.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad stride or alignment */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels implement (e.g. head_dim) */
+  PKV_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  PKV_ERR_DEVICE_BOUNDS = 4, /* device-side: out-of-range block id or position (via dev_err) */
+  PKV_ERR_TIMEOUT = 5        /* device-side: a bounded wait gave up (via dev_err) */
+} pkv_status;
+
+typedef enum pkv_qk_mode {
+  PKV_QK_BF16 = 0, /* exact QK: bf16 q . bf16 k, fp32 accumulate [P109 review, int8_qk=False] */
+  PKV_QK_INT8 = 1  /* int8 QK: per-row int8 q . per-token-head int8 k, exact integer dot,
+                      scaled by q_scale * k_scale [P109 review, int8_qk=True] */
+} pkv_qk_mode;
+
+/* Message of the last failed call on this host thread ("" if none). Never NULL. */
+PKV_API const char* pkv_last_error(void);
+
+/* ABI version of this header (incremented on any signature change). */
+#define PKV_ABI_VERSION 1
+PKV_API int32_t pkv_abi_version(void);
+
+/*
+ * kv_int8_stats_quant - per-token-head symmetric int8 quantization of the bf16 K cache
+ * [P109: _k_stats_kernel (per-token-head statistics read through blk = block_table[...]) and
+ *  _k_quant_kernel (int8 K written to a dense scratch indexed by position, one scale per slot)].
+ *
+ * For every request r, key position pos in [pos_begin[r], pos_end[r]) and KV head h, with
+ * x = the bf16 row k_cache[blk(r,pos)][pos % block_size][h][0..head_dim):
+ *   absmax = max |x|;  scale = absmax / 127 (fp32, round to nearest);
+ *   k8[r][pos][h][d] = clamp(rint(x[d] * (127 / absmax)), -127, 127)  (one fp32 divide per
+ *   row, one fp32 multiply per element, ties to even); absmax == 0 gives scale 0, codes 0.
+ * Output k8 int8 [num_reqs][max_ctx][num_kv_heads][head_dim] (contiguous),
+ *        k8_scale fp32 [num_reqs][max_ctx][num_kv_heads]; other positions are not written.
+ * pos_begin / pos_end: device int32 [num_reqs], 0 <= pos_begin <= pos_end <= max_ctx.
+ * max_tokens: host upper bound on pos_end[r] - pos_begin[r] (sizes the grid).
+ * max_blocks: columns of the block table (pos_end <= max_blocks * block_size).
+ */
+PKV_API pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_blocks, int64_t stride_blk,
+                                   int64_t stride_tok, int64_t stride_head,
+                                   const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                   const int32_t* pos_begin, const int32_t* pos_end, int32_t num_reqs,
+                                   int32_t max_tokens, int32_t block_size, int32_t num_kv_heads,
+                                   int32_t head_dim, int8_t* k8, float* k8_scale, int64_t max_ctx,
+                                   int32_t* dev_err, void* stream);
+
+/*
+ * kv_fp8_dequant_dense - per-tensor fp8 e4m3 K/V cache to a dense bf16 scratch, once per layer
+ * [P3360 "What changed"].
+ *
+ * For every request r, position pos < seq_lens[r], head h and d:
+ *   k_dense[r][pos][h][d] = bf16_rn(float(e4m3(k_fp8[blk][slot][h][d])) * (*k_scale))
+ * (one fp32 multiply rounded to nearest, then round-to-nearest-even to bf16), same for V.
+ * e4m3 is the OCP FP8 E4M3 format. Dense outputs are [num_reqs][max_seq][num_kv_heads][head_dim]
+ * contiguous bf16; positions >= seq_lens[r] are not written. The consumer then calls
+ * pkv_paged_prefill_attn on the dense scratch with block_size = max_seq, num_blocks = num_reqs
+ * and the identity table block_table[r] = r, so the paged address is the dense address.
+ * k_scale / v_scale: device pointers to one fp32 each. max_seq: host, >= every seq_lens[r].
+ */
+PKV_API pkv_status pkv_kv_fp8_dequant_dense(const uint8_t* k_fp8, const uint8_t* v_fp8, int64_t num_blocks,
+                                    int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                    const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                    const int32_t* seq_lens, int32_t num_reqs, int32_t max_seq,
+                                    int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                    const float* k_scale, const float* v_scale, void* k_dense,
+                                    void* v_dense, int32_t* dev_err, void* stream);
+
+/*
+ * paged_prefill_attn - chunked causal prefill attention over a paged bf16 cache
+ * [P109: _prefill_attn_kernel; exact-QK and int8-QK arms].
+ *
+ * q:   bf16 [total_q][num_q_heads][head_dim], contiguous; request r owns rows
+ *      query_start_loc[r] .. query_start_loc[r+1]-1 (device int32 [num_reqs+1]).
+ * out: bf16, same layout as q.
+ * For query row i of request r (position p = seq_lens[r] - q_len + i) and query head qh:
+ *   s_j = softmax_scale * q . k_j              (PKV_QK_BF16; fp32 accumulation)
+ *   s_j = softmax_scale * q_scale * k8_scale[r][j][kvh] * (q8 . k8[r][j][kvh])   (PKV_QK_INT8;
+ *         q8 / q_scale = the kv_int8_stats_quant quantizer applied to the bf16 q row; the
+ *         integer dot product is exact)
+ *   out = sum_{j<=p} exp(s_j - m) v_j / sum_{j<=p} exp(s_j - m),   v_j from the bf16 V cache.
+ * PKV_QK_INT8 reads k8 / k8_scale ([num_reqs][max_ctx][num_kv_heads][head_dim] / [...][kvh], as
+ * written by pkv_kv_int8_stats_quant, covering positions 0..seq_len-1) instead of the K cache;
+ * k_cache may then be NULL. PKV_QK_BF16 ignores k8, k8_scale and max_ctx.
+ * max_q_len: host upper bound on any request's q_len. total_q: host, = query_start_loc[num_reqs].
+ * Requirements: head_dim == 256; block_size a multiple of 8; q, caches and strides 16-byte
+ * aligned; num_q_heads a multiple of num_kv_heads.
+ */
+PKV_API pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, const void* v_cache,
+                                  int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                  int64_t stride_head, const int32_t* block_table, int64_t bt_stride,
+                                  int32_t max_blocks, const int32_t* seq_lens,
+                                  const int32_t* query_start_loc, int32_t num_reqs, int32_t total_q,
+                                  int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t block_size, float softmax_scale,
+                                  int32_t qk_mode, const int8_t* k8, const float* k8_scale,
+                                  int64_t max_ctx, void* out, int32_t* dev_err, void* stream);
+
+/*
+ * spec_verify_attn_partial - speculative-decode verify attention over an int8 per-token-head
+ * cache, as split-KV partials [P91: _spec_attn_partial; scales read via the same blk].
+ *
+ * Every request has T query tokens (rows r*T .. r*T+T-1 of q, bf16 [num_reqs*T][num_q_heads]
+ * [head_dim]); seq_lens[r] counts the cached prefix plus these T tokens, and query token t sits
+ * at position seq_lens[r] - T + t. Keys and values are int8 codes times fp32 per-token-head
+ * scales: k = k_cache[...] * k_scale[blk*scale_stride_blk + slot*scale_stride_tok + h], same for v.
+ * Split s of request r covers key positions [s*split_tokens, min((s+1)*split_tokens, seq_len));
+ * request r has ceil(seq_lens[r] / split_tokens) <= max_splits splits. For each split and row:
+ *   part_o[s][row][qh][:] = sum_j w_j v_j / sum_j w_j,  part_lse[s][row][qh] = m + ln(sum_j w_j),
+ *   w_j = exp(s_j - m) over the split's keys the row can see, s_j = softmax_scale * q . k_j;
+ *   a split with no visible key gives part_lse = -inf and part_o = 0.
+ * part_o fp32 [max_splits][num_reqs*T][num_q_heads][head_dim], part_lse fp32
+ * [max_splits][num_reqs*T][num_q_heads]: caller-allocated, pkv_spec_verify_workspace_bytes()
+ * bytes in total (part_o first, part_lse right after, each 256-byte aligned when carved from
+ * one allocation). split_tokens must be a positive multiple of 128.
+ * Requirements: head_dim == 256; T * (num_q_heads / num_kv_heads) == 32 (8 tokens x 4 query
+ * heads per KV head, the pages' geometry); num_kv_heads a multiple of 4; block_size a multiple
+ * of 8; scale strides multiples of 4 elements; q, caches and scales 16-byte aligned. Keys in a
+ * block whose id is out of range read as zero (k = v = 0) and PKV_ERR_DEVICE_BOUNDS is recorded.
+ */
+PKV_API size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_splits);
+PKV_API pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                        const float* k_scale, const float* v_scale,
+                                        int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                        int64_t stride_head, int64_t scale_stride_blk,
+                                        int64_t scale_stride_tok, const int32_t* block_table,
+                                        int64_t bt_stride, int32_t max_blocks,
+                                        const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size,
+                                        float softmax_scale, int32_t split_tokens,
+                                        int32_t max_splits, float* part_o, float* part_lse,
+                                        int32_t* dev_err, void* stream);
+
+/*
+ * spec_verify_combine - log-sum-exp merge of the split-KV partials [P91, split-KV verify].
+ *   LSE = ln sum_s exp(part_lse[s]);  out = sum_s exp(part_lse[s] - LSE) part_o[s]
+ * over the ceil(seq_lens[r] / split_tokens) splits of each request; out bf16
+ * [num_reqs*T][num_q_heads][head_dim].
+ */
+PKV_API pkv_status pkv_spec_verify_combine(const float* part_o, const float* part_lse,
+                                   const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                   int32_t num_q_heads, int32_t head_dim, int32_t split_tokens,
+                                   int32_t max_splits, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

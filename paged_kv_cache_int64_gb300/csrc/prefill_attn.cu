@@ -1,0 +1,669 @@
+// prefill_attn.cu - pkv_paged_prefill_attn: chunked causal prefill attention over a paged bf16
+// KV cache, exact-QK (bf16) or int8-QK.
+//
+// HyperQwen PR #109 (_prefill_attn_kernel in prefill_attn_hd256.py; review: the "int8_qk=False"
+// and "int8_qk=True" arms, chunk 2048, head_dim 256, block 880): for every query of the chunk,
+// softmax(scale * q.K^T) V over the keys at or before its position, K and V read through the
+// block table with the block id widened to int64 before the stride product.
+//
+// sm_103a design (one CTA = 128 query rows of one query head of one request):
+//   warp 0      TMA producer: Q once; per 128-key tile, K and V gathered from the paged pool in
+//               segments of gcd(block_size, 128) keys with a 4-D tensor map
+//               [head_dim, kv_heads, block_size, num_blocks] whose block coordinate is the block
+//               id (the TMA unit forms the 64-bit address); one lane per segment reads the table
+//               and issues that segment's copies; the next tile's block ids are read early.
+//   warp 1      MMA issuer (one thread): S = Q K^T (tcgen05.mma kind::f16, M=128 N=128 K=256,
+//               both operands in shared memory, f32 accumulator in tensor memory), then
+//               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
+//   warp 2      tensor-memory allocation (512 columns: O 256, two S buffers of 128).
+//   warps 4-7   softmax: thread i owns row i (TMEM lane i): scale, causal mask, running max
+//               (moved only when it grows by more than 2^8, so O is rarely rescaled), exp2, row
+//               sum, P packed to bf16 into the S columns; the epilogue normalises O, stores bf16.
+//   warps 8-11  int8-QK only: widen the int8 K tile (dense scratch of kv_int8_stats_quant) to
+//               fp16 integers; the softmax warps quantize their Q rows in place first. Q8.K8 runs
+//               as an f16 MMA: every product and partial sum is an integer below 2^24, so the f32
+//               accumulator holds the exact integer dot product.
+// Rows of the last tile past seq_len (and of any out-of-range block) are zero-filled in shared
+// memory before the MMAs read them, so stale or NaN pool bytes never reach P.V. Every wait is
+// bounded: on expiry the CTA records PKV_ERR_TIMEOUT, drains and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "host_common.h"
+#include "sm103.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kD = 256;
+constexpr int kBM = 128;                // query rows per CTA
+constexpr int kBN = 128;                // keys per tile
+constexpr int kChunkBytes = 128 * 128;  // one [128 rows][64 x 16-bit] swizzled chunk
+constexpr int kTileBytes = 4 * kChunkBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;
+constexpr uint32_t kColS0 = 256;
+constexpr uint32_t kColS1 = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// dynamic shared memory layout (1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffV = kOffK + kTileBytes;
+constexpr int kOffK8 = kOffV + kTileBytes;  // int8 mode: [2 chunks][128 rows][128 B]
+constexpr int kK8Bytes = 2 * kChunkBytes;
+
+struct Barriers {
+  uint64_t q_full;      // TMA Q landed
+  uint64_t q_ready;     // int8: Q quantized in place
+  uint64_t k_full[4];   // chunk c of K tile j ready (TMA bytes, or converter arrivals)
+  uint64_t k_empty[4];  // chunk c of K tile j consumed by the QK MMAs
+  uint64_t k8_full;     // int8: K8 tile landed
+  uint64_t k8_free;     // int8: K8 stage consumed by the converter
+  uint64_t v_full;      // V tile j ready
+  uint64_t fix;         // producer-private: copies of a tile that needs zero-filled rows
+  uint64_t s_full[2];   // S_j in TMEM
+  uint64_t p_full;      // P_j in TMEM and O rescaled
+  uint64_t pv_done;     // PV_j complete (V free, O current)
+  uint32_t tmem_base;
+  int abort;
+  float kscale[2][kBN];  // int8: per-key scales of the tile
+};
+
+struct Params {
+  CUtensorMap qmap;   // bf16 q: dims {D, Hq, total_q}, box {64, 1, 128}
+  CUtensorMap kmap;   // bf16 pool: dims {D, Hkv, bs, nb}, box {64, 1, G, 1}
+  CUtensorMap vmap;
+  CUtensorMap k8map;  // int8 scratch: dims {D, Hkv, R*max_ctx}, box {128, 1, 128}
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t num_q_heads, group, block_size, seg;
+  float scale_log2;
+  const float* k8_scale;
+  int64_t max_ctx;
+  int32_t num_kv_heads;
+  int32_t n_mtiles;
+  __nv_bfloat16* out;
+  int* dev_err;
+};
+
+template <bool kInt8>
+struct Cfg {
+  static constexpr int kThreads = kInt8 ? 384 : 256;
+  static constexpr int kTiles = kInt8 ? kOffK8 + kK8Bytes : kOffK8;
+  static constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Quantize this thread's Q row (row i of the swizzled bf16 Q tile) in place to fp16 integers and
+// return its scale: absmax / 127 and codes rint(x * (127 / absmax)) clamped to +-127, the
+// arithmetic of kv_int8_stats_quant.
+__device__ float quantize_q_row_inplace(uint8_t* sQ, int i) {
+  float amax = 0.0f;
+  bool nan = false;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sQ + c * kChunkBytes + sw128_offset(i, q * 8));
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(b[e]);
+        nan |= (f.x != f.x) | (f.y != f.y);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  const bool live = !nan && amax > 0.0f;
+  const float scale = nan ? __int_as_float(0x7fc00000) : (amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f);
+  const float inv = live ? __fdiv_rn(127.0f, amax) : 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint4* ptr = reinterpret_cast<uint4*>(sQ + c * kChunkBytes + sw128_offset(i, q * 8));
+      uint4 v = *ptr;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        int c0 = 0, c1 = 0;
+        if (live) {
+          c0 = max(-127, min(127, __float2int_rn(__fmul_rn(f.x, inv))));
+          c1 = max(-127, min(127, __float2int_rn(__fmul_rn(f.y, inv))));
+        }
+        const __half2 h = __halves2half2(__int2half_rn(c0), __int2half_rn(c1));
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *ptr = v;
+    }
+  }
+  return scale;
+}
+
+// 16 int8 codes -> 16 fp16 integers (exact).
+__device__ __forceinline__ void widen16(uint4 in, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b0 = (int)(int8_t)(w[i] & 0xffu), b1 = (int)(int8_t)((w[i] >> 8) & 0xffu);
+    const int b2 = (int)(int8_t)((w[i] >> 16) & 0xffu), b3 = (int)(int8_t)(w[i] >> 24);
+    const __half2 h01 = __halves2half2(__int2half_rn(b0), __int2half_rn(b1));
+    const __half2 h23 = __halves2half2(__int2half_rn(b2), __int2half_rn(b3));
+    o[2 * i] = *reinterpret_cast<const uint32_t*>(&h01);
+    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Zero whole 128-byte rows (all four chunks) of a [4][128][128 B] tile: rows >= n_valid and rows
+// of segments whose bit is set in bad_mask. Executed by one warp.
+__device__ __forceinline__ void zero_rows(uint8_t* tile, int n_valid, uint32_t bad_mask, int G, int lane) {
+  for (int idx = lane; idx < 4 * kBN * 8; idx += 32) {
+    const int piece = idx & 7;
+    const int row = (idx >> 3) & (kBN - 1);
+    const int c = idx >> 10;
+    if (row >= n_valid || ((bad_mask >> (row / G)) & 1u))
+      *reinterpret_cast<uint4*>(tile + c * kChunkBytes + row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <bool kInt8>
+__global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
+    paged_prefill_attn_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  uint8_t* sK8 = smem + kOffK8;
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kInt8>::kTiles);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.z;
+  const int qh = blockIdx.y;
+  const int mt = p.n_mtiles - 1 - (int)blockIdx.x;  // latest (heaviest) tiles first
+  const int kvh = qh / p.group;
+  const int q0 = __ldg(p.qsl + r);
+  const int q_len = __ldg(p.qsl + r + 1) - q0;
+  const int seq_len = __ldg(p.seq_lens + r);
+  if (mt * kBM >= q_len || q_len > seq_len) return;  // CTA-uniform
+  const int rows_valid = min(kBM, q_len - mt * kBM);
+  const int p0 = seq_len - q_len + mt * kBM;         // position of row 0
+  const int kv_end = min(seq_len, p0 + rows_valid);  // keys [0, kv_end)
+  const int n_tiles = (kv_end + kBN - 1) / kBN;
+  const int tok0 = q0 + mt * kBM;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_ready, 128);
+    for (int c = 0; c < 4; ++c) {
+      mbar_init(&bar.k_full[c], kInt8 ? 128 : 1);
+      mbar_init(&bar.k_empty[c], 1);
+    }
+    mbar_init(&bar.k8_full, 1);
+    mbar_init(&bar.k8_free, 128);
+    mbar_init(&bar.v_full, 1);
+    mbar_init(&bar.fix, 1);
+    mbar_init(&bar.s_full[0], 1);
+    mbar_init(&bar.s_full[1], 1);
+    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.pv_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bar.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  volatile int* abort = &bar.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------------------- producer
+    const int G = p.seg;
+    const int nseg = kBN / G;
+    const uint32_t seg_bytes = (uint32_t)G * 128u;  // one chunk of one segment
+    if (lane == 0) {
+      prefetch_tensormap(&p.qmap);
+      prefetch_tensormap(&p.vmap);
+      if (kInt8) prefetch_tensormap(&p.k8map); else prefetch_tensormap(&p.kmap);
+      mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
+      for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
+    }
+    // block id of segment `lane` of tile j: >= 0, -1 past seq_len, -2 out-of-range entry
+    auto lookup = [&](int j) -> int {
+      const int pos = j * kBN + lane * G;
+      if (lane >= nseg || pos >= seq_len) return -1;
+      const int col = pos / p.block_size;
+      if (col >= p.max_blocks) return -2;
+      const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
+      if (blk < 0 || (int64_t)blk >= p.num_blocks) return -2;
+      return blk;
+    };
+    auto issue_seg = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, int blk, int key0) {
+      const int slot = (key0 + lane * G) % p.block_size;
+      for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes + lane * G * 128, map, mb, c * 64, kvh, slot, blk);
+    };
+    struct TileInfo {
+      int blk;           // this lane's segment block id (>= 0), -1 past seq_len, -2 bad entry
+      uint32_t bad;      // segments with a bad table entry
+      uint32_t nloaded;  // segments with a valid block
+      bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
+    };
+    auto info = [&](int j) -> TileInfo {
+      TileInfo t;
+      t.blk = j < n_tiles ? lookup(j) : -1;
+      t.bad = __ballot_sync(0xffffffffu, t.blk == -2);
+      t.nloaded = __popc(__ballot_sync(0xffffffffu, t.blk >= 0));
+      t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
+      return t;
+    };
+    // K tile j through k_full[c] (bf16) or the K8 stage (int8), chunk by chunk as QK_{j-1} frees it
+    auto load_k = [&](int j, const TileInfo& t) {
+      const int key0 = j * kBN;
+      if (kInt8) {
+        if (lane == 0 && (j == 0 || mbar_wait(&bar.k8_free, (j - 1) & 1, abort))) {
+          mbar_arrive_expect_tx(&bar.k8_full, kK8Bytes);
+          const int row = (int)((int64_t)r * p.max_ctx + key0);
+          for (int c = 0; c < 2; ++c) tma_load_3d(sK8 + c * kChunkBytes, &p.k8map, &bar.k8_full, c * 128, kvh, row);
+        }
+        __syncwarp();
+        return;
+      }
+      const int slot = (key0 + lane * G) % p.block_size;
+      for (int c = 0; c < 4; ++c) {
+        if (lane == 0) {
+          if (j == 0 || mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort))
+            mbar_arrive_expect_tx(&bar.k_full[c], t.nloaded * seg_bytes);
+        }
+        __syncwarp();
+        if (*abort) return;
+        if (t.blk >= 0)
+          tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
+      }
+    };
+    uint32_t fix_phase = 0;
+    TileInfo cur = info(0);
+    TileInfo nxt = info(1);
+    if (kInt8 || !cur.fix) load_k(0, cur);
+    for (int j = 0; j < n_tiles && !*abort; ++j) {
+      const int key0 = j * kBN;
+      const int n_valid = min(kBN, seq_len - key0);
+      if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
+      // K of the next tile first: it streams in while QK_j runs
+      if (j + 1 < n_tiles && (kInt8 || !nxt.fix)) load_k(j + 1, nxt);
+      __syncwarp();
+      if (*abort) break;
+      // V_j once PV_{j-1} has released the V tile
+      if (lane == 0 && j > 0) mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      __syncwarp();
+      if (*abort) break;
+      if (!cur.fix) {
+        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, 4u * cur.nloaded * seg_bytes);
+        __syncwarp();
+        if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
+      } else {
+        // A tile with rows to zero-fill (the CTA's tail past seq_len, or a bad table entry): load
+        // K (bf16) and V through the private barrier, zero those rows, then publish both.
+        if (lane == 0) {
+          if (!kInt8)
+            for (int c = 0; c < 4 && j > 0; ++c)
+              if (!mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
+          if (!*abort) mbar_arrive_expect_tx(&bar.fix, (kInt8 ? 4u : 8u) * cur.nloaded * seg_bytes);
+        }
+        __syncwarp();
+        if (*abort) break;
+        if (cur.blk >= 0) {
+          issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
+          if (!kInt8) issue_seg(sK, &p.kmap, &bar.fix, cur.blk, key0);
+        }
+        if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+        ++fix_phase;
+        __syncwarp();
+        if (*abort) break;
+        zero_rows(sV, n_valid, cur.bad, G, lane);
+        if (!kInt8) zero_rows(sK, kBN, cur.bad, G, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (!kInt8)
+            for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
+          mbar_arrive(&bar.v_full);
+        }
+      }
+      __syncwarp();
+      cur = nxt;
+      nxt = info(j + 2);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_f16(128, 128, !kInt8, false, false);
+      constexpr uint32_t id_pv = idesc_f16(128, 256, true, false, true);
+      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
+      bool ok = mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, 0, abort);
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(&bar.p_full, i & 1, abort)) return false;
+        if (!mbar_wait(&bar.v_full, i & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t a = tmem + ((i & 1) ? kColS1 : kColS0);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_f16_ts(tmem + kColO, a + ks * 8, smem_desc(v_base + ks * 2048, 16384, 1024), id_pv,
+                      (i > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&bar.pv_done);
+        return true;
+      };
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j >= 2 && !mbar_wait(&bar.pv_done, (j - 2) & 1, abort)) break;
+        const uint32_t dS = tmem + ((j & 1) ? kColS1 : kColS0);
+        for (int c = 0; c < 4; ++c) {
+          if (!mbar_wait(&bar.k_full[c], j & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t off = c * kChunkBytes + kk * 32;
+            umma_f16_ss(dS, smem_desc(q_base + off, 16, 1024), smem_desc(k_base + off, 16, 1024), id_qk,
+                        (c | kk) ? 1u : 0u);
+          }
+          umma_commit(&bar.k_empty[c]);
+        }
+        if (!ok) break;
+        umma_commit(&bar.s_full[j & 1]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------------------------- softmax
+    const int quarter = warp - 4;
+    const int i = quarter * 32 + lane;
+    const int p_i = min(p0 + i, seq_len - 1);
+    const bool row_valid = i < rows_valid;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float sc = p.scale_log2;
+    bool ok = true;
+    if (kInt8) {
+      ok = mbar_wait(&bar.q_full, 0, abort);
+      if (ok) {
+        sc = p.scale_log2 * quantize_q_row_inplace(sQ, i);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.q_ready);
+      }
+    }
+    float m_run = -INFINITY, l_run = 0.0f;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int key0 = j * kBN;
+      const float* ks = bar.kscale[j & 1];
+      if (kInt8) {
+        const int key = key0 + i;
+        float v = 0.0f;
+        if (key < seq_len) v = __ldg(p.k8_scale + ((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh);
+        bar.kscale[j & 1][i] = v;
+        named_bar_sync(1, 128);
+      }
+      if (!mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const uint32_t sb = tmem + lane_off + ((j & 1) ? kColS1 : kColS0);
+      const bool need_mask = key0 + kBN - 1 > p_i;
+      const int lim = p_i - key0;  // columns > lim are masked
+      // pass 1: row max of the scaled, masked scores
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(sb + cc * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = cc * 32 + e;
+          float s = __uint_as_float(v[e]) * (kInt8 ? sc * ks[col] : sc);
+          if (need_mask && col > lim) s = -INFINITY;
+          mx = fmaxf(mx, s);
+        }
+      }
+      bool rescale = false;
+      float alpha = 1.0f;
+      if (m_run == -INFINITY || mx > m_run + kRescaleThreshold) {
+        const float m_new = fmaxf(m_run, mx);
+        if (m_new != -INFINITY) {
+          rescale = m_run != -INFINITY;
+          alpha = rescale ? ex2_approx(m_run - m_new) : 0.0f;
+          l_run *= alpha;
+          m_run = m_new;
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+      // pass 2: P = exp2(s - m), row sum, bf16 pairs written over the consumed S columns
+      float lsum = 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(sb + cc * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = cc * 32 + 2 * e;
+          float s0 = __uint_as_float(v[2 * e]) * (kInt8 ? sc * ks[col] : sc);
+          float s1 = __uint_as_float(v[2 * e + 1]) * (kInt8 ? sc * ks[col + 1] : sc);
+          if (need_mask && col > lim) s0 = -INFINITY;
+          if (need_mask && col + 1 > lim) s1 = -INFINITY;
+          const float e0 = ex2_approx(s0 - m_use), e1 = ex2_approx(s1 - m_use);
+          lsum += e0 + e1;
+          pk[e] = pack_bf16x2(e0, e1);
+        }
+        tmem_st_32x32b_x16(sb + cc * 16, pk);
+      }
+      tmem_wait_st();
+      l_run += lsum;
+      // O may be touched only once PV_{j-1} has completed
+      if (j > 0) {
+        if (!mbar_wait(&bar.pv_done, (j - 1) & 1, abort)) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+    }
+    // epilogue: O / l -> bf16 rows
+    if (!*abort && n_tiles > 0 && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort)) {
+      tc_fence_after();
+      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(tok0 + i) * p.num_q_heads + qh) * kD);
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
+        tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv_l, __uint_as_float(v[8 * q + 1]) * inv_l);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv_l, __uint_as_float(v[8 * q + 3]) * inv_l);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv_l, __uint_as_float(v[8 * q + 5]) * inv_l);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv_l, __uint_as_float(v[8 * q + 7]) * inv_l);
+            dst[cc * 4 + q] = o;
+          }
+        }
+      }
+    }
+  } else if (kInt8 && warp >= 8) {
+    // ---------------------------------------------------------------------------- int8 K widening
+    const int t = (warp - 8) * 32 + lane;  // row of the K tile
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!mbar_wait(&bar.k8_full, j & 1, abort)) break;
+      bool ok = true;
+      for (int c = 0; c < 4; ++c) {
+        if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t q8 = 4u * (c & 1) + q;  // 16-byte piece of the int8 row within chunk c/2
+          const uint4 v = *reinterpret_cast<const uint4*>(sK8 + (c >> 1) * kChunkBytes + t * 128 +
+                                                          ((q8 ^ (t & 7)) * 16));
+          uint4 lo, hi;
+          widen16(v, lo, hi);
+          uint8_t* row = sK + c * kChunkBytes + t * 128;
+          *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.k_full[c]);
+      }
+      if (!ok) break;
+      mbar_arrive(&bar.k8_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && bar.abort) record_error(p.dev_err, kErrTimeout);
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+}  // namespace
+
+}  // namespace pkv
+
+extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, const void* v_cache,
+                                             int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                             int64_t stride_head, const int32_t* block_table, int64_t bt_stride,
+                                             int32_t max_blocks, const int32_t* seq_lens,
+                                             const int32_t* query_start_loc, int32_t num_reqs, int32_t total_q,
+                                             int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size, float softmax_scale,
+                                             int32_t qk_mode, const int8_t* k8, const float* k8_scale,
+                                             int64_t max_ctx, void* out, int32_t* dev_err, void* stream) {
+  using namespace pkv;
+  clear_error();
+  PKV_UNSUP(head_dim == kD, "paged_prefill_attn: head_dim must be 256 (got %d)", head_dim);
+  PKV_ARG(qk_mode == PKV_QK_BF16 || qk_mode == PKV_QK_INT8, "paged_prefill_attn: unknown qk_mode %d", qk_mode);
+  const bool int8 = qk_mode == PKV_QK_INT8;
+  PKV_ARG(q && v_cache && block_table && seq_lens && query_start_loc && out,
+          "paged_prefill_attn: null pointer argument");
+  PKV_ARG(int8 ? (k8 && k8_scale && max_ctx > 0) : (k_cache != nullptr),
+          "paged_prefill_attn: missing K source for the selected qk_mode");
+  PKV_ARG(num_reqs >= 0 && total_q >= 0 && max_q_len >= 0 && num_blocks > 0 && block_size > 0 &&
+              max_blocks > 0 && bt_stride >= max_blocks && num_q_heads > 0 && num_kv_heads > 0,
+          "paged_prefill_attn: bad size argument");
+  PKV_UNSUP(num_q_heads % num_kv_heads == 0, "paged_prefill_attn: num_q_heads %% num_kv_heads != 0");
+  PKV_UNSUP(block_size % 8 == 0, "paged_prefill_attn: block_size must be a multiple of 8 (got %d)", block_size);
+  PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0, "paged_prefill_attn: strides must be positive");
+  PKV_ARG(aligned16(q) && aligned16(v_cache) && aligned16(out) && (int8 || aligned16(k_cache)) &&
+              (!int8 || aligned16(k8)) && stride_blk % 8 == 0 && stride_tok % 8 == 0 && stride_head % 8 == 0,
+          "paged_prefill_attn: q, caches, out and strides must be 16-byte aligned");
+  PKV_ARG(softmax_scale > 0.0f, "paged_prefill_attn: softmax_scale must be positive");
+  PKV_UNSUP(!int8 || (int64_t)num_reqs * max_ctx < (1ll << 31), "paged_prefill_attn: int8 scratch too large");
+  if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+
+  Params p{};
+  const int G = gcd_int(block_size, kBN);
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_q_heads, (uint64_t)total_q};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)num_q_heads * kD * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kBM};
+    pkv_status s = encode_tiled(&p.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, "q");
+    if (s != PKV_OK) return s;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
+    const uint64_t strides[3] = {(uint64_t)stride_head * 2, (uint64_t)stride_tok * 2, (uint64_t)stride_blk * 2};
+    const uint32_t box[4] = {64, 1, (uint32_t)G, 1};
+    pkv_status s = encode_tiled(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v_cache, dims, strides, box, "v_cache");
+    if (s != PKV_OK) return s;
+    if (!int8) {
+      s = encode_tiled(&p.kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k_cache, dims, strides, box, "k_cache");
+      if (s != PKV_OK) return s;
+    }
+  }
+  if (int8) {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_kv_heads, (uint64_t)num_reqs * (uint64_t)max_ctx};
+    const uint64_t strides[2] = {(uint64_t)kD, (uint64_t)num_kv_heads * kD};
+    const uint32_t box[3] = {128, 1, (uint32_t)kBN};
+    pkv_status s = encode_tiled(&p.k8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k8, dims, strides, box, "k8");
+    if (s != PKV_OK) return s;
+  }
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.num_q_heads = num_q_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.seg = G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.k8_scale = k8_scale;
+  p.max_ctx = max_ctx;
+  p.num_kv_heads = num_kv_heads;
+  p.n_mtiles = (max_q_len + kBM - 1) / kBM;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.dev_err = dev_err;
+
+  dim3 grid((unsigned)p.n_mtiles, (unsigned)num_q_heads, (unsigned)num_reqs);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (int8) {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(paged_prefill_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<true>::kSmem);
+      attr = true;
+    }
+    paged_prefill_attn_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmem, st>>>(p);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(paged_prefill_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<false>::kSmem);
+      attr = true;
+    }
+    paged_prefill_attn_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmem, st>>>(p);
+  }
+  return check_launch("paged_prefill_attn");
+}

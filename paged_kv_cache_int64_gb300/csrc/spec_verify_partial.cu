@@ -1,0 +1,544 @@
+// spec_verify_partial.cu - pkv_spec_verify_attn_partial: speculative-decode verify attention over
+// an int8 per-token-head KV cache, as split-KV partials.
+//
+// HyperQwen PR #91 (_spec_attn_partial in spec_decode_attn.py): each request verifies T draft
+// tokens against its long cached prefix; K/V are read through blk = table[req][pos // BLOCK_SIZE]
+// with the block id widened to int64, and the int8 per-token-head scales are addressed with the
+// same block id; the key range is cut into splits whose partials are merged by log-sum-exp.
+//
+// sm_103a design, one CTA = (split, KV head, request); the T tokens x g query heads that share the
+// KV head form N = 32 query columns, and the MMAs are "swapped" so the 128 keys of a tile are the
+// M dimension (the verify step is HBM-bound at ~63 flop per cache byte, beyond CUDA cores):
+//   warp 0     TMA producer: Q once; per 128-key tile, int8 K, int8 V (4-D maps over the paged
+//              pool, block id as a coordinate) and the fp32 K/V scales (3-D maps, same block id)
+//              into a double-buffered stage.
+//   warp 1     MMA issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
+//              from tensor memory, Q fp16 in shared memory), then O^T += V^T P^T (two M=128
+//              halves of head_dim, N=32, K=128 keys; V MN-major fp16 and P^T fp16 in shared memory).
+//   warps 4-7  thread k owns key k of the tile: widen its int8 K row to fp16 integers straight
+//              into tensor memory and its int8 V row into the shared V tile (byte-permute
+//              conversion: fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one subtraction of
+//              1152 gives b exactly - the int8->fp16 method of Kim et al. 2022, "Who Says
+//              Elephants Can't Run"); fold the K scale into its score and the V scale into its P
+//              entry; online softmax per query column (column max by warp butterfly + shared
+//              memory across warps; the running max moves only when it grows by more than 2^8);
+//              at the end, column sums, normalised partial O and its log-sum-exp.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "host_common.h"
+#include "sm103.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kD = 256;
+constexpr int kBN = 128;  // keys per tile
+constexpr int kNQ = 32;   // query columns (T * group)
+constexpr int kThreads = 256;
+constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
+constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
+constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
+constexpr int kPChunk = kNQ * 128;      // fp16 P^T [32 rows][64 keys] swizzled chunk
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColK = 0;    // 128 columns: fp16 K rows, two per column
+constexpr uint32_t kColS = 128;  // 32 columns: S^T
+constexpr uint32_t kColO = 160;  // 2 x 32 columns: O^T halves
+constexpr float kRescaleThreshold = 8.0f;
+
+// shared memory layout (1024-aligned)
+constexpr int kOffQ = 0;                         // 4 x kQChunk = 16 KB
+constexpr int kStageK8 = 0;                      // within a stage
+constexpr int kStageV8 = 2 * kChunk8;
+constexpr int kStageKS = 4 * kChunk8;            // [128 keys][4] fp32
+constexpr int kStageVS = kStageKS + kBN * 16;
+constexpr int kStageBytes = kStageVS + kBN * 16;  // 68 KB
+constexpr int kOffStage = kOffQ + 4 * kQChunk;
+constexpr int kOffV16 = kOffStage + 2 * kStageBytes;
+constexpr int kOffP = kOffV16 + 4 * kChunk16;
+constexpr int kTiles = kOffP + 2 * kPChunk;
+
+struct Barriers {
+  uint64_t q_full, q_ready;
+  uint64_t st_full[2], st_free[2];
+  uint64_t kv_ready;  // K in TMEM and V in shared memory for tile j
+  uint64_t qk_done;   // S^T_j ready, K free
+  uint64_t p_full;    // P^T_j written, O^T rescaled
+  uint64_t pv_done;   // PV_j complete
+  uint32_t tmem_base;
+  int abort;
+  uint32_t bad[2];          // per stage: segments whose block id was out of range
+  float red[2][4][kNQ];     // per-warp column partials
+};
+
+struct Params {
+  CUtensorMap qmap;   // bf16 [R*T][Hq][D]: dims {D, Hq, R*T}, box {64, g, T}
+  CUtensorMap k8map;  // int8 pool: dims {D, Hkv, bs, nb}, box {128, 1, G, 1}
+  CUtensorMap v8map;
+  CUtensorMap ksmap;  // fp32 scales: dims {Hkv, bs, nb}, box {4, G, 1}
+  CUtensorMap vsmap;
+  const int32_t* block_table;
+  int64_t bt_stride, num_blocks;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t T, group, num_q_heads, block_size, seg, split_tokens, max_splits;
+  float scale_log2;
+  float* part_o;
+  float* part_lse;
+  int64_t rows;  // num_reqs * T * Hq
+  int* dev_err;
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// 16 int8 codes -> 16 fp16 integers, exact (byte-permute + one fp16 subtraction per pair).
+__device__ __forceinline__ void widen16_f16(uint4 in, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t u = w[i] ^ 0x80808080u;
+    uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140);
+    uint32_t hi = __byte_perm(u, 0x64646464u, 0x7362);
+    __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+    __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+    o[2 * i] = *reinterpret_cast<uint32_t*>(&hl);
+    o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&hh);
+  }
+}
+
+// Butterfly reduce-scatter: on entry every lane holds 32 column values; on exit lane l holds the
+// reduction over the warp of column l. 31 shuffles.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_columns(float (&v)[kNQ], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float keep = upper ? v[q + o] : v[q];
+      const float send = upper ? v[q] : v[q + o];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[q] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sV16 = smem + kOffV16;
+  uint8_t* sP = smem + kOffP;
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + kTiles);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int r = blockIdx.z;
+  const int seq_len = __ldg(p.seq_lens + r);
+  const int64_t k_begin64 = (int64_t)split * p.split_tokens;
+  if (k_begin64 >= seq_len) return;  // CTA-uniform: split past this request's keys
+  const int k_begin = (int)k_begin64;
+  const int k_end = min(seq_len, k_begin + p.split_tokens);
+  const int n_tiles = (k_end - k_begin + kBN - 1) / kBN;
+  const int prefix = seq_len - p.T;  // query token t sits at position prefix + t
+
+  if (threadIdx.x == 0) {
+    // the last launched split must reach seq_len; keys past max_splits * split_tokens are lost
+    const bool short_grid = split == p.max_splits - 1 && (int64_t)k_begin + p.split_tokens < seq_len;
+    if (short_grid || prefix < 0) record_error(p.dev_err, kErrDeviceBounds);
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_ready, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.st_full[s], 1);
+      mbar_init(&bar.st_free[s], 128);
+    }
+    mbar_init(&bar.kv_ready, 128);
+    mbar_init(&bar.qk_done, 1);
+    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.pv_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (prefix < 0) return;  // CTA-uniform (after the error is noted)
+  if (warp == 2) {
+    tmem_alloc(&bar.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  volatile int* abort = &bar.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------------------- producer
+    const int G = p.seg;
+    const int nseg = kBN / G;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar.q_full, 4 * kQChunk);
+      for (int c = 0; c < 4; ++c)
+        tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T);
+    }
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      uint8_t* stage = smem + kOffStage + st * kStageBytes;
+      if (lane == 0 && j >= 2) mbar_wait(&bar.st_free[st], ((j >> 1) - 1) & 1, abort);
+      __syncwarp();
+      if (*abort) break;
+      const int key0 = k_begin + j * kBN;
+      int blk = -1;
+      if (lane < nseg && key0 + lane * G < k_end) {
+        const int pos = key0 + lane * G;
+        const int col = pos / p.block_size;
+        blk = col < p.max_blocks ? __ldg(p.block_table + (int64_t)r * p.bt_stride + col) : -2;
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) blk = -2;
+      }
+      const uint32_t bad = __ballot_sync(0xffffffffu, blk == -2);
+      const uint32_t nloaded = __popc(__ballot_sync(0xffffffffu, blk >= 0));
+      if (lane == 0) {
+        if (bad) record_error(p.dev_err, kErrDeviceBounds);
+        bar.bad[st] = bad;
+        mbar_arrive_expect_tx(&bar.st_full[st], nloaded * (uint32_t)G * (4u * 128u + 2u * 16u));
+      }
+      __syncwarp();
+      if (blk >= 0) {
+        const int slot = (key0 + lane * G) % p.block_size;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_4d(stage + kStageK8 + c * kChunk8 + lane * G * 128, &p.k8map, &bar.st_full[st], c * 128, kvh,
+                      slot, blk);
+          tma_load_4d(stage + kStageV8 + c * kChunk8 + lane * G * 128, &p.v8map, &bar.st_full[st], c * 128, kvh,
+                      slot, blk);
+        }
+        tma_load_3d(stage + kStageKS + lane * G * 16, &p.ksmap, &bar.st_full[st], (kvh & ~3), slot, blk);
+        tma_load_3d(stage + kStageVS + lane * G * 16, &p.vsmap, &bar.st_full[st], (kvh & ~3), slot, blk);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_f16(128, kNQ, false, false, false);
+      constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
+      const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
+      bool ok = mbar_wait(&bar.q_ready, 0, abort);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (!mbar_wait(&bar.kv_ready, j & 1, abort)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < 16; ++ks)
+          umma_f16_ts(tmem + kColS, tmem + kColK + ks * 8,
+                      smem_desc(q_base + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
+        umma_commit(&bar.qk_done);
+        if (!mbar_wait(&bar.p_full, j & 1, abort)) break;
+        tc_fence_after();
+        for (int hh = 0; hh < 2; ++hh)
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
+                        smem_desc(p_base + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
+                        (j > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&bar.pv_done);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------------------- keys / softmax
+    const int quarter = warp - 4;
+    const int k = quarter * 32 + lane;  // key row of the tile (TMEM lane k)
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int G = p.seg;
+    // Q: bf16 -> fp16 in place (32 rows x 256)
+    bool ok = mbar_wait(&bar.q_full, 0, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const int row = k & 31, c = k >> 5;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        uint4* ptr = reinterpret_cast<uint4*>(sQ + c * kQChunk + row * 128 + q * 16);
+        uint4 v = *ptr;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          w[e] = pack_f16x2(f.x, f.y);
+        }
+        *ptr = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.q_ready);
+    }
+    float m_run[kNQ], l_part[kNQ];
+#pragma unroll
+    for (int q = 0; q < kNQ; ++q) {
+      m_run[q] = -INFINITY;
+      l_part[q] = 0.0f;
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int st = j & 1;
+      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
+      bool got = mbar_wait(&bar.st_full[st], (j >> 1) & 1, abort);
+      if (got && j > 0) got = mbar_wait(&bar.qk_done, (j - 1) & 1, abort) && mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int key = k_begin + j * kBN + k;
+      const bool bad = (bar.bad[st] >> (k / G)) & 1u;
+      const bool in_range = key < k_end;
+      const float ks = (in_range && !bad) ? reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)] : 0.0f;
+      const float vs = (in_range && !bad) ? reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)] : 0.0f;
+      // K row -> fp16 into TMEM lane k; V row -> fp16 into the MN-major V tile
+#pragma unroll 1
+      for (int w4 = 0; w4 < 4; ++w4) {
+        uint32_t kv[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q8 = 4 * (w4 & 1) + i;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageK8 + (w4 >> 1) * kChunk8 + k * 128 +
+                                                          ((q8 ^ (k & 7)) * 16));
+          uint32_t o[8];
+          widen16_f16(v, o);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) kv[8 * i + e] = o[e];
+        }
+        tmem_st_32x32b_x32(tmem + lane_off + kColK + 32 * w4, kv);
+      }
+#pragma unroll 1
+      for (int c8 = 0; c8 < 2; ++c8) {
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageV8 + c8 * kChunk8 + k * 128 +
+                                                          ((q8 ^ (k & 7)) * 16));
+          uint32_t o[8];
+          widen16_f16(v, o);
+          uint8_t* row = sV16 + (2 * c8 + (q8 >> 2)) * kChunk16 + k * 128;
+          const uint32_t piece = 2u * (q8 & 3);
+          *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(row + (((piece + 1) ^ (k & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.st_free[st]);
+      mbar_arrive(&bar.kv_ready);
+      // scores of key k against the 32 query columns
+      got = mbar_wait(&bar.qk_done, j & 1, abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      float s[kNQ];
+      {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + kColS, v);
+        tmem_wait_ld();
+        const float f = p.scale_log2 * ks;
+#pragma unroll
+        for (int q = 0; q < kNQ; ++q) {
+          const int t = q / p.group;
+          const bool vis = in_range && key <= prefix + t;
+          s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
+        }
+      }
+      float red[kNQ];
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) red[q] = s[q];
+      bar.red[st][quarter][lane] = warp_reduce_columns<true>(red, lane);
+      named_bar_sync(1, 128);
+      float alpha[kNQ];
+      bool any_rescale = false;
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const float mt = fmaxf(fmaxf(bar.red[st][0][q], bar.red[st][1][q]), fmaxf(bar.red[st][2][q], bar.red[st][3][q]));
+        alpha[q] = 1.0f;
+        if (m_run[q] == -INFINITY || mt > m_run[q] + kRescaleThreshold) {
+          const float m_new = fmaxf(m_run[q], mt);
+          if (m_new != -INFINITY) {
+            const bool had = m_run[q] != -INFINITY;
+            alpha[q] = had ? ex2_approx(m_run[q] - m_new) : 0.0f;
+            any_rescale |= had;
+            m_run[q] = m_new;
+          }
+        }
+      }
+      // P^T column for key k: p = exp2(s - m) * v_scale, fp16; per-thread column sums
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const float mu = m_run[q] == -INFINITY ? 0.0f : m_run[q];
+        const float e = ex2_approx(s[q] - mu);
+        l_part[q] = l_part[q] * alpha[q] + e;
+        const __half h = __float2half_rn(e * vs);
+        *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = h;
+      }
+      if (any_rescale) {  // identical in every thread: all hold the same running maxima
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * alpha[q]);
+          tmem_st_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+    }
+    // epilogue: column sums, O^T / l, log-sum-exp
+    bool fin = ok && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    fin = __all_sync(0xffffffffu, fin);
+    if (fin) {
+      tc_fence_after();
+      named_bar_sync(1, 128);  // every warp is past its last read of bar.red
+      bar.red[0][quarter][lane] = warp_reduce_columns<false>(l_part, lane);
+      named_bar_sync(1, 128);
+      float inv_l[kNQ];
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const float l = bar.red[0][0][q] + bar.red[0][1][q] + bar.red[0][2][q] + bar.red[0][3][q];
+        inv_l[q] = l > 0.0f ? 1.0f / l : 0.0f;
+        if (k == q) {
+          const int t = q / p.group, hh = q % p.group;
+          const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
+          p.part_lse[(int64_t)split * p.rows + row] =
+              l > 0.0f ? (m_run[q] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+      }
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+        tmem_wait_ld();
+        const int d = hh * 128 + k;
+#pragma unroll
+        for (int q = 0; q < kNQ; ++q) {
+          const int t = q / p.group, h2 = q % p.group;
+          const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + h2;
+          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * inv_l[q];
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && bar.abort) record_error(p.dev_err, kErrTimeout);
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+}  // namespace
+
+}  // namespace pkv
+
+extern "C" size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t num_q_heads, int32_t head_dim,
+                                                  int32_t max_splits) {
+  if (num_tokens <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_splits <= 0) return 0;
+  const size_t rows = (size_t)num_tokens * (size_t)num_q_heads * (size_t)max_splits;
+  const size_t o = (rows * (size_t)head_dim * 4 + 255) & ~(size_t)255;
+  const size_t l = (rows * 4 + 255) & ~(size_t)255;
+  return o + l;
+}
+
+extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                                   const float* k_scale, const float* v_scale, int64_t num_blocks,
+                                                   int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                                   int64_t scale_stride_blk, int64_t scale_stride_tok,
+                                                   const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                                   const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                   int32_t block_size, float softmax_scale, int32_t split_tokens,
+                                                   int32_t max_splits, float* part_o, float* part_lse,
+                                                   int32_t* dev_err, void* stream) {
+  using namespace pkv;
+  clear_error();
+  PKV_UNSUP(head_dim == kD, "spec_verify_attn_partial: head_dim must be 256 (got %d)", head_dim);
+  PKV_ARG(q && k_cache && v_cache && k_scale && v_scale && block_table && seq_lens && part_o && part_lse,
+          "spec_verify_attn_partial: null pointer argument");
+  PKV_ARG(num_reqs >= 0 && T > 0 && num_q_heads > 0 && num_kv_heads > 0 && num_blocks > 0 && block_size > 0 &&
+              max_blocks > 0 && bt_stride >= max_blocks && max_splits > 0 && split_tokens > 0,
+          "spec_verify_attn_partial: bad size argument");
+  PKV_UNSUP(num_q_heads % num_kv_heads == 0, "spec_verify_attn_partial: num_q_heads %% num_kv_heads != 0");
+  const int group = num_q_heads / num_kv_heads;
+  PKV_UNSUP(group * T == kNQ, "spec_verify_attn_partial: T * (num_q_heads / num_kv_heads) must be 32 (got %d)",
+            group * T);
+  PKV_UNSUP(num_kv_heads % 4 == 0, "spec_verify_attn_partial: num_kv_heads must be a multiple of 4");
+  PKV_UNSUP(block_size % 8 == 0, "spec_verify_attn_partial: block_size must be a multiple of 8");
+  PKV_UNSUP(split_tokens % kBN == 0, "spec_verify_attn_partial: split_tokens must be a multiple of 128");
+  PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0 && scale_stride_blk > 0 && scale_stride_tok > 0,
+          "spec_verify_attn_partial: strides must be positive");
+  PKV_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(k_scale) && aligned16(v_scale) &&
+              stride_blk % 16 == 0 && stride_tok % 16 == 0 && stride_head % 16 == 0 && scale_stride_blk % 4 == 0 &&
+              scale_stride_tok % 4 == 0,
+          "spec_verify_attn_partial: pointers and strides must be 16-byte aligned");
+  PKV_ARG(softmax_scale > 0.0f, "spec_verify_attn_partial: softmax_scale must be positive");
+  if (num_reqs == 0) return PKV_OK;
+  Params p{};
+  const int G = gcd_int(block_size, kBN);
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_q_heads, (uint64_t)num_reqs * (uint64_t)T};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)num_q_heads * kD * 2};
+    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)T};
+    pkv_status s = encode_tiled(&p.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, "q");
+    if (s != PKV_OK) return s;
+  }
+  {
+    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
+    const uint64_t strides[3] = {(uint64_t)stride_head, (uint64_t)stride_tok, (uint64_t)stride_blk};
+    const uint32_t box[4] = {128, 1, (uint32_t)G, 1};
+    pkv_status s = encode_tiled(&p.k8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_cache, dims, strides, box, "k_cache");
+    if (s != PKV_OK) return s;
+    s = encode_tiled(&p.v8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v_cache, dims, strides, box, "v_cache");
+    if (s != PKV_OK) return s;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
+    const uint64_t strides[2] = {(uint64_t)scale_stride_tok * 4, (uint64_t)scale_stride_blk * 4};
+    const uint32_t box[3] = {4, (uint32_t)G, 1};
+    pkv_status s = encode_tiled(&p.ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_scale, dims, strides, box, "k_scale",
+                                false);
+    if (s != PKV_OK) return s;
+    s = encode_tiled(&p.vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_scale, dims, strides, box, "v_scale", false);
+    if (s != PKV_OK) return s;
+  }
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks;
+  p.seq_lens = seq_lens;
+  p.T = T;
+  p.group = group;
+  p.num_q_heads = num_q_heads;
+  p.block_size = block_size;
+  p.seg = G;
+  p.split_tokens = split_tokens;
+  p.max_splits = max_splits;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.rows = (int64_t)num_reqs * T * num_q_heads;
+  p.dev_err = dev_err;
+  constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(spec_verify_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    attr = true;
+  }
+  dim3 grid((unsigned)max_splits, (unsigned)num_kv_heads, (unsigned)num_reqs);
+  spec_verify_partial_kernel<<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  return check_launch("spec_verify_attn_partial");
+}

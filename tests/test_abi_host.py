@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI, no GPU needed: libpkv.so builds for sm_103a, loads, exports every
+function include/pkv.h declares, and its argument validation rejects bad calls before anything is
+launched (no CUDA call is reached on these paths)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*PKV_API\s+(?:const\s+)?\w+\s*\*?\s*(pkv_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from paged_kv_cache_int64_gb300 import _build
+    return _build.build()
+
+
+@pytest.fixture(scope="module")
+def pkv(libpath):
+    import paged_kv_cache_int64_gb300 as m
+    return m
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for base in ("kv_int8_stats_quant", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_attn_partial",
+                 "spec_verify_combine"):
+        assert "pkv_" + base in names
+
+
+def test_library_exports_every_declared_symbol(libpath, pkv):
+    names = declared_functions()
+    lib = C.CDLL(libpath)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+    # the Python binding wraps exactly the declared calls
+    assert set(pkv.EXPORTED_SYMBOLS) == set(names)
+    # nothing but the ABI leaks out of the library (hidden visibility)
+    assert not [s for s in exported if s.startswith("_ZN3pkv")]
+
+
+def test_library_targets_sm103a(libpath):
+    from paged_kv_cache_int64_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+
+
+def test_abi_version(pkv):
+    assert pkv.lib.pkv_abi_version() == 1
+
+
+def test_workspace_bytes(pkv):
+    n = pkv.spec_verify_workspace_bytes(256, 16, 256, 10)
+    rows = 256 * 16 * 10
+    assert n >= rows * 256 * 4 + rows * 4 and n % 256 == 0
+    assert pkv.spec_verify_workspace_bytes(0, 16, 256, 10) == 0
+
+
+def _prefill_args(**kw):
+    a = dict(q=16, k=16, v=16, nb=4, sb=16384, st=1024, sh=256, bt=16, bts=1, mb=1, sl=16, qsl=16, R=1, total_q=1,
+             max_q=1, hq=16, hkv=4, d=256, bs=16, scale=0.0625, mode=0, k8=None, k8s=None, max_ctx=0, out=16,
+             err=None, stream=None)
+    a.update(kw)
+    return [a[k] for k in ("q", "k", "v", "nb", "sb", "st", "sh", "bt", "bts", "mb", "sl", "qsl", "R", "total_q",
+                           "max_q", "hq", "hkv", "d", "bs", "scale", "mode", "k8", "k8s", "max_ctx", "out", "err",
+                           "stream")]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=128), 2),                 # head_dim != 256 -> unsupported
+    (dict(q=None), 1),                # null pointer
+    (dict(hq=15), 2),                 # q heads not a multiple of kv heads
+    (dict(bs=20), 2),                 # block_size not a multiple of 8
+    (dict(q=24), 1),                  # misaligned pointer
+    (dict(mode=7), 1),                # unknown qk mode
+    (dict(mode=1), 1),                # int8 mode without k8 / k8_scale
+    (dict(sb=-5), 1),                 # negative stride
+])
+def test_prefill_rejects_bad_arguments(pkv, kw, status):
+    rc = pkv.lib.pkv_paged_prefill_attn(*_prefill_args(**kw))
+    assert rc == status
+    assert pkv.lib.pkv_last_error().decode()
+
+
+def test_verify_rejects_unsupported_geometry(pkv):
+    f = pkv.lib.pkv_spec_verify_attn_partial
+    # T * group = 6 * 4 = 24 != 32
+    rc = f(16, 16, 16, 16, 16, 4, 16384, 1024, 256, 64, 4, 16, 1, 1, 16, 1, 6, 16, 4, 256, 16, 0.1, 128, 2, 16, 16,
+           None, None)
+    assert rc == 2 and "32" in pkv.lib.pkv_last_error().decode()
+    # split_tokens not a multiple of 128
+    rc = f(16, 16, 16, 16, 16, 4, 16384, 1024, 256, 64, 4, 16, 1, 1, 16, 1, 8, 16, 4, 256, 16, 0.1, 100, 2, 16, 16,
+           None, None)
+    assert rc == 2
+
+
+def test_quant_and_dequant_reject_bad_arguments(pkv):
+    rc = pkv.lib.pkv_kv_int8_stats_quant(16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 4, 16, 4, 128, 16, 16, 8,
+                                         None, None)
+    assert rc == 2
+    rc = pkv.lib.pkv_kv_fp8_dequant_dense(16, 16, 4, 16384, 1024, 256, None, 1, 1, 16, 1, 16, 16, 4, 256, 16, 16,
+                                          16, 16, None, None)
+    assert rc == 1
+    rc = pkv.lib.pkv_spec_verify_combine(16, 16, 16, 1, 8, 16, 512, 128, 2, 16, None)
+    assert rc == 2
+
+
+def test_empty_batches_launch_nothing(pkv):
+    # num_reqs == 0 returns before any CUDA call (none is available here)
+    assert pkv.lib.pkv_paged_prefill_attn(*_prefill_args(R=0, total_q=0, max_q=0)) == 0
+    assert pkv.lib.pkv_spec_verify_combine(16, 16, 16, 0, 8, 16, 256, 128, 2, 16, None) == 0

@@ -1,0 +1,385 @@
+"""GPU parity: libpkv's kernels (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bars: bit-exact for the int8 codes / scales and the fp8 -> bf16 dense bytes, and for top-vs-bottom
+pool placement; max-abs error <= 2e-3 (bf16 and fp8 paths, verify) and <= 5e-3 (int8-QK path)
+against the oracle. Outputs are bf16, whose rounding alone is up to 2^-9 relative; cases whose
+outputs exceed 1 in magnitude (early positions, where attention is peaked) add that term.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-3
+TOL_INT8 = 5e-3
+BF16_REL = 2.0 ** -8  # output rounding allowance (one bf16 ulp, relative) for |o| > 1
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_int64_gb300 as m
+    return m
+
+
+from _devsetup import (bf16_to_u16, dev_err, device_meta, device_pool, device_q, device_scale_pool,  # noqa: E402
+                       max_abs)
+
+
+def _close(gpu_bf16_u16, ref, tol):
+    g = W.bf16_bits_to_f32(gpu_bf16_u16).astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert not np.isnan(g).any(), "NaN in GPU output"
+    err = np.abs(g - ref) - BF16_REL * np.maximum(np.abs(ref) - 1.0, 0.0)
+    return float(err.max())
+
+
+# ---------------------------------------------------------------------------------------------
+# A1: int8 per-token-head quantization - bit exact
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bs,seqs,begins", [(16, [300, 97, 1], [0, 13, 0]), (880, [2000, 881], [120, 0])])
+def test_kv_int8_stats_quant_bit_exact(pkv, bs, seqs, begins):
+    p = W.make_problem("q", seed=31, seq_lens=seqs, q_lens=[1] * len(seqs), num_blocks=64, block_size=bs)
+    k = device_pool(p, "k")
+    bt, sl, _ = device_meta(p)
+    max_ctx = max(seqs) + 5
+    pb = torch.tensor(begins, dtype=torch.int32, device="cuda")
+    pe = torch.tensor(seqs, dtype=torch.int32, device="cuda")
+    k8 = torch.zeros((p.num_reqs, max_ctx, 4, 256), dtype=torch.int8, device="cuda")
+    ks = torch.zeros((p.num_reqs, max_ctx, 4), dtype=torch.float32, device="cuda")
+    err = dev_err()
+    pkv.kv_int8_stats_quant(k, bt, pb, pe, max(s - b for s, b in zip(seqs, begins)), k8, ks, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rk8, rks = oracle.kv_int8_stats_quant(p.pool_numpy("k"), p.block_table(fill=0), begins, seqs, bs, max_ctx)
+    assert np.array_equal(k8.cpu().numpy(), rk8)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), rks.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------------------------
+# A4: fp8 -> dense bf16 - bit exact
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bs,scale", [(16, 0.5), (880, 0.3)])
+def test_kv_fp8_dequant_dense_bit_exact(pkv, bs, scale):
+    p = W.make_problem("f", seed=41, seq_lens=[1500, 77], q_lens=[1, 1], num_blocks=40, block_size=bs,
+                       kv_dtype="e4m3")
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, sl, _ = device_meta(p)
+    max_seq = 1600
+    kd = torch.zeros((p.num_reqs, max_seq, 4, 256), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    ksc = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    vsc = torch.tensor([scale * 2], dtype=torch.float32, device="cuda")
+    err = dev_err()
+    pkv.kv_fp8_dequant_dense(k, v, bt, sl, ksc, vsc, kd, vd, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rk, rv = oracle.kv_fp8_dequant_dense(p.pool_numpy("k"), p.pool_numpy("v"), p.block_table(fill=0), p.seq_lens,
+                                         max_seq, scale, scale * 2)
+    assert np.array_equal(bf16_to_u16(kd), rk)
+    assert np.array_equal(bf16_to_u16(vd), rv)
+
+
+# ---------------------------------------------------------------------------------------------
+# A3: paged prefill attention
+# ---------------------------------------------------------------------------------------------
+
+def _run_prefill(pkv, p, mode=0, k_pool=None, v_pool=None):
+    k = device_pool(p, "k") if k_pool is None else k_pool
+    v = device_pool(p, "v") if v_pool is None else v_pool
+    bt, sl, qsl = device_meta(p)
+    q = device_q(p)
+    out = torch.full_like(q, float("nan"))
+    err = dev_err()
+    k8 = ks = None
+    if mode == 1:
+        max_ctx = int(p.seq_lens.max())
+        k8 = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads, 256), dtype=torch.int8, device="cuda")
+        ks = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads), dtype=torch.float32, device="cuda")
+        pb = torch.zeros(p.num_reqs, dtype=torch.int32, device="cuda")
+        pkv.kv_int8_stats_quant(k, bt, pb, sl, max_ctx, k8, ks, dev_err=err)
+    max_q = max(r.q_len for r in p.requests)
+    pkv.paged_prefill_attn(q, None if mode == 1 else k, v, bt, sl, qsl, max_q, p.softmax_scale, out,
+                           qk_mode=mode, k8=k8, k8_scale=ks, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device status {err.item()}"
+    return bf16_to_u16(out), (k8, ks)
+
+
+def _oracle_prefill(p, mode=0, k8=None, ks=None, tok_begin=0, tok_end=None):
+    kp, vp = p.pool_numpy("k"), p.pool_numpy("v")
+    if mode == 1 and k8 is None:
+        k8, ks = oracle.kv_int8_stats_quant(kp, p.block_table(fill=0), [0] * p.num_reqs, p.seq_lens, p.block_size,
+                                            int(p.seq_lens.max()))
+    return oracle.paged_prefill_attn(p.q, kp, vp, p.block_table(fill=0), p.seq_lens, p.query_start_loc,
+                                     p.num_q_heads, p.softmax_scale, qk_mode=mode, k8=k8, k8_scale=ks,
+                                     tok_begin=tok_begin, tok_end=tok_end)
+
+
+def test_prefill_tiny_config_bf16(pkv):
+    """1 request, context 512, last 128-query chunk, 16/4 heads, D 256, bs 16, permuted 64-block pool."""
+    p = W.tiny_bf16()
+    got, _ = _run_prefill(pkv, p)
+    ref = _oracle_prefill(p)
+    assert _close(got, ref, TOL_BF16) <= TOL_BF16
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("case", ["ragged", "gqa6", "from_scratch", "bs880"])
+def test_prefill_ragged_cases(pkv, mode, case):
+    if case == "ragged":     # several requests, q_len and seq_len off every tile boundary
+        p = W.make_problem("r", seed=5, seq_lens=[700, 129, 300, 1], q_lens=[300, 129, 1, 1], num_blocks=80,
+                           block_size=16)
+    elif case == "gqa6":     # the pages' 24 query / 4 KV heads
+        p = W.make_problem("g", seed=6, seq_lens=[517, 260], q_lens=[200, 133], num_blocks=64, block_size=16,
+                           num_q_heads=24, num_kv_heads=4)
+    elif case == "from_scratch":  # a first chunk: q_len == seq_len, queries from position 0
+        p = W.make_problem("s", seed=7, seq_lens=[333], q_lens=[333], num_blocks=32, block_size=16)
+    else:                    # block 880, tiles straddle blocks in 16-key segments
+        p = W.make_problem("b", seed=8, seq_lens=[2000, 1000], q_lens=[300, 1000], num_blocks=40, block_size=880)
+    got, _ = _run_prefill(pkv, p, mode)
+    ref = _oracle_prefill(p, mode)
+    assert _close(got, ref, 0) <= (TOL_INT8 if mode else TOL_BF16)
+
+
+def test_prefill_block_size_dense_scratch(pkv):
+    """block_size == max_seq with an identity table: the dense-scratch addressing of the fp8 path."""
+    p = W.make_problem("d", seed=9, seq_lens=[3000, 2500], q_lens=[256, 700], num_blocks=2, block_size=4096,
+                       placement="explicit", block_lists=[[0], [1]])
+    got, _ = _run_prefill(pkv, p)
+    assert _close(got, _oracle_prefill(p), 0) <= TOL_BF16
+
+
+@pytest.fixture(scope="module")
+def bigpool_gpu(pkv):
+    """configs: 2,600-block bf16 pool (bs 880, 4.69 GB per K or V), 20,000-token request on blocks
+    2577-2599 and on 0-22 with identical bytes; the last 2,048-token chunk."""
+    out = {}
+    for top in (True, False):
+        p = W.bigpool(top=top)
+        k, v = device_pool(p, "k"), device_pool(p, "v")
+        for mode in (0, 1):
+            out[(top, mode)], _ = _run_prefill(pkv, p, mode, k_pool=k, v_pool=v)
+        del k, v
+        torch.cuda.empty_cache()
+        out[("p", top)] = p
+    return out
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bigpool_top_equals_bottom_bit_exact(bigpool_gpu, mode):
+    top, bot = bigpool_gpu[(True, mode)], bigpool_gpu[(False, mode)]
+    assert np.isfinite(W.bf16_bits_to_f32(top)).all()
+    assert np.array_equal(top, bot)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bigpool_sampled_rows_vs_oracle(bigpool_gpu, mode):
+    p = bigpool_gpu[("p", True)]
+    got = bigpool_gpu[(True, mode)]
+    worst = 0.0
+    for t in (0, 1, 127, 128, 1000, 2047):
+        ref = _oracle_prefill(p, mode, tok_begin=t, tok_end=t + 1)
+        worst = max(worst, _close(got[t:t + 1], ref, 0))
+    assert worst <= (TOL_INT8 if mode else TOL_BF16)
+
+
+def test_int8_prefill_chunked_context(pkv):
+    """int8-QK prefill of a 24,576-token context in 2,048-token chunks over a 2,600-block pool
+    (bs 880, random table): every chunk quantizes its new K rows (A1) then attends (A3); sampled rows
+    of the first, a middle and the last chunk against the oracle."""
+    ctx, bs = 24576, 880
+    p = W.make_problem("i8", seed=33, seq_lens=[ctx], q_lens=[ctx], num_blocks=2600, block_size=bs)
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, _, _ = device_meta(p)
+    q_all = device_q(p)
+    k8 = torch.zeros((1, ctx, 4, 256), dtype=torch.int8, device="cuda")
+    ks = torch.zeros((1, ctx, 4), dtype=torch.float32, device="cuda")
+    err = dev_err()
+    outs = {}
+    sched = W.chunk_schedule(ctx)
+    for ci, (L, ql) in enumerate(sched):
+        sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+        pb = torch.tensor([L - ql], dtype=torch.int32, device="cuda")
+        qsl = torch.tensor([0, ql], dtype=torch.int32, device="cuda")
+        pkv.kv_int8_stats_quant(k, bt, pb, sl, ql, k8, ks, dev_err=err)
+        q = q_all[L - ql:L].contiguous()
+        out = torch.empty_like(q)
+        pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, ql, p.softmax_scale, out, qk_mode=1, k8=k8, k8_scale=ks,
+                               dev_err=err)
+        if ci in (0, len(sched) // 2, len(sched) - 1):
+            outs[ci] = bf16_to_u16(out)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    kp, vp = p.pool_numpy("k"), p.pool_numpy("v")
+    rk8, rks = oracle.kv_int8_stats_quant(kp, p.block_table(fill=0), [0], [ctx], bs, ctx)
+    assert np.array_equal(k8.cpu().numpy(), rk8)
+    worst = 0.0
+    for ci, got in outs.items():
+        L, ql = sched[ci]
+        for t in (0, 777, ql - 1):
+            ref = oracle.paged_prefill_attn(p.q, kp, vp, p.block_table(fill=0), [L], [0, L], p.num_q_heads,
+                                            p.softmax_scale, qk_mode=1, k8=rk8, k8_scale=rks,
+                                            tok_begin=L - ql + t, tok_end=L - ql + t + 1)
+            worst = max(worst, _close(got[t:t + 1], ref, 0))
+    assert worst <= TOL_INT8
+
+
+def test_fp8_prefill_through_dense_scratch(pkv):
+    """fp8 e4m3 KV (values N(0,1) * 0.5 as e4m3 codes of N(0,1) with per-tensor scale 0.5), 32,768-token
+    context; per 2,048-token chunk: dequantize [0, seq_len) to the dense bf16 scratch (identity table,
+    block_size = max_seq), then bf16 attention on it. Checks the last chunk."""
+    ctx = 32768
+    p = W.make_problem("f8", seed=44, seq_lens=[ctx], q_lens=[2048], num_blocks=200, block_size=880,
+                       kv_dtype="e4m3")
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, sl, qsl = device_meta(p)
+    scale = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    kd = torch.zeros((1, ctx, 4, 256), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    err = dev_err()
+    pkv.kv_fp8_dequant_dense(k, v, bt, sl, scale, scale, kd, vd, dev_err=err)
+    ident = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    q = device_q(p)
+    out = torch.empty_like(q)
+    pkv.paged_prefill_attn(q, kd, vd, ident, sl, qsl, 2048, p.softmax_scale, out, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rk, rv = oracle.kv_fp8_dequant_dense(p.pool_numpy("k"), p.pool_numpy("v"), p.block_table(fill=0), [ctx], ctx,
+                                         0.5, 0.5)
+    assert np.array_equal(bf16_to_u16(kd), rk) and np.array_equal(bf16_to_u16(vd), rv)
+    got = bf16_to_u16(out)
+    worst = 0.0
+    for t in (0, 1023, 2047):
+        ref = oracle.paged_prefill_attn(p.q, rk.reshape(1, ctx, 4, 256), rv.reshape(1, ctx, 4, 256),
+                                        np.zeros((1, 1), np.int32), [ctx], [0, 2048], 16, p.softmax_scale,
+                                        tok_begin=t, tok_end=t + 1)
+        worst = max(worst, _close(got[t:t + 1], ref, 0))
+    assert worst <= TOL_BF16
+
+
+# ---------------------------------------------------------------------------------------------
+# A5 / A6: speculative verify
+# ---------------------------------------------------------------------------------------------
+
+def _run_verify(pkv, p, split, T=8, k_pool=None, v_pool=None):
+    k = device_pool(p, "k") if k_pool is None else k_pool
+    v = device_pool(p, "v") if v_pool is None else v_pool
+    ksp, vsp = device_scale_pool(p, "k"), device_scale_pool(p, "v")
+    bt, sl, _ = device_meta(p)
+    q = device_q(p)
+    S = pkv.splits_needed(int(p.seq_lens.max()), split)
+    po = torch.full((S, q.shape[0], q.shape[1], 256), float("nan"), dtype=torch.float32, device="cuda")
+    pl = torch.full((S, q.shape[0], q.shape[1]), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full_like(q, float("nan"))
+    err = dev_err()
+    pkv.spec_verify_attn_partial(q, k, v, ksp, vsp, bt, sl, T, p.softmax_scale, split, po, pl, dev_err=err)
+    pkv.spec_verify_combine(po, pl, sl, T, split, out)
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device status {err.item()}"
+    return bf16_to_u16(out), po.cpu().numpy(), pl.cpu().numpy()
+
+
+def _verify_oracle_args(p):
+    return (p.q, p.pool_numpy("k"), p.pool_numpy("v"), p.scale_pool_numpy("k"), p.scale_pool_numpy("v"),
+            p.block_table(fill=0), p.seq_lens)
+
+
+@pytest.mark.parametrize("split", [128, 512])
+def test_verify_partials_and_combine(pkv, split):
+    T = 8
+    p = W.make_problem("v", seed=51, seq_lens=[L + T for L in (100, 1000, 4000, 129)], q_lens=[T] * 4,
+                       num_blocks=80, block_size=80, kv_dtype="int8",
+                       softmax_scale=1.0 / 16.0)
+    got, po, pl = _run_verify(pkv, p, split, T)
+    args = _verify_oracle_args(p)
+    ref = oracle.spec_verify_attn(*args, T, p.num_q_heads, p.softmax_scale)
+    assert _close(got, ref, 0) <= TOL_BF16
+    S = po.shape[0]
+    rpo, rpl = oracle.spec_verify_partial(*args, T, p.num_q_heads, p.softmax_scale, split, S)
+    for r, L in enumerate(p.seq_lens):
+        ns = math.ceil(L / split)
+        rows = slice(r * T, (r + 1) * T)
+        assert max_abs(po[:ns, rows], rpo[:ns, rows]) <= 1e-3
+        a, b = pl[:ns, rows], rpl[:ns, rows]
+        assert np.array_equal(np.isneginf(a), np.isneginf(b))
+        fin = np.isfinite(b)
+        assert max_abs(a[fin], b[fin]) <= 1e-3
+
+
+def test_verify_bigpool_top_equals_bottom(pkv):
+    """int8 per-token-head cache, 2,600-block pool (bs 880), request of L = 20,000 + 8 tokens on the top
+    blocks and on the bottom blocks with identical bytes: bit-identical outputs, and the oracle."""
+    T = 8
+    outs = {}
+    for top in (True, False):
+        nb = (20000 + T + 879) // 880
+        first = 2600 - nb if top else 0
+        p = W.make_problem("vb", seed=61, seq_lens=[20000 + T], q_lens=[T], num_blocks=2600, block_size=880,
+                           kv_dtype="int8", placement="explicit", block_lists=[np.arange(first, first + nb)],
+                           softmax_scale=1.0 / 16.0)
+        outs[top], _, _ = _run_verify(pkv, p, 2048, T)
+    assert np.array_equal(outs[True], outs[False])
+    ref = oracle.spec_verify_attn(*_verify_oracle_args(p), T, p.num_q_heads, p.softmax_scale)
+    assert _close(outs[True], ref, 0) <= TOL_BF16
+
+
+def test_verify_batch_config_sampled(pkv):
+    """32 requests, lognormal prefixes 4k-80k (median 16k), T = 8, int8 KV, bs 880, distinct blocks;
+    four requests checked against the oracle."""
+    T = 8
+    p = W.verify_batch()
+    got, _, _ = _run_verify(pkv, p, 2048, T)
+    args = _verify_oracle_args(p)
+    worst = 0.0
+    for r in (0, 7, 19, 31):
+        ref = oracle.spec_verify_attn(*args, T, p.num_q_heads, p.softmax_scale, req_begin=r, req_end=r + 1)
+        worst = max(worst, _close(got[r * T:(r + 1) * T], ref[r * T:(r + 1) * T], 0))
+    assert worst <= TOL_BF16
+
+
+# ---------------------------------------------------------------------------------------------
+# boundary behaviour
+# ---------------------------------------------------------------------------------------------
+
+def test_empty_batch_is_a_no_op(pkv):
+    q = torch.zeros((0, 16, 256), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((4, 16, 4, 256), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((0, 1), dtype=torch.int32, device="cuda")
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.paged_prefill_attn(q, k, k, torch.zeros((1, 1), dtype=torch.int32, device="cuda"), z, torch.zeros(2, dtype=torch.int32, device="cuda"),
+                           0, 0.0625, q)
+    del bt
+
+
+def test_unsupported_head_dim_is_rejected(pkv):
+    q = torch.zeros((4, 16, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((4, 16, 4, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    one = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_prefill_attn(q, k, k, bt, one, torch.tensor([0, 1], dtype=torch.int32, device="cuda"), 1, 0.1, q)
+    assert e.value.status == pkv.PKV_ERR_UNSUPPORTED
+
+
+def test_out_of_range_block_id_is_reported_not_read(pkv):
+    p = W.make_problem("bad", seed=71, seq_lens=[200], q_lens=[50], num_blocks=16, block_size=16)
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, sl, qsl = device_meta(p)
+    bt[0, 3] = 16  # == num_blocks: one past the pool
+    q = device_q(p)
+    out = torch.empty_like(q)
+    err = dev_err()
+    pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, 50, p.softmax_scale, out, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == pkv.PKV_ERR_DEVICE_BOUNDS
+    assert np.isfinite(W.bf16_bits_to_f32(bf16_to_u16(out))).all()

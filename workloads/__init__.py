@@ -2,7 +2,7 @@
 
 This module is shared by the oracle tests, the GPU tests and the bench, and it
 holds none of the attention method's arithmetic: it only draws random numbers
-(SplitMix64 + Box-Muller), converts them to the storage dtypes with torch's CPU
+(numpy's seeded PCG64 normals, SplitMix64 keys), converts them to the storage dtypes with torch's CPU
 casts (bf16 bits, e4m3 bytes), builds seeded block tables (permutations) and
 request lengths, and places per-token rows into a pool at the block/slot that a
 block table names (fixture construction, not the attention gather).
@@ -34,20 +34,13 @@ def splitmix64(seed: int, n: int) -> np.ndarray:
 
 
 def uniform01(seed: int, n: int) -> np.ndarray:
-    """Uniform doubles in (0, 1] with 53 random bits."""
+    """Uniform doubles in (0, 1] with 53 random bits (SplitMix64)."""
     return ((splitmix64(seed, n) >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
 
 
 def normal(seed: int, n: int) -> np.ndarray:
-    """n standard normal doubles by the Box-Muller transform (Box & Muller, 1958)."""
-    m = (n + 1) // 2
-    u = uniform01(seed, 2 * m)
-    r = np.sqrt(-2.0 * np.log(u[0::2]))
-    th = (2.0 * math.pi) * u[1::2]
-    z = np.empty(2 * m, dtype=np.float64)
-    z[0::2] = r * np.cos(th)
-    z[1::2] = r * np.sin(th)
-    return z[:n]
+    """n standard normal float32 values from numpy's seeded PCG64 generator."""
+    return np.random.Generator(np.random.PCG64(seed & 0xFFFFFFFFFFFFFFFF)).standard_normal(n, dtype=np.float32)
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -77,12 +70,16 @@ def permutation(seed: int, n: int) -> np.ndarray:
     return np.argsort(splitmix64(seed, n), kind="stable").astype(np.int64)
 
 
-def int8_codes(seed: int, shape, spread: float = 40.0) -> np.ndarray:
-    """Random int8 codes in [-127, 127], rounded N(0, spread^2): the value mix of a
-    symmetric per-token-head int8 cache without running any quantizer."""
+def int8_codes(seed: int, shape) -> np.ndarray:
+    """Random int8 codes in [-127, 127] with a triangular (sum of two uniforms) distribution, the
+    centred value mix of a symmetric per-token-head int8 cache, drawn without running a quantizer."""
     n = int(np.prod(shape))
-    z = np.clip(np.rint(normal(seed, n) * spread), -127, 127)
-    return z.astype(np.int8).reshape(shape)
+    g = np.random.Generator(np.random.PCG64(seed & 0xFFFFFFFFFFFFFFFF))
+    u = np.frombuffer(g.bytes(2 * n), dtype=np.uint8)
+    a = (u[:n] >> 1).astype(np.int16)
+    a += u[n:] >> 1
+    a -= 127
+    return a.astype(np.int8).reshape(shape)
 
 
 def positive_scales(seed: int, shape, lo: float = 0.02, hi: float = 0.03) -> np.ndarray:
@@ -92,7 +89,7 @@ def positive_scales(seed: int, shape, lo: float = 0.02, hi: float = 0.03) -> np.
 
 
 def lognormal_lengths(seed: int, n: int, median: float, sigma: float, lo: int, hi: int) -> np.ndarray:
-    z = normal(seed, n)
+    z = normal(seed, n).astype(np.float64)
     return np.clip(np.rint(median * np.exp(sigma * z)), lo, hi).astype(np.int64)
 
 
