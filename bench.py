@@ -265,11 +265,7 @@ def run_gpu(args):
                 per_kernel.setdefault(name, []).append(x.elapsed_time(y))
         barrier()
         wall = time.perf_counter() - t_wall
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
 
     # end-to-end through the public API from pinned host memory
     e2e = run_e2e(torch, pkv, wl, args, dev)
@@ -298,7 +294,7 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": dominant,
                 "peak_source": peaks["source"]}
-    value = world * wl.TOKENS_PER_STEP * args.steps / (total_ms * 1e-3)
+    value = whole_job_value(wl.TOKENS_PER_STEP, args.steps, world, total_ms)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
@@ -329,6 +325,22 @@ def run_gpu(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The slowest rank's timing (every rank holds its own replica of the workload)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_step: int, steps: int, world: int, max_total_ms: float) -> float:
+    """Weak scaling: all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_step * steps / (max_total_ms * 1e-3)
 
 
 def _gbs(nbytes, ms, peaks):
@@ -514,6 +526,65 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_ncu_case(args):
+    """A small, self-contained case of one kernel for profiler capture (not a bench line): the big-pool
+    request (20,000 tokens, last 2,048-token chunk) in a 64-block pool (the request's 23 blocks at its
+    top), or the 32-request verify batch, launched `--steps` times after `--warmup` launches."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    import paged_kv_cache_int64_gb300 as pkv
+    from _devsetup import device_meta, device_pool, device_q, device_scale_pool
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    case = args.ncu_case
+    if case == "verify":
+        p = W.verify_batch()
+        k, v = device_pool(p, "k"), device_pool(p, "v")
+        ks, vs = device_scale_pool(p, "k"), device_scale_pool(p, "v")
+        bt, sl, _ = device_meta(p)
+        q = device_q(p)
+        S = pkv.splits_needed(int(p.seq_lens.max()), SPLIT)
+        po = torch.empty((S, q.shape[0], HQ, D), dtype=torch.float32, device=dev)
+        pl = torch.empty((S, q.shape[0], HQ), dtype=torch.float32, device=dev)
+        out = torch.empty_like(q)
+
+        def fn():
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sl, T_VERIFY, p.softmax_scale, SPLIT, po, pl)
+            pkv.spec_verify_combine(po, pl, sl, T_VERIFY, SPLIT, out)
+    else:
+        nb = 64
+        kv_dtype = "e4m3" if case == "fp8_dequant" else "bf16"
+        p = W.make_problem("ncu", seed=2, seq_lens=[L], q_lens=[CHUNK], num_blocks=nb, block_size=BS,
+                           kv_dtype=kv_dtype, placement="explicit", block_lists=[np.arange(nb - 23, nb)],
+                           softmax_scale=1.0 / 16.0)
+        k, v = device_pool(p, "k"), device_pool(p, "v")
+        bt, sl, qsl = device_meta(p)
+        q = device_q(p)
+        out = torch.empty_like(q)
+        k8 = torch.zeros((1, L, HKV, D), dtype=torch.int8, device=dev)
+        k8s = torch.zeros((1, L, HKV), dtype=torch.float32, device=dev)
+        zero = torch.zeros(1, dtype=torch.int32, device=dev)
+        pb = torch.tensor([L - CHUNK], dtype=torch.int32, device=dev)
+        if case == "prefill_int8":
+            pkv.kv_int8_stats_quant(k, bt, zero, sl, L, k8, k8s)
+        kd = torch.empty((1, L, HKV, D), dtype=torch.bfloat16, device=dev)
+        vd = torch.empty_like(kd)
+        sc = torch.tensor([0.5], dtype=torch.float32, device=dev)
+        fns = {
+            "prefill_bf16": lambda: pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, CHUNK, p.softmax_scale, out),
+            "prefill_int8": lambda: pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, CHUNK, p.softmax_scale, out,
+                                                           qk_mode=pkv.PKV_QK_INT8, k8=k8, k8_scale=k8s),
+            "int8_quant": lambda: pkv.kv_int8_stats_quant(k, bt, pb, sl, CHUNK, k8, k8s),
+            "fp8_dequant": lambda: pkv.kv_fp8_dequant_dense(k, v, bt, sl, sc, sc, kd, vd),
+        }
+        fn = fns[case]
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_case": case, "launches": args.warmup + args.steps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -523,7 +594,12 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=0, help="query tokens per prefill pass (0: one per core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-batch", action="store_true")
+    ap.add_argument("--ncu-case", choices=["prefill_bf16", "prefill_int8", "int8_quant", "fp8_dequant", "verify"],
+                    help="run one kernel on a small case for profiler capture instead of the bench")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

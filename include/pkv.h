@@ -190,6 +190,25 @@ PKV_API pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_c
                                         int32_t* dev_err, void* stream);
 
 /*
+ * spec_verify_attn_partial_fp8 - the same split-KV verify over a per-tensor fp8 e4m3 cache
+ * [P91: the fp8 arm of the big-pool verify test ("k_descale" argument) and the split-KV verify on
+ * the per-tensor fp8 KV cache that the review names].
+ * k = float(e4m3(k_fp8[...])) * (*k_descale), v = float(e4m3(v_fp8[...])) * (*v_descale), one
+ * descale per tensor (device scalars); everything else (layouts, splits, partials, requirements
+ * other than the scale arrays) as pkv_spec_verify_attn_partial; merge with pkv_spec_verify_combine.
+ */
+PKV_API pkv_status pkv_spec_verify_attn_partial_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
+                                                    const float* k_descale, const float* v_descale,
+                                                    int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                                    int64_t stride_head, const int32_t* block_table,
+                                                    int64_t bt_stride, int32_t max_blocks,
+                                                    const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                                    int32_t num_q_heads, int32_t num_kv_heads,
+                                                    int32_t head_dim, int32_t block_size, float softmax_scale,
+                                                    int32_t split_tokens, int32_t max_splits, float* part_o,
+                                                    float* part_lse, int32_t* dev_err, void* stream);
+
+/*
  * spec_verify_combine - log-sum-exp merge of the split-KV partials [P91, split-KV verify].
  *   LSE = ln sum_s exp(part_lse[s]);  out = sum_s exp(part_lse[s] - LSE) part_o[s]
  * over the ceil(seq_lens[r] / split_tokens) splits of each request; out bf16

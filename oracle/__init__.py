@@ -66,11 +66,15 @@ def lib():
                                               vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, i32, i32,
                                               vp, vp]
         L.orc_spec_verify_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+        L.orc_spec_verify_attn_fp8.argtypes = [vp, vp, vp, f32, f32, i64, i64, i64, i64, vp, i64, vp, i32, i32,
+                                               i32, i32, i32, i32, f32, i32, i32, vp]
+        L.orc_spec_verify_partial_fp8.argtypes = [vp, vp, vp, f32, f32, i64, i64, i64, i64, vp, i64, vp, i32,
+                                                  i32, i32, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp]
         for name in ("orc_quant_row_i8", "orc_set_offset_mode_for_testing"):
             getattr(L, name).restype = None
         for name in ("orc_kv_int8_stats_quant", "orc_kv_fp8_dequant_dense", "orc_paged_prefill_attn",
                      "orc_dense_attn", "orc_spec_verify_attn", "orc_spec_verify_partial",
-                     "orc_spec_verify_combine"):
+                     "orc_spec_verify_combine", "orc_spec_verify_attn_fp8", "orc_spec_verify_partial_fp8"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -239,3 +243,41 @@ def spec_verify_combine(part_o, part_lse, seq_lens, T, split_tokens):
                                        max_splits, _p(out))
     _check(rc, "spec_verify_combine")
     return out
+
+
+# ---- fp8 verify (per-tensor e4m3 cache) ------------------------------------------------------
+
+def spec_verify_attn_fp8(q, k_pool, v_pool, k_descale, v_descale, block_table, seq_lens, T, num_q_heads,
+                         softmax_scale, req_begin=0, req_end=None):
+    q = _c(q, np.uint16)
+    k_pool, v_pool = _c(k_pool, np.uint8), _c(v_pool, np.uint8)
+    nb, bs, hkv, d = k_pool.shape
+    bt, sl = _c(block_table, np.int32), _c(seq_lens, np.int32)
+    R = bt.shape[0]
+    if req_end is None:
+        req_end = R
+    out = np.zeros((R * T, num_q_heads, d), dtype=np.float32)
+    rc = lib().orc_spec_verify_attn_fp8(_p(q), _p(k_pool), _p(v_pool), float(k_descale), float(v_descale), nb,
+                                        bs * hkv * d, hkv * d, d, _p(bt), bt.shape[1], _p(sl), R, T, num_q_heads,
+                                        hkv, d, bs, float(softmax_scale), req_begin, req_end, _p(out))
+    _check(rc, "spec_verify_attn_fp8")
+    return out
+
+
+def spec_verify_partial_fp8(q, k_pool, v_pool, k_descale, v_descale, block_table, seq_lens, T, num_q_heads,
+                            softmax_scale, split_tokens, max_splits, req_begin=0, req_end=None):
+    q = _c(q, np.uint16)
+    k_pool, v_pool = _c(k_pool, np.uint8), _c(v_pool, np.uint8)
+    nb, bs, hkv, d = k_pool.shape
+    bt, sl = _c(block_table, np.int32), _c(seq_lens, np.int32)
+    R = bt.shape[0]
+    if req_end is None:
+        req_end = R
+    part_o = np.zeros((max_splits, R * T, num_q_heads, d), dtype=np.float32)
+    part_lse = np.full((max_splits, R * T, num_q_heads), -np.inf, dtype=np.float32)
+    rc = lib().orc_spec_verify_partial_fp8(_p(q), _p(k_pool), _p(v_pool), float(k_descale), float(v_descale), nb,
+                                           bs * hkv * d, hkv * d, d, _p(bt), bt.shape[1], _p(sl), R, T,
+                                           num_q_heads, hkv, d, bs, float(softmax_scale), split_tokens, max_splits,
+                                           req_begin, req_end, _p(part_o), _p(part_lse))
+    _check(rc, "spec_verify_partial_fp8")
+    return part_o, part_lse

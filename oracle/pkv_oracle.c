@@ -230,11 +230,12 @@ static int find_request(const int32_t* qsl, int num_reqs, int64_t t) {
   return -1;
 }
 
-/* Softmax-weighted sum for one query row, given its scores s[0..n) and a value fetcher.
+/* Softmax-weighted sum for one query row, given its scores s[0..n) and a fetcher that gathers the
+ * value row of key j (through the block table) into a buffer of head_dim doubles.
  * o = sum_j exp(s_j - m) v_j / sum_j exp(s_j - m), m = max_j s_j; two passes, ascending j. */
-typedef double (*value_fn)(void* ctx, int64_t j, int d);
+typedef void (*row_fn)(void* ctx, int64_t j, double* row, int head_dim);
 
-static void softmax_pv(const double* s, int64_t n, int head_dim, value_fn val, void* ctx,
+static void softmax_pv(const double* s, int64_t n, int head_dim, row_fn fetch, void* ctx,
                        float* out, double* lse_out) {
   double m = -INFINITY;
   int any_nan = 0;
@@ -248,16 +249,19 @@ static void softmax_pv(const double* s, int64_t n, int head_dim, value_fn val, v
     return;
   }
   double* acc = (double*)calloc((size_t)head_dim, sizeof(double));
+  double* v = (double*)malloc(sizeof(double) * (size_t)head_dim);
   double l = 0.0;
   if (n > 0 && m != -INFINITY) {
     for (int64_t j = 0; j < n; ++j) {
       double w = exp(s[j] - m);
       l += w;
-      for (int d = 0; d < head_dim; ++d) acc[d] += w * val(ctx, j, d);
+      fetch(ctx, j, v, head_dim);
+      for (int d = 0; d < head_dim; ++d) acc[d] += w * v[d];
     }
   }
   for (int d = 0; d < head_dim; ++d) out[d] = l > 0.0 ? (float)(acc[d] / l) : 0.0f;
   if (lse_out) *lse_out = l > 0.0 ? m + log(l) : -INFINITY;
+  free(v);
   free(acc);
 }
 
@@ -273,11 +277,11 @@ typedef struct {
   uint16_t nan_bits;
 } vctx;
 
-static double v_bf16(void* c, int64_t j, int d) {
+static void v_bf16(void* c, int64_t j, double* row, int head_dim) {
   vctx* x = (vctx*)c;
   int64_t off = paged_offset(x->v, x->r, x->base_pos + j, x->h, x->bad);
-  if (off < 0) return NAN;
-  return (double)orc_bf16_to_f32(x->bf16[off + d]);
+  for (int d = 0; d < head_dim; ++d)
+    row[d] = off < 0 ? NAN : (double)orc_bf16_to_f32(x->bf16[off + d]);
 }
 
 /* Int8 per-token-head value: v8 * vs, the scale read through the same block id [P91]. */
@@ -290,13 +294,12 @@ static double scale_of(const paged_view* v, const float* sc, int64_t sc_blk, int
   return (double)sc[off];
 }
 
-static double v_int8(void* c, int64_t j, int d) {
+static void v_int8(void* c, int64_t j, double* row, int head_dim) {
   vctx* x = (vctx*)c;
   int64_t pos = x->base_pos + j;
   int64_t off = paged_offset(x->v, x->r, pos, x->h, x->bad);
-  if (off < 0) return NAN;
-  double s = scale_of(x->v, x->vscale, x->sc_blk, x->sc_tok, x->r, pos, x->h, x->bad);
-  return (double)x->i8[off + d] * s;
+  double sc = off < 0 ? NAN : scale_of(x->v, x->vscale, x->sc_blk, x->sc_tok, x->r, pos, x->h, x->bad);
+  for (int d = 0; d < head_dim; ++d) row[d] = off < 0 ? NAN : (double)x->i8[off + d] * sc;
 }
 
 /* Prefill attention for global query tokens [tok_begin, tok_end), all query heads.
@@ -493,6 +496,119 @@ int orc_spec_verify_partial(const uint16_t* q, const int8_t* k_cache, const int8
           vctx c = {&vv, r, kvh, j0, NULL, v_cache, v_scale, scale_stride_blk, scale_stride_tok, &bad, 0};
           double lse;
           softmax_pv(s, n, head_dim, v_int8, &c, part_o + (sp * rows + row) * head_dim, &lse);
+          part_lse[sp * rows + row] = (float)lse;
+        }
+      }
+    }
+  }
+  free(s);
+  return bad ? ORC_ERR_BOUNDS : ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* Verify over a per-tensor fp8 e4m3 cache [P91 description and review: the fp8 arm of the    */
+/* big-pool test, "k_descale"; the split-KV verify on the per-tensor fp8 KV cache]             */
+/* k = e4m3(byte) * k_descale, v = e4m3(byte) * v_descale; otherwise as the int8 verify.      */
+/* ---------------------------------------------------------------------------------------- */
+
+static int64_t verify_scores_fp8(const uint16_t* q, const uint8_t* k_cache, double k_descale,
+                                 const paged_view* kv, int r, int T, int t, int h, int kvh,
+                                 int num_q_heads, int head_dim, int64_t seq_len, float softmax_scale,
+                                 int64_t j0, int64_t j1, double* s, int* bad) {
+  int64_t last = seq_len - T + t;
+  if (j1 > last + 1) j1 = last + 1;
+  const uint16_t* qrow = q + (((int64_t)r * T + t) * num_q_heads + h) * head_dim;
+  int64_t n = 0;
+  for (int64_t j = j0; j < j1; ++j, ++n) {
+    int64_t off = paged_offset(kv, r, j, kvh, bad);
+    if (off < 0) { s[n] = NAN; continue; }
+    double acc = 0.0;
+    for (int d = 0; d < head_dim; ++d)
+      acc += (double)orc_bf16_to_f32(qrow[d]) * ((double)orc_e4m3_to_f32(k_cache[off + d]) * k_descale);
+    s[n] = (double)softmax_scale * acc;
+  }
+  return n;
+}
+
+typedef struct {
+  const paged_view* v;
+  int r, h;
+  int64_t base_pos;
+  const uint8_t* codes;
+  double descale;
+  int* bad;
+} vctx_fp8;
+
+static void v_e4m3(void* c, int64_t j, double* row, int head_dim) {
+  vctx_fp8* x = (vctx_fp8*)c;
+  int64_t off = paged_offset(x->v, x->r, x->base_pos + j, x->h, x->bad);
+  for (int d = 0; d < head_dim; ++d)
+    row[d] = off < 0 ? NAN : (double)orc_e4m3_to_f32(x->codes[off + d]) * x->descale;
+}
+
+int orc_spec_verify_attn_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                             float k_descale, float v_descale, int64_t num_blocks, int64_t stride_blk,
+                             int64_t stride_tok, int64_t stride_head, const int32_t* block_table,
+                             int64_t bt_stride, const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, float softmax_scale, int32_t req_begin,
+                             int32_t req_end, float* out) {
+  int group = num_q_heads / num_kv_heads;
+  paged_view kv = make_view(k_cache, num_blocks, stride_blk, stride_tok, stride_head, block_table,
+                            bt_stride, block_size);
+  paged_view vv = make_view(v_cache, num_blocks, stride_blk, stride_tok, stride_head, block_table,
+                            bt_stride, block_size);
+  int bad = 0;
+  for (int r = req_begin; r < req_end; ++r) {
+    int64_t L = seq_lens[r];
+    double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    for (int t = 0; t < T; ++t) {
+      for (int h = 0; h < num_q_heads; ++h) {
+        int kvh = h / group;
+        int64_t n = verify_scores_fp8(q, k_cache, k_descale, &kv, r, T, t, h, kvh, num_q_heads,
+                                      head_dim, L, softmax_scale, 0, L, s, &bad);
+        vctx_fp8 c = {&vv, r, kvh, 0, v_cache, v_descale, &bad};
+        softmax_pv(s, n, head_dim, v_e4m3, &c,
+                   out + (((int64_t)r * T + t) * num_q_heads + h) * (int64_t)head_dim, NULL);
+      }
+    }
+    free(s);
+  }
+  return bad ? ORC_ERR_BOUNDS : ORC_OK;
+}
+
+int orc_spec_verify_partial_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                float k_descale, float v_descale, int64_t num_blocks,
+                                int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, float softmax_scale, int32_t split_tokens,
+                                int32_t max_splits, int32_t req_begin, int32_t req_end,
+                                float* part_o, float* part_lse) {
+  int group = num_q_heads / num_kv_heads;
+  int64_t rows = (int64_t)num_reqs * T * num_q_heads;
+  paged_view kv = make_view(k_cache, num_blocks, stride_blk, stride_tok, stride_head, block_table,
+                            bt_stride, block_size);
+  paged_view vv = make_view(v_cache, num_blocks, stride_blk, stride_tok, stride_head, block_table,
+                            bt_stride, block_size);
+  int bad = 0;
+  double* s = (double*)malloc(sizeof(double) * (size_t)split_tokens);
+  for (int r = req_begin; r < req_end; ++r) {
+    int64_t L = seq_lens[r];
+    int64_t nsplit = (L + split_tokens - 1) / split_tokens;
+    if (nsplit > max_splits) { free(s); return ORC_ERR_ARG; }
+    for (int64_t sp = 0; sp < nsplit; ++sp) {
+      int64_t j0 = sp * split_tokens, j1 = j0 + split_tokens < L ? j0 + split_tokens : L;
+      for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < num_q_heads; ++h) {
+          int kvh = h / group;
+          int64_t row = ((int64_t)r * T + t) * num_q_heads + h;
+          int64_t n = verify_scores_fp8(q, k_cache, k_descale, &kv, r, T, t, h, kvh, num_q_heads,
+                                        head_dim, L, softmax_scale, j0, j1, s, &bad);
+          vctx_fp8 c = {&vv, r, kvh, j0, v_cache, v_descale, &bad};
+          double lse;
+          softmax_pv(s, n, head_dim, v_e4m3, &c, part_o + (sp * rows + row) * head_dim, &lse);
           part_lse[sp * rows + row] = (float)lse;
         }
       }

@@ -20,7 +20,7 @@ __all__ = [
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA", "PKV_ERR_DEVICE_BOUNDS",
     "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PkvError", "lib", "library_path",
     "kv_int8_stats_quant", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
-    "spec_verify_attn_partial", "spec_verify_combine", "EXPORTED_SYMBOLS",
+    "spec_verify_attn_partial", "spec_verify_attn_partial_fp8", "spec_verify_combine", "EXPORTED_SYMBOLS",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_BOUNDS, PKV_ERR_TIMEOUT = range(6)
@@ -29,7 +29,7 @@ PKV_QK_BF16, PKV_QK_INT8 = 0, 1
 EXPORTED_SYMBOLS = (
     "pkv_last_error", "pkv_abi_version", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense",
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
-    "pkv_spec_verify_combine",
+    "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8",
 )
 
 library_path = _build.LIB
@@ -43,8 +43,8 @@ class PkvError(RuntimeError):
 
 def _load():
     if not os.path.exists(library_path):
-        raise ImportError(f"{library_path} is missing: build it with paged_kv_cache_int64_gb300._build.build() "
-                          "(needs nvcc); there is no CPU fallback")
+        raise ImportError(f"{library_path} is missing: build it first with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc); there is no CPU fallback")
     L = C.CDLL(library_path)
     i32, i64, f32, vp, sz = C.c_int32, C.c_int64, C.c_float, C.c_void_p, C.c_size_t
     L.pkv_last_error.restype = C.c_char_p
@@ -60,8 +60,10 @@ def _load():
     L.pkv_spec_verify_attn_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
                                                i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
     L.pkv_spec_verify_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    L.pkv_spec_verify_attn_partial_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, i32,
+                                                   i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
     for name in ("pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
-                 "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine"):
+                 "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8"):
         getattr(L, name).restype = i32
     return L
 
@@ -166,6 +168,22 @@ def spec_verify_attn_partial(q, k_cache, v_cache, k_scale, v_scale, block_table,
                                             _ptr(_i32(seq_lens)), R, int(T), q.shape[1], hkv, d, bs,
                                             float(softmax_scale), int(split_tokens), max_splits, _ptr(part_o),
                                             _ptr(part_lse), _ptr(dev_err), _stream(stream)))
+
+
+def spec_verify_attn_partial_fp8(q, k_fp8, v_fp8, k_descale, v_descale, block_table, seq_lens, T, softmax_scale,
+                                 split_tokens, part_o, part_lse, dev_err=None, stream=None):
+    """Split-KV verify partials over a per-tensor fp8 e4m3 cache (uint8 [nb][bs][hkv][D]); k_descale /
+    v_descale: device fp32 scalars."""
+    nb, bs, hkv, d, sb, st, sh = _cache_strides(k_fp8)
+    assert v_fp8.stride() == k_fp8.stride()
+    _i32(block_table)
+    R = block_table.shape[0]
+    _check(lib.pkv_spec_verify_attn_partial_fp8(_ptr(q), _ptr(k_fp8), _ptr(v_fp8), _ptr(k_descale),
+                                                _ptr(v_descale), nb, sb, st, sh, _ptr(block_table),
+                                                block_table.stride(0), block_table.shape[1], _ptr(_i32(seq_lens)), R,
+                                                int(T), q.shape[1], hkv, d, bs, float(softmax_scale),
+                                                int(split_tokens), part_o.shape[0], _ptr(part_o), _ptr(part_lse),
+                                                _ptr(dev_err), _stream(stream)))
 
 
 def spec_verify_combine(part_o, part_lse, seq_lens, T, split_tokens, out, stream=None):

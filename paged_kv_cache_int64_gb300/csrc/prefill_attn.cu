@@ -17,8 +17,9 @@
 //               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
 //   warp 2      tensor-memory allocation (512 columns: O 256, two S buffers of 128).
 //   warps 4-7   softmax: thread i owns row i (TMEM lane i): scale, causal mask, running max
-//               (moved only when it grows by more than 2^8, so O is rarely rescaled), exp2, row
-//               sum, P packed to bf16 into the S columns; the epilogue normalises O, stores bf16.
+//               (moved only when it grows by more than 2^8, so O is rarely rescaled), exp2, P
+//               packed to bf16 into the S columns, row sum of the rounded P; the epilogue
+//               normalises O and stores bf16.
 //   warps 8-11  int8-QK only: widen the int8 K tile (dense scratch of kv_int8_stats_quant) to
 //               fp16 integers; the softmax warps quantize their Q rows in place first. Q8.K8 runs
 //               as an f16 MMA: every product and partial sum is an integer below 2^24, so the f32
@@ -274,7 +275,10 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
       return t;
     };
-    // K tile j through k_full[c] (bf16) or the K8 stage (int8), chunk by chunk as QK_{j-1} frees it
+    uint32_t fix_phase = 0;
+    // K tile j through k_full[c] (bf16) or the K8 stage (int8), chunk by chunk as QK_{j-1} frees it.
+    // K rows past seq_len need no zero-fill (their scores are masked); rows of a bad segment do,
+    // so such a tile goes through the private barrier, is patched, then published.
     auto load_k = [&](int j, const TileInfo& t) {
       const int key0 = j * kBN;
       if (kInt8) {
@@ -283,6 +287,27 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
           const int row = (int)((int64_t)r * p.max_ctx + key0);
           for (int c = 0; c < 2; ++c) tma_load_3d(sK8 + c * kChunkBytes, &p.k8map, &bar.k8_full, c * 128, kvh, row);
         }
+        __syncwarp();
+        return;
+      }
+      if (t.bad) {
+        if (lane == 0) {
+          for (int c = 0; c < 4 && j > 0; ++c)
+            if (!mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
+          if (!*abort) mbar_arrive_expect_tx(&bar.fix, 4u * t.nloaded * seg_bytes);
+        }
+        __syncwarp();
+        if (*abort) return;
+        if (t.blk >= 0) issue_seg(sK, &p.kmap, &bar.fix, t.blk, key0);
+        if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+        ++fix_phase;
+        __syncwarp();
+        if (*abort) return;
+        zero_rows(sK, kBN, t.bad, G, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
         __syncwarp();
         return;
       }
@@ -298,16 +323,15 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
           tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
       }
     };
-    uint32_t fix_phase = 0;
     TileInfo cur = info(0);
     TileInfo nxt = info(1);
-    if (kInt8 || !cur.fix) load_k(0, cur);
+    load_k(0, cur);
     for (int j = 0; j < n_tiles && !*abort; ++j) {
       const int key0 = j * kBN;
       const int n_valid = min(kBN, seq_len - key0);
       if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
-      // K of the next tile first: it streams in while QK_j runs
-      if (j + 1 < n_tiles && (kInt8 || !nxt.fix)) load_k(j + 1, nxt);
+      // K of the next tile first: it streams in while QK_j runs (it waits only for QK_j)
+      if (j + 1 < n_tiles) load_k(j + 1, nxt);
       __syncwarp();
       if (*abort) break;
       // V_j once PV_{j-1} has released the V tile
@@ -319,33 +343,19 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         __syncwarp();
         if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
       } else {
-        // A tile with rows to zero-fill (the CTA's tail past seq_len, or a bad table entry): load
-        // K (bf16) and V through the private barrier, zero those rows, then publish both.
-        if (lane == 0) {
-          if (!kInt8)
-            for (int c = 0; c < 4 && j > 0; ++c)
-              if (!mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
-          if (!*abort) mbar_arrive_expect_tx(&bar.fix, (kInt8 ? 4u : 8u) * cur.nloaded * seg_bytes);
-        }
+        // V rows past seq_len or in a bad segment must be zero (P is 0 there, but 0 * NaN is not):
+        // load through the private barrier, zero those rows, then publish.
+        if (lane == 0) mbar_arrive_expect_tx(&bar.fix, 4u * cur.nloaded * seg_bytes);
         __syncwarp();
-        if (*abort) break;
-        if (cur.blk >= 0) {
-          issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
-          if (!kInt8) issue_seg(sK, &p.kmap, &bar.fix, cur.blk, key0);
-        }
+        if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
         if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
         ++fix_phase;
         __syncwarp();
         if (*abort) break;
         zero_rows(sV, n_valid, cur.bad, G, lane);
-        if (!kInt8) zero_rows(sK, kBN, cur.bad, G, lane);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          if (!kInt8)
-            for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
-          mbar_arrive(&bar.v_full);
-        }
+        if (lane == 0) mbar_arrive(&bar.v_full);
       }
       __syncwarp();
       cur = nxt;
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
     float sc = p.scale_log2;
     bool ok = true;
     if (kInt8) {
-      ok = mbar_wait(&bar.q_full, 0, abort);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
       if (ok) {
         sc = p.scale_log2 * quantize_q_row_inplace(sQ, i);
         fence_proxy_async_smem();
@@ -420,7 +430,8 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         bar.kscale[j & 1][i] = v;
         named_bar_sync(1, 128);
       }
-      if (!mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort)) break;
+      // tcgen05.ld/st below are warp-collective: every exit decision is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort))) break;
       tc_fence_after();
       const uint32_t sb = tmem + lane_off + ((j & 1) ? kColS1 : kColS0);
       const bool need_mask = key0 + kBN - 1 > p_i;
@@ -468,8 +479,10 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
           if (need_mask && col > lim) s0 = -INFINITY;
           if (need_mask && col + 1 > lim) s1 = -INFINITY;
           const float e0 = ex2_approx(s0 - m_use), e1 = ex2_approx(s1 - m_use);
-          lsum += e0 + e1;
           pk[e] = pack_bf16x2(e0, e1);
+          // the row sum uses the bf16-rounded weights that the PV MMA multiplies, so the result is
+          // an exact convex combination of V rows with weights perturbed by at most 2^-9
+          lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
         }
         tmem_st_32x32b_x16(sb + cc * 16, pk);
       }
@@ -477,7 +490,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       l_run += lsum;
       // O may be touched only once PV_{j-1} has completed
       if (j > 0) {
-        if (!mbar_wait(&bar.pv_done, (j - 1) & 1, abort)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort))) break;
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, rescale)) {
@@ -496,7 +509,9 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       mbar_arrive(&bar.p_full);
     }
     // epilogue: O / l -> bf16 rows
-    if (!*abort && n_tiles > 0 && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort)) {
+    bool fin = ok && !*abort && n_tiles > 0;
+    fin = fin && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    if (__all_sync(0xffffffffu, fin)) {
       tc_fence_after();
       const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(tok0 + i) * p.num_q_heads + qh) * kD);
@@ -584,6 +599,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   PKV_UNSUP(head_dim == kD, "paged_prefill_attn: head_dim must be 256 (got %d)", head_dim);
   PKV_ARG(qk_mode == PKV_QK_BF16 || qk_mode == PKV_QK_INT8, "paged_prefill_attn: unknown qk_mode %d", qk_mode);
   const bool int8 = qk_mode == PKV_QK_INT8;
+  if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;  // nothing to do, nothing read
   PKV_ARG(q && v_cache && block_table && seq_lens && query_start_loc && out,
           "paged_prefill_attn: null pointer argument");
   PKV_ARG(int8 ? (k8 && k8_scale && max_ctx > 0) : (k_cache != nullptr),

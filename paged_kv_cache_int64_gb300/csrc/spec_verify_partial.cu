@@ -88,6 +88,8 @@ struct Params {
   float* part_lse;
   int64_t rows;  // num_reqs * T * Hq
   int* dev_err;
+  const float* k_descale;  // fp8 cache: per-tensor scales (device scalars)
+  const float* v_descale;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -110,6 +112,21 @@ __device__ __forceinline__ void widen16_f16(uint4 in, uint32_t (&o)[8]) {
   }
 }
 
+// 16 e4m3 codes -> 16 fp16 values, exact (every e4m3 value is an fp16 value): hardware conversion.
+__device__ __forceinline__ void widen16_e4m3(uint4 in, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * i]) : "h"((uint16_t)(w[i] & 0xffffu)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o[2 * i + 1]) : "h"((uint16_t)(w[i] >> 16)));
+  }
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void widen16(uint4 in, uint32_t (&o)[8]) {
+  if (kFp8) widen16_e4m3(in, o); else widen16_f16(in, o);
+}
+
 // Butterfly reduce-scatter: on entry every lane holds 32 column values; on exit lane l holds the
 // reduction over the warp of column l. 31 shuffles.
 template <bool kMax>
@@ -128,6 +145,7 @@ __device__ __forceinline__ float warp_reduce_columns(float (&v)[kNQ], int lane) 
   return v[0];
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (lane == 0) {
         if (bad) record_error(p.dev_err, kErrDeviceBounds);
         bar.bad[st] = bad;
-        mbar_arrive_expect_tx(&bar.st_full[st], nloaded * (uint32_t)G * (4u * 128u + 2u * 16u));
+        mbar_arrive_expect_tx(&bar.st_full[st], nloaded * (uint32_t)G * (kFp8 ? 4u * 128u : 4u * 128u + 2u * 16u));
       }
       __syncwarp();
       if (blk >= 0) {
@@ -216,8 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           tma_load_4d(stage + kStageV8 + c * kChunk8 + lane * G * 128, &p.v8map, &bar.st_full[st], c * 128, kvh,
                       slot, blk);
         }
-        tma_load_3d(stage + kStageKS + lane * G * 16, &p.ksmap, &bar.st_full[st], (kvh & ~3), slot, blk);
-        tma_load_3d(stage + kStageVS + lane * G * 16, &p.vsmap, &bar.st_full[st], (kvh & ~3), slot, blk);
+        if (!kFp8) {
+          tma_load_3d(stage + kStageKS + lane * G * 16, &p.ksmap, &bar.st_full[st], (kvh & ~3), slot, blk);
+          tma_load_3d(stage + kStageVS + lane * G * 16, &p.vsmap, &bar.st_full[st], (kvh & ~3), slot, blk);
+        }
       }
     }
   } else if (warp == 1) {
@@ -251,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int k = quarter * 32 + lane;  // key row of the tile (TMEM lane k)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int G = p.seg;
+    const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
+    const float v_descale = kFp8 ? __ldg(p.v_descale) : 0.0f;
     // Q: bf16 -> fp16 in place (32 rows x 256)
     bool ok = mbar_wait(&bar.q_full, 0, abort);
     ok = __all_sync(0xffffffffu, ok);
@@ -287,8 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const int key = k_begin + j * kBN + k;
       const bool bad = (bar.bad[st] >> (k / G)) & 1u;
       const bool in_range = key < k_end;
-      const float ks = (in_range && !bad) ? reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)] : 0.0f;
-      const float vs = (in_range && !bad) ? reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)] : 0.0f;
+      float ks = 0.0f, vs = 0.0f;
+      if (in_range && !bad) {
+        if (kFp8) {
+          ks = k_descale;
+          vs = v_descale;
+        } else {
+          ks = reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)];
+          vs = reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)];
+        }
+      }
       // K row -> fp16 into TMEM lane k; V row -> fp16 into the MN-major V tile
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
@@ -299,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageK8 + (w4 >> 1) * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
-          widen16_f16(v, o);
+          widen16<kFp8>(v, o);
 #pragma unroll
           for (int e = 0; e < 8; ++e) kv[8 * i + e] = o[e];
         }
@@ -312,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageV8 + c8 * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
-          widen16_f16(v, o);
+          widen16<kFp8>(v, o);
           uint8_t* row = sV16 + (2 * c8 + (q8 >> 2)) * kChunk16 + k * 128;
           const uint32_t piece = 2u * (q8 & 3);
           *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -454,39 +484,40 @@ extern "C" size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t nu
   return o + l;
 }
 
-extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
-                                                   const float* k_scale, const float* v_scale, int64_t num_blocks,
-                                                   int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
-                                                   int64_t scale_stride_blk, int64_t scale_stride_tok,
-                                                   const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
-                                                   const int32_t* seq_lens, int32_t num_reqs, int32_t T,
-                                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                                   int32_t block_size, float softmax_scale, int32_t split_tokens,
-                                                   int32_t max_splits, float* part_o, float* part_lse,
-                                                   int32_t* dev_err, void* stream) {
-  using namespace pkv;
+namespace pkv {
+namespace {
+
+// Shared host path of the int8 (per-token-head scales) and fp8 (per-tensor descales) verify calls.
+template <bool kFp8>
+pkv_status launch_verify(const char* name, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_sc, const float* v_sc, int64_t num_blocks, int64_t stride_blk,
+                         int64_t stride_tok, int64_t stride_head, int64_t scale_stride_blk,
+                         int64_t scale_stride_tok, const int32_t* block_table, int64_t bt_stride,
+                         int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         float softmax_scale, int32_t split_tokens, int32_t max_splits, float* part_o,
+                         float* part_lse, int32_t* dev_err, void* stream) {
   clear_error();
-  PKV_UNSUP(head_dim == kD, "spec_verify_attn_partial: head_dim must be 256 (got %d)", head_dim);
-  PKV_ARG(q && k_cache && v_cache && k_scale && v_scale && block_table && seq_lens && part_o && part_lse,
-          "spec_verify_attn_partial: null pointer argument");
-  PKV_ARG(num_reqs >= 0 && T > 0 && num_q_heads > 0 && num_kv_heads > 0 && num_blocks > 0 && block_size > 0 &&
+  PKV_UNSUP(head_dim == kD, "%s: head_dim must be 256 (got %d)", name, head_dim);
+  if (num_reqs == 0) return PKV_OK;  // nothing to do, nothing read
+  PKV_ARG(q && k_cache && v_cache && k_sc && v_sc && block_table && seq_lens && part_o && part_lse,
+          "%s: null pointer argument", name);
+  PKV_ARG(num_reqs > 0 && T > 0 && num_q_heads > 0 && num_kv_heads > 0 && num_blocks > 0 && block_size > 0 &&
               max_blocks > 0 && bt_stride >= max_blocks && max_splits > 0 && split_tokens > 0,
-          "spec_verify_attn_partial: bad size argument");
-  PKV_UNSUP(num_q_heads % num_kv_heads == 0, "spec_verify_attn_partial: num_q_heads %% num_kv_heads != 0");
+          "%s: bad size argument", name);
+  PKV_UNSUP(num_q_heads % num_kv_heads == 0, "%s: num_q_heads %% num_kv_heads != 0", name);
   const int group = num_q_heads / num_kv_heads;
-  PKV_UNSUP(group * T == kNQ, "spec_verify_attn_partial: T * (num_q_heads / num_kv_heads) must be 32 (got %d)",
-            group * T);
-  PKV_UNSUP(num_kv_heads % 4 == 0, "spec_verify_attn_partial: num_kv_heads must be a multiple of 4");
-  PKV_UNSUP(block_size % 8 == 0, "spec_verify_attn_partial: block_size must be a multiple of 8");
-  PKV_UNSUP(split_tokens % kBN == 0, "spec_verify_attn_partial: split_tokens must be a multiple of 128");
-  PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0 && scale_stride_blk > 0 && scale_stride_tok > 0,
-          "spec_verify_attn_partial: strides must be positive");
-  PKV_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(k_scale) && aligned16(v_scale) &&
-              stride_blk % 16 == 0 && stride_tok % 16 == 0 && stride_head % 16 == 0 && scale_stride_blk % 4 == 0 &&
-              scale_stride_tok % 4 == 0,
-          "spec_verify_attn_partial: pointers and strides must be 16-byte aligned");
-  PKV_ARG(softmax_scale > 0.0f, "spec_verify_attn_partial: softmax_scale must be positive");
-  if (num_reqs == 0) return PKV_OK;
+  PKV_UNSUP(group * T == kNQ, "%s: T * (num_q_heads / num_kv_heads) must be 32 (got %d)", name, group * T);
+  PKV_UNSUP(kFp8 || num_kv_heads % 4 == 0, "%s: num_kv_heads must be a multiple of 4", name);
+  PKV_UNSUP(block_size % 8 == 0, "%s: block_size must be a multiple of 8", name);
+  PKV_UNSUP(split_tokens % kBN == 0, "%s: split_tokens must be a multiple of 128", name);
+  PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0 && (kFp8 || (scale_stride_blk > 0 && scale_stride_tok > 0)),
+          "%s: strides must be positive", name);
+  PKV_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && (kFp8 || (aligned16(k_sc) && aligned16(v_sc))) &&
+              stride_blk % 16 == 0 && stride_tok % 16 == 0 && stride_head % 16 == 0 &&
+              (kFp8 || (scale_stride_blk % 4 == 0 && scale_stride_tok % 4 == 0)),
+          "%s: pointers and strides must be 16-byte aligned", name);
+  PKV_ARG(softmax_scale > 0.0f, "%s: softmax_scale must be positive", name);
   Params p{};
   const int G = gcd_int(block_size, kBN);
   {
@@ -505,15 +536,18 @@ extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* 
     s = encode_tiled(&p.v8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v_cache, dims, strides, box, "v_cache");
     if (s != PKV_OK) return s;
   }
-  {
+  if (!kFp8) {
     const uint64_t dims[3] = {(uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
     const uint64_t strides[2] = {(uint64_t)scale_stride_tok * 4, (uint64_t)scale_stride_blk * 4};
     const uint32_t box[3] = {4, (uint32_t)G, 1};
-    pkv_status s = encode_tiled(&p.ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_scale, dims, strides, box, "k_scale",
+    pkv_status s = encode_tiled(&p.ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_sc, dims, strides, box, "k_scale",
                                 false);
     if (s != PKV_OK) return s;
-    s = encode_tiled(&p.vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_scale, dims, strides, box, "v_scale", false);
+    s = encode_tiled(&p.vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_sc, dims, strides, box, "v_scale", false);
     if (s != PKV_OK) return s;
+  } else {
+    p.k_descale = k_sc;
+    p.v_descale = v_sc;
   }
   p.block_table = block_table;
   p.bt_stride = bt_stride;
@@ -535,10 +569,46 @@ extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* 
   constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(spec_verify_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaFuncSetAttribute(spec_verify_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     attr = true;
   }
   dim3 grid((unsigned)max_splits, (unsigned)num_kv_heads, (unsigned)num_reqs);
-  spec_verify_partial_kernel<<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
-  return check_launch("spec_verify_attn_partial");
+  spec_verify_partial_kernel<kFp8><<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  return check_launch(name);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                                   const float* k_scale, const float* v_scale, int64_t num_blocks,
+                                                   int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                                   int64_t scale_stride_blk, int64_t scale_stride_tok,
+                                                   const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                                   const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                   int32_t block_size, float softmax_scale, int32_t split_tokens,
+                                                   int32_t max_splits, float* part_o, float* part_lse,
+                                                   int32_t* dev_err, void* stream) {
+  return pkv::launch_verify<false>("spec_verify_attn_partial", q, k_cache, v_cache, k_scale, v_scale, num_blocks,
+                                   stride_blk, stride_tok, stride_head, scale_stride_blk, scale_stride_tok,
+                                   block_table, bt_stride, max_blocks, seq_lens, num_reqs, T, num_q_heads,
+                                   num_kv_heads, head_dim, block_size, softmax_scale, split_tokens, max_splits,
+                                   part_o, part_lse, dev_err, stream);
+}
+
+extern "C" pkv_status pkv_spec_verify_attn_partial_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
+                                                       const float* k_descale, const float* v_descale,
+                                                       int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                                       int64_t stride_head, const int32_t* block_table,
+                                                       int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens,
+                                                       int32_t num_reqs, int32_t T, int32_t num_q_heads,
+                                                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                                       float softmax_scale, int32_t split_tokens, int32_t max_splits,
+                                                       float* part_o, float* part_lse, int32_t* dev_err,
+                                                       void* stream) {
+  return pkv::launch_verify<true>("spec_verify_attn_partial_fp8", q, k_fp8, v_fp8, k_descale, v_descale, num_blocks,
+                                  stride_blk, stride_tok, stride_head, 0, 0, block_table, bt_stride, max_blocks,
+                                  seq_lens, num_reqs, T, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  softmax_scale, split_tokens, max_splits, part_o, part_lse, dev_err, stream);
 }

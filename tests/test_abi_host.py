@@ -20,8 +20,8 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def libpath():
-    from paged_kv_cache_int64_gb300 import _build
-    return _build.build()
+    import __graft_entry__
+    return __graft_entry__._build_module().build()
 
 
 @pytest.fixture(scope="module")
@@ -52,8 +52,8 @@ def test_library_exports_every_declared_symbol(libpath, pkv):
 
 
 def test_library_targets_sm103a(libpath):
-    from paged_kv_cache_int64_gb300 import _build
-    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+    import __graft_entry__
+    assert "arch=compute_103a,code=sm_103a" in " ".join(__graft_entry__._build_module().ARCH)
 
 
 def test_abi_version(pkv):

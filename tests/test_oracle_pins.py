@@ -428,3 +428,44 @@ def test_verify_zero_keys_mean_of_visible_dequantized_values():
         n = 30 + t + 1
         for h in range(p.num_q_heads):
             np.testing.assert_allclose(out[t, h], vf[:n, h // g].mean(axis=0), atol=1e-6)
+
+
+# --------------------------------------------------------------------------------------------
+# verify over a per-tensor fp8 e4m3 cache
+# --------------------------------------------------------------------------------------------
+
+
+def _small_verify_fp8(seed=8, lengths=(100, 37, 260), T=8):
+    return W.make_problem("vf", seed=seed, seq_lens=[L + T for L in lengths], q_lens=[T] * len(lengths),
+                          num_blocks=64, block_size=16, num_q_heads=8, num_kv_heads=2, head_dim=32,
+                          kv_dtype="e4m3", softmax_scale=0.2)
+
+
+def test_verify_fp8_equals_prefill_path_on_bf16_copy():
+    # every e4m3 value is exact in bf16, and so is its product with a power-of-two descale: the same
+    # values through the bf16 prefill oracle must agree
+    T = 8
+    p = _small_verify_fp8()
+    kd, vd = 0.5, 0.25
+    ver = oracle.spec_verify_attn_fp8(p.q, p.pool_numpy("k"), p.pool_numpy("v"), kd, vd, p.block_table(),
+                                      p.seq_lens, T, p.num_q_heads, p.softmax_scale)
+    bf = W.make_problem("b", seed=1, seq_lens=list(p.seq_lens), q_lens=[T] * p.num_reqs, num_blocks=64,
+                        block_size=16, num_q_heads=8, num_kv_heads=2, head_dim=32, softmax_scale=p.softmax_scale)
+    for rb, rv in zip(bf.requests, p.requests):
+        rb.blocks = rv.blocks
+        f = lambda codes, sc: W.to_bf16_bits(
+            torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy() * sc)
+        rb.k_tok, rb.v_tok = f(rv.k_tok, kd), f(rv.v_tok, vd)
+    bf.q = p.q
+    np.testing.assert_allclose(ver, _run_paged(bf), atol=1e-6, rtol=0)
+
+
+@pytest.mark.parametrize("split", [16, 64])
+def test_verify_fp8_split_combine_equals_unsplit(split):
+    T = 8
+    p = _small_verify_fp8()
+    args = (p.q, p.pool_numpy("k"), p.pool_numpy("v"), 0.5, 0.25, p.block_table(), p.seq_lens)
+    full = oracle.spec_verify_attn_fp8(*args, T, p.num_q_heads, p.softmax_scale)
+    S = int(math.ceil(p.seq_lens.max() / split))
+    po, pl = oracle.spec_verify_partial_fp8(*args, T, p.num_q_heads, p.softmax_scale, split, S)
+    np.testing.assert_allclose(oracle.spec_verify_combine(po, pl, p.seq_lens, T, split), full, atol=1e-6, rtol=1e-5)
