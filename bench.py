@@ -105,7 +105,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons = [], None, set()  # median SM clock under load, max clock, active slowdown reasons
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -351,11 +351,19 @@ def _gbs(nbytes, ms, peaks):
 
 
 def load_traffic(kernel):
-    """dram bytes per launch of `kernel` from the committed ncu summary, if it matches the current build."""
+    """dram read + write bytes per launch of `kernel` from the committed ncu capture, or None when
+    there is none or the kernel source has changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f).get(kernel)
+            ent = json.load(f).get(kernel)
+        if not ent:
+            return None
+        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != ent["source_sha256"]:
+                return None
+        return int(ent["dram_bytes_per_launch"])
     except Exception:
         return None
 
@@ -588,7 +596,7 @@ def run_ncu_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=0, help="query tokens per prefill pass (0: one per core)")

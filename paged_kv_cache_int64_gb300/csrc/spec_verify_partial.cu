@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const bool bad = (bar.bad[st] >> (k / G)) & 1u;
       const bool in_range = key < k_end;
       float ks = 0.0f, vs = 0.0f;
-      if (in_range && !bad) {
+      const bool live = in_range && !bad;  // a key of this split with a valid block
+      if (live) {
         if (kFp8) {
           ks = k_descale;
           vs = v_descale;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           uint32_t o[8];
           widen16<kFp8>(v, o);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) kv[8 * i + e] = o[e];
+          for (int e = 0; e < 8; ++e) kv[8 * i + e] = live ? o[e] : 0u;
         }
         tmem_st_32x32b_x32(tmem + lane_off + kColK + 32 * w4, kv);
       }
@@ -343,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
           widen16<kFp8>(v, o);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = live ? o[e] : 0u;  // rows past the split: zero (0 * NaN != 0)
           uint8_t* row = sV16 + (2 * c8 + (q8 >> 2)) * kChunk16 + k * 128;
           const uint32_t piece = 2u * (q8 & 3);
           *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
