@@ -219,6 +219,35 @@ PKV_API pkv_status pkv_spec_verify_combine(const float* part_o, const float* par
                                    int32_t num_q_heads, int32_t head_dim, int32_t split_tokens,
                                    int32_t max_splits, void* out, void* stream);
 
+/*
+ * spec_verify_attn_noalloc - pkv_spec_verify_attn_partial followed by pkv_spec_verify_combine, with
+ * the split partials kept in a fixed scratch array inside the library instead of a caller
+ * workspace. The paper has no counterpart; it exists for callers that cannot allocate device
+ * memory (a plugin whose host owns the device allocator, a path that must not allocate between
+ * steps, a caller that can only pass inputs and outputs). It allocates nothing.
+ * Limit: the partials need num_reqs*T*num_q_heads*max_splits*(head_dim+1)*4 bytes (plus
+ * alignment), at most pkv_spec_verify_noalloc_capacity_bytes() (32 MiB); larger calls return
+ * PKV_ERR_INVALID_ARG with a message - use fewer splits (larger split_tokens) or the workspace call.
+ * The array is reserved on every GPU that loads the library until the process exits. Its device
+ * address is looked up on the first call made on each device (with that device current), so make
+ * that first call before any stream capture. All calls on a device share the array and overwrite
+ * it; calls that overlap on the GPU race on it. Each call writes every partial it reads.
+ * Arguments, layouts and requirements are those of pkv_spec_verify_attn_partial, with out bf16
+ * [num_reqs*T][num_q_heads][head_dim] as in pkv_spec_verify_combine.
+ */
+PKV_API size_t pkv_spec_verify_noalloc_capacity_bytes(void);
+PKV_API pkv_status pkv_spec_verify_attn_noalloc(const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                                const float* k_scale, const float* v_scale,
+                                                int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,
+                                                int64_t stride_head, int64_t scale_stride_blk,
+                                                int64_t scale_stride_tok, const int32_t* block_table,
+                                                int64_t bt_stride, int32_t max_blocks,
+                                                const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                                int32_t num_q_heads, int32_t num_kv_heads,
+                                                int32_t head_dim, int32_t block_size, float softmax_scale,
+                                                int32_t split_tokens, int32_t max_splits, void* out,
+                                                int32_t* dev_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

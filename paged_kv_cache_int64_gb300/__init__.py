@@ -29,7 +29,8 @@ PKV_QK_BF16, PKV_QK_INT8 = 0, 1
 EXPORTED_SYMBOLS = (
     "pkv_last_error", "pkv_abi_version", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense",
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
-    "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8",
+    "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
+    "pkv_spec_verify_attn_noalloc",
 )
 
 library_path = _build.LIB
@@ -62,6 +63,11 @@ def _load():
     L.pkv_spec_verify_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     L.pkv_spec_verify_attn_partial_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, i32,
                                                    i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
+    L.pkv_spec_verify_noalloc_capacity_bytes.argtypes = []
+    L.pkv_spec_verify_noalloc_capacity_bytes.restype = sz
+    L.pkv_spec_verify_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
+                                               i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp]
+    L.pkv_spec_verify_attn_noalloc.restype = i32
     for name in ("pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
                  "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8"):
         getattr(L, name).restype = i32
