@@ -16,14 +16,16 @@
 //               both operands in shared memory, f32 accumulator in tensor memory), then
 //               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
 //   warp 2      tensor-memory allocation (512 columns: O 256, two S buffers of 128).
-//   warps 4-7   softmax: thread i owns row i (TMEM lane i): scale, causal mask, running max
-//               (moved only when it grows by more than 2^8, so O is rarely rescaled), exp2, P
-//               packed to bf16 into the S columns, row sum of the rounded P; the epilogue
-//               normalises O and stores bf16.
-//   warps 8-11  int8-QK only: widen the int8 K tile (dense scratch of kv_int8_stats_quant) to
-//               fp16 integers; the softmax warps quantize their Q rows in place first. Q8.K8 runs
-//               as an f16 MMA: every product and partial sum is an integer below 2^24, so the f32
-//               accumulator holds the exact integer dot product.
+//   warps 4-11  softmax, two warpgroups that split every row (score columns 0-63 / 64-127, O
+//               columns 0-127 / 128-255; row i lives in TMEM lane i): one tensor-memory read of S
+//               per tile, scale, causal mask, row maximum shared through shared memory, running
+//               max moved only when it grows by more than 2^8 (so O is rarely rescaled), exp2, P
+//               packed to bf16 into the consumed S columns, row sums of the rounded P; the
+//               epilogue normalises O and stores bf16.
+//   warps 12-15 int8-QK only: read the int8 K rows (dense scratch of kv_int8_stats_quant) and
+//               widen them to fp16 integers in the K tile; half 0 of the softmax quantizes the Q
+//               rows in place first. Q8.K8 runs as an f16 MMA: every product and partial sum is an
+//               integer below 2^24, so the f32 accumulator holds the exact integer dot product.
 // Rows of the last tile past seq_len (and of any out-of-range block) are zero-filled in shared
 // memory before the MMAs read them, so stale or NaN pool bytes never reach P.V. Every wait is
 // bounded: on expiry the CTA records PKV_ERR_TIMEOUT, drains and exits.
@@ -52,16 +54,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kTileBytes;
-constexpr int kOffK8 = kOffV + kTileBytes;  // int8 mode: [2 chunks][128 rows][128 B]
-constexpr int kK8Bytes = 2 * kChunkBytes;
+constexpr int kTilesEnd = kOffV + kTileBytes;
 
 struct Barriers {
   uint64_t q_full;      // TMA Q landed
   uint64_t q_ready;     // int8: Q quantized in place
   uint64_t k_full[4];   // chunk c of K tile j ready (TMA bytes, or converter arrivals)
   uint64_t k_empty[4];  // chunk c of K tile j consumed by the QK MMAs
-  uint64_t k8_full;     // int8: K8 tile landed
-  uint64_t k8_free;     // int8: K8 stage consumed by the converter
   uint64_t v_full;      // V tile j ready
   uint64_t fix;         // producer-private: copies of a tile that needs zero-filled rows
   uint64_t s_full[2];   // S_j in TMEM
@@ -70,13 +69,15 @@ struct Barriers {
   uint32_t tmem_base;
   int abort;
   float kscale[2][kBN];  // int8: per-key scales of the tile
+  float qscale[kBM];     // int8: per-row q scales
+  float rowmax[2][2][kBM];  // per tile parity, per half: row maxima (and the final row sums)
 };
 
 struct Params {
   CUtensorMap qmap;   // bf16 q: dims {D, Hq, total_q}, box {64, 1, 128}
   CUtensorMap kmap;   // bf16 pool: dims {D, Hkv, bs, nb}, box {64, 1, G, 1}
   CUtensorMap vmap;
-  CUtensorMap k8map;  // int8 scratch: dims {D, Hkv, R*max_ctx}, box {128, 1, 128}
+  const int8_t* k8;   // int8 scratch [R][max_ctx][Hkv][D] (read row by row by the converter)
   const int32_t* block_table;
   int64_t bt_stride;
   int64_t num_blocks;
@@ -95,8 +96,8 @@ struct Params {
 
 template <bool kInt8>
 struct Cfg {
-  static constexpr int kThreads = kInt8 ? 384 : 256;
-  static constexpr int kTiles = kInt8 ? kOffK8 + kK8Bytes : kOffK8;
+  static constexpr int kThreads = kInt8 ? 512 : 384;
+  static constexpr int kTiles = kTilesEnd;
   static constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
 };
 
@@ -188,7 +189,6 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  uint8_t* sK8 = smem + kOffK8;
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kInt8>::kTiles);
 
   const int warp = threadIdx.x >> 5;
@@ -214,13 +214,11 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       mbar_init(&bar.k_full[c], kInt8 ? 128 : 1);
       mbar_init(&bar.k_empty[c], 1);
     }
-    mbar_init(&bar.k8_full, 1);
-    mbar_init(&bar.k8_free, 128);
     mbar_init(&bar.v_full, 1);
     mbar_init(&bar.fix, 1);
     mbar_init(&bar.s_full[0], 1);
     mbar_init(&bar.s_full[1], 1);
-    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.p_full, 256);
     mbar_init(&bar.pv_done, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -243,7 +241,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&p.qmap);
       prefetch_tensormap(&p.vmap);
-      if (kInt8) prefetch_tensormap(&p.k8map); else prefetch_tensormap(&p.kmap);
+      if (!kInt8) prefetch_tensormap(&p.kmap);
       mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
       for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
     }
@@ -281,15 +279,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
     // so such a tile goes through the private barrier, is patched, then published.
     auto load_k = [&](int j, const TileInfo& t) {
       const int key0 = j * kBN;
-      if (kInt8) {
-        if (lane == 0 && (j == 0 || mbar_wait(&bar.k8_free, (j - 1) & 1, abort))) {
-          mbar_arrive_expect_tx(&bar.k8_full, kK8Bytes);
-          const int row = (int)((int64_t)r * p.max_ctx + key0);
-          for (int c = 0; c < 2; ++c) tma_load_3d(sK8 + c * kChunkBytes, &p.k8map, &bar.k8_full, c * 128, kvh, row);
-        }
-        __syncwarp();
-        return;
-      }
+      if (kInt8) return;  // the converter warps read the int8 K rows themselves
       if (t.bad) {
         if (lane == 0) {
           for (int c = 0; c < 4 && j > 0; ++c)
@@ -402,55 +392,76 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------------------------- softmax
-    const int quarter = warp - 4;
+    // Two warpgroups share every row: half h = 0 owns score columns 0-63 and O columns 0-127,
+    // half h = 1 columns 64-127 and O columns 128-255. Thread (h, i) owns row i = TMEM lane i.
+    // Both halves meet at named barrier 1 (256 threads) a fixed number of times per tile; a
+    // failed wait never skips a barrier - it only marks the warp dead, so the barriers stay paired.
+    const int h = (warp - 4) >> 2;
+    const int quarter = warp & 3;
     const int i = quarter * 32 + lane;
     const int p_i = min(p0 + i, seq_len - 1);
     const bool row_valid = i < rows_valid;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float sc = p.scale_log2;
-    bool ok = true;
+    bool dead = false;  // warp-uniform
     if (kInt8) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
-      if (ok) {
-        sc = p.scale_log2 * quantize_q_row_inplace(sQ, i);
+      dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
+      if (!dead && h == 0) {
+        bar.qscale[i] = quantize_q_row_inplace(sQ, i);
         fence_proxy_async_smem();
         mbar_arrive(&bar.q_ready);
       }
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0, abort));
+      if (!dead) sc = p.scale_log2 * bar.qscale[i];
     }
     float m_run = -INFINITY, l_run = 0.0f;
-    for (int j = 0; ok && j < n_tiles; ++j) {
+    for (int j = 0; j < n_tiles; ++j) {
       const int key0 = j * kBN;
-      const float* ks = bar.kscale[j & 1];
-      if (kInt8) {
+      const float* ks = bar.kscale[j & 1] + 64 * h;
+      if (kInt8 && h == 0 && !dead) {
         const int key = key0 + i;
         float v = 0.0f;
         if (key < seq_len) v = __ldg(p.k8_scale + ((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh);
         bar.kscale[j & 1][i] = v;
-        named_bar_sync(1, 128);
       }
-      // tcgen05.ld/st below are warp-collective: every exit decision is made warp-uniform
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort))) break;
-      tc_fence_after();
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort));
       const uint32_t sb = tmem + lane_off + ((j & 1) ? kColS1 : kColS0);
-      const bool need_mask = key0 + kBN - 1 > p_i;
-      const int lim = p_i - key0;  // columns > lim are masked
-      // pass 1: row max of the scaled, masked scores
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(sb + cc * 32, v);
+      uint32_t sv[64];
+      if (!dead) {
+        tc_fence_after();
+        uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+        uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+        tmem_ld_32x32b_x32(sb + 64 * h, a);
+        tmem_ld_32x32b_x32(sb + 64 * h + 32, b);
         tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = cc * 32 + e;
-          float s = __uint_as_float(v[e]) * (kInt8 ? sc * ks[col] : sc);
-          if (need_mask && col > lim) s = -INFINITY;
-          mx = fmaxf(mx, s);
-        }
+        for (int e = 0; e < 64; ++e) sv[e] = 0u;
       }
+      const int lim = p_i - key0 - 64 * h;  // this half's columns > lim are masked
+      const bool need_mask = lim < 63;
+      if (kInt8) {  // fold the per-key scales in place: s = S * ks
+        named_bar_sync(1, 256);  // this tile's kscale, written by half 0, is visible
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        float v = __uint_as_float(sv[e]);
+        if (need_mask && e > lim) v = -INFINITY;
+        mx = fmaxf(mx, v);
+      }
+      mx *= sc;  // sc > 0 (or NaN for a NaN q row)
+      // both halves of a row agree on its maximum through shared memory; the barrier also orders
+      // this tile's S reads (both halves) before the P writes that overwrite S columns 0-63
+      bar.rowmax[j & 1][h][i] = mx;
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      mx = fmaxf(mx, bar.rowmax[j & 1][h ^ 1][i]);
       bool rescale = false;
       float alpha = 1.0f;
       if (m_run == -INFINITY || mx > m_run + kRescaleThreshold) {
@@ -463,62 +474,60 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      // pass 2: P = exp2(s - m), row sum, bf16 pairs written over the consumed S columns
+      // P = exp2(s*sc - m) packed to bf16 pairs; the row sum uses the rounded weights that the PV
+      // MMA multiplies, so the result is a convex combination of V rows
+      uint32_t pk[32];
       float lsum = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
+        if (need_mask && 2 * e > lim) s0 = -INFINITY;
+        if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
+        const float e0 = ex2_approx(fmaf(s0, sc, -m_use)), e1 = ex2_approx(fmaf(s1, sc, -m_use));
+        pk[e] = pack_bf16x2(e0, e1);
+        lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+      }
+      l_run += lsum;
+      if (!dead) {
+        tmem_st_32x32b_x32(sb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
+        tmem_wait_st();
+        // O may be touched only once PV_{j-1} has completed
+        if (j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
+      }
+      if (!dead) {
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            const uint32_t oa = tmem + lane_off + kColO + 128 * h + cc * 32;
+            tmem_ld_32x32b_x32(oa, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st_32x32b_x32(oa, v);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+      }
+    }
+    // epilogue: O / l -> bf16, each half writes its 128 output columns of the row
+    bool fin = !dead && !*abort && n_tiles > 0;
+    fin = fin && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    fin = __all_sync(0xffffffffu, fin);
+    bar.rowmax[n_tiles & 1][h][i] = l_run;  // the slots of the parity no later tile reads
+    named_bar_sync(1, 256);
+    const float l_tot = l_run + bar.rowmax[n_tiles & 1][h ^ 1][i];
+    if (fin) {
+      tc_fence_after();
+      const float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(tok0 + i) * p.num_q_heads + qh) * kD + 128 * h);
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(sb + cc * 32, v);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = cc * 32 + 2 * e;
-          float s0 = __uint_as_float(v[2 * e]) * (kInt8 ? sc * ks[col] : sc);
-          float s1 = __uint_as_float(v[2 * e + 1]) * (kInt8 ? sc * ks[col + 1] : sc);
-          if (need_mask && col > lim) s0 = -INFINITY;
-          if (need_mask && col + 1 > lim) s1 = -INFINITY;
-          const float e0 = ex2_approx(s0 - m_use), e1 = ex2_approx(s1 - m_use);
-          pk[e] = pack_bf16x2(e0, e1);
-          // the row sum uses the bf16-rounded weights that the PV MMA multiplies, so the result is
-          // an exact convex combination of V rows with weights perturbed by at most 2^-9
-          lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
-        }
-        tmem_st_32x32b_x16(sb + cc * 16, pk);
-      }
-      tmem_wait_st();
-      l_run += lsum;
-      // O may be touched only once PV_{j-1} has completed
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort))) break;
-        tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      mbar_arrive(&bar.p_full);
-    }
-    // epilogue: O / l -> bf16 rows
-    bool fin = ok && !*abort && n_tiles > 0;
-    fin = fin && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
-    if (__all_sync(0xffffffffu, fin)) {
-      tc_fence_after();
-      const float inv_l = l_run > 0.0f ? 1.0f / l_run : 0.0f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(tok0 + i) * p.num_q_heads + qh) * kD);
-#pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + kColO + cc * 32, v);
+        tmem_ld_32x32b_x32(tmem + lane_off + kColO + 128 * h + cc * 32, v);
         tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
@@ -533,25 +542,36 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         }
       }
     }
-  } else if (kInt8 && warp >= 8) {
+  } else if (kInt8 && warp >= 12) {
     // ---------------------------------------------------------------------------- int8 K widening
-    const int t = (warp - 8) * 32 + lane;  // row of the K tile
+    // thread t owns key row t of each tile: its 256 int8 codes come straight from the dense scratch
+    // (16 x 16-byte loads, issued before waiting for the K tile to be free), are widened to fp16
+    // integers and stored into the swizzled K tile chunk by chunk as QK_{j-1} releases it
+    const int t = (warp - 12) * 32 + lane;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!mbar_wait(&bar.k8_full, j & 1, abort)) break;
+      const int key = j * kBN + t;
+      uint4 raw[16];
+      if (key < seq_len) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.k8 + (((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh) * kD);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) raw[q] = __ldg(src + q);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) raw[q] = make_uint4(0, 0, 0, 0);
+      }
       bool ok = true;
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) {
           ok = false;
           break;
         }
+        uint8_t* row = sK + c * kChunkBytes + t * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t q8 = 4u * (c & 1) + q;  // 16-byte piece of the int8 row within chunk c/2
-          const uint4 v = *reinterpret_cast<const uint4*>(sK8 + (c >> 1) * kChunkBytes + t * 128 +
-                                                          ((q8 ^ (t & 7)) * 16));
+        for (int q = 0; q < 4; ++q) {  // 16 codes = fp16 elements 64c + 16q .. +15
           uint4 lo, hi;
-          widen16(v, lo, hi);
-          uint8_t* row = sK + c * kChunkBytes + t * 128;
+          widen16(raw[4 * c + q], lo, hi);
           *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
           *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
         }
@@ -559,7 +579,6 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         mbar_arrive(&bar.k_full[c]);
       }
       if (!ok) break;
-      mbar_arrive(&bar.k8_free);
     }
   }
 
@@ -637,13 +656,6 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
       if (s != PKV_OK) return s;
     }
   }
-  if (int8) {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_kv_heads, (uint64_t)num_reqs * (uint64_t)max_ctx};
-    const uint64_t strides[2] = {(uint64_t)kD, (uint64_t)num_kv_heads * kD};
-    const uint32_t box[3] = {128, 1, (uint32_t)kBN};
-    pkv_status s = encode_tiled(&p.k8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, k8, dims, strides, box, "k8");
-    if (s != PKV_OK) return s;
-  }
   p.block_table = block_table;
   p.bt_stride = bt_stride;
   p.num_blocks = num_blocks;
@@ -656,6 +668,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   p.seg = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.k8_scale = k8_scale;
+  p.k8 = k8;
   p.max_ctx = max_ctx;
   p.num_kv_heads = num_kv_heads;
   p.n_mtiles = (max_q_len + kBM - 1) / kBM;
