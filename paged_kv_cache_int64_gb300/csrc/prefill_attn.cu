@@ -7,11 +7,12 @@
 // block table with the block id widened to int64 before the stride product.
 //
 // sm_103a design (one CTA = 128 query rows of one query head of one request):
-//   warp 0      TMA producer: Q once; per 128-key tile, K and V gathered from the paged pool in
-//               segments of gcd(block_size, 128) keys with a 4-D tensor map
-//               [head_dim, kv_heads, block_size, num_blocks] whose block coordinate is the block
-//               id (the TMA unit forms the 64-bit address); one lane per segment reads the table
-//               and issues that segment's copies; the next tile's block ids are read early.
+//   warp 0      TMA producer: Q once; per 128-key tile, K and V gathered from the paged pool with
+//               4-D tensor maps [head_dim, kv_heads, block_size, num_blocks] whose block
+//               coordinate is the block id (the TMA unit forms the 64-bit address): a tile inside
+//               one block is 4 copies of 128 rows per tensor; a tile across blocks is split into
+//               segments of gcd(block_size, 128) keys, one lane per segment reading the table; the
+//               next tile's block ids are read early.
 //   warp 1      MMA issuer (one thread): S = Q K^T (tcgen05.mma kind::f16, M=128 N=128 K=256,
 //               both operands in shared memory, f32 accumulator in tensor memory), then
 //               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
@@ -77,6 +78,9 @@ struct Params {
   CUtensorMap qmap;   // bf16 q: dims {D, Hq, total_q}, box {64, 1, 128}
   CUtensorMap kmap;   // bf16 pool: dims {D, Hkv, bs, nb}, box {64, 1, G, 1}
   CUtensorMap vmap;
+  CUtensorMap kmap_big;  // same pool, box {64, 1, 128, 1}: a whole tile inside one block (bs >= 128)
+  CUtensorMap vmap_big;
+  int32_t big_ok;        // block_size >= 128
   const int8_t* k8;   // int8 scratch [R][max_ctx][Hkv][D] (read row by row by the converter)
   const int32_t* block_table;
   int64_t bt_stride;
@@ -242,6 +246,10 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       prefetch_tensormap(&p.qmap);
       prefetch_tensormap(&p.vmap);
       if (!kInt8) prefetch_tensormap(&p.kmap);
+      if (p.big_ok) {
+        prefetch_tensormap(&p.vmap_big);
+        if (!kInt8) prefetch_tensormap(&p.kmap_big);
+      }
       mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
       for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
     }
@@ -264,6 +272,8 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       uint32_t bad;      // segments with a bad table entry
       uint32_t nloaded;  // segments with a valid block
       bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
+      bool big;          // the 128 keys lie in one valid block: 4 copies of 128 rows per tensor
+      int blk0, slot0;   // block and first slot of key 0 of the tile
     };
     auto info = [&](int j) -> TileInfo {
       TileInfo t;
@@ -271,7 +281,15 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       t.bad = __ballot_sync(0xffffffffu, t.blk == -2);
       t.nloaded = __popc(__ballot_sync(0xffffffffu, t.blk >= 0));
       t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
+      t.blk0 = __shfl_sync(0xffffffffu, t.blk, 0);
+      t.slot0 = (j * kBN) % p.block_size;
+      t.big = p.big_ok && t.bad == 0 && t.blk0 >= 0 && t.slot0 + kBN <= p.block_size;
       return t;
+    };
+    // a whole tile of one tensor with 4 copies of [128 rows][64 x 16-bit] (lane 0)
+    auto issue_big = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, const TileInfo& t) {
+      if (lane == 0)
+        for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes, map, mb, c * 64, kvh, t.slot0, t.blk0);
     };
     uint32_t fix_phase = 0;
     // K tile j through k_full[c] (bf16) or the K8 stage (int8), chunk by chunk as QK_{j-1} frees it.
@@ -298,6 +316,17 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         __syncwarp();
         if (lane == 0)
           for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
+        __syncwarp();
+        return;
+      }
+      if (t.big) {
+        if (lane == 0) {
+          for (int c = 0; c < 4; ++c) {
+            if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
+            mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+            tma_load_4d(sK + c * kChunkBytes, &p.kmap_big, &bar.k_full[c], c * 64, kvh, t.slot0, t.blk0);
+          }
+        }
         __syncwarp();
         return;
       }
@@ -329,15 +358,17 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       __syncwarp();
       if (*abort) break;
       if (!cur.fix) {
-        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, 4u * cur.nloaded * seg_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
         __syncwarp();
-        if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
+        if (cur.big) issue_big(sV, &p.vmap_big, &bar.v_full, cur);
+        else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
       } else {
         // V rows past seq_len or in a bad segment must be zero (P is 0 there, but 0 * NaN is not):
         // load through the private barrier, zero those rows, then publish.
-        if (lane == 0) mbar_arrive_expect_tx(&bar.fix, 4u * cur.nloaded * seg_bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&bar.fix, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
         __syncwarp();
-        if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
+        if (cur.big) issue_big(sV, &p.vmap_big, &bar.fix, cur);
+        else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
         if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
         ++fix_phase;
         __syncwarp();
@@ -654,6 +685,16 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
     if (!int8) {
       s = encode_tiled(&p.kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k_cache, dims, strides, box, "k_cache");
       if (s != PKV_OK) return s;
+    }
+    p.big_ok = block_size >= kBN;
+    if (p.big_ok) {
+      const uint32_t big[4] = {64, 1, (uint32_t)kBN, 1};
+      s = encode_tiled(&p.vmap_big, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v_cache, dims, strides, big, "v_cache");
+      if (s != PKV_OK) return s;
+      if (!int8) {
+        s = encode_tiled(&p.kmap_big, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k_cache, dims, strides, big, "k_cache");
+        if (s != PKV_OK) return s;
+      }
     }
   }
   p.block_table = block_table;

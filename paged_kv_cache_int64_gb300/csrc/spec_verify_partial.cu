@@ -11,18 +11,23 @@
 // M dimension (the verify step is HBM-bound at ~63 flop per cache byte, beyond CUDA cores):
 //   warp 0     TMA producer: Q once; per 128-key tile, int8 K, int8 V (4-D maps over the paged
 //              pool, block id as a coordinate) and the fp32 K/V scales (3-D maps, same block id)
-//              into a double-buffered stage.
+//              into a double-buffered stage: 6 copies for a tile inside one block, per-segment
+//              copies (gcd(block_size, 128) keys) for a tile across blocks.
 //   warp 1     MMA issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
-//              from tensor memory, Q fp16 in shared memory), then O^T += V^T P^T (two M=128
-//              halves of head_dim, N=32, K=128 keys; V MN-major fp16 and P^T fp16 in shared memory).
-//   warps 4-7  thread k owns key k of the tile: widen its int8 K row to fp16 integers straight
-//              into tensor memory and its int8 V row into the shared V tile (byte-permute
-//              conversion: fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one subtraction of
-//              1152 gives b exactly - the int8->fp16 method of Kim et al. 2022, "Who Says
-//              Elephants Can't Run"); fold the K scale into its score and the V scale into its P
-//              entry; online softmax per query column (column max by warp butterfly + shared
-//              memory across warps; the running max moves only when it grows by more than 2^8);
-//              at the end, column sums, normalised partial O and its log-sum-exp.
+//              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory),
+//              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
+//              and P^T fp16 in shared memory).
+//   warps 8-11 converter: thread k owns key row k: widens its K row into the tile's tensor-memory
+//              K buffer (two buffers, so tile j+1 is widened while tile j is scored) and, once the
+//              previous PV has read the V tile, its V row into shared memory. int8 -> fp16 by byte
+//              permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one subtraction of 1152
+//              gives b exactly - the int8->fp16 method of Kim et al. 2022, "Who Says Elephants
+//              Can't Run"); e4m3 -> fp16 by the hardware conversion (exact).
+//   warps 4-7  softmax: thread k owns key k's 32 scores (TMEM lane k of S^T); the K scale folds
+//              into its scores and the V scale into its P^T entry; column maxima by redux.sync per
+//              warp and shared memory across the four warps; the running max moves only when it
+//              grows by more than 2^8; at the end, column sums, normalised partial O and its
+//              log-sum-exp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,15 +41,15 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
 constexpr int kPChunk = kNQ * 128;      // fp16 P^T [32 rows][64 keys] swizzled chunk
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColK = 0;    // 128 columns: fp16 K rows, two per column
-constexpr uint32_t kColS = 128;  // 32 columns: S^T
-constexpr uint32_t kColO = 160;  // 2 x 32 columns: O^T halves
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; }    // 2 x 128: fp16 K rows
+__host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
+constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
 constexpr float kRescaleThreshold = 8.0f;
 
 // shared memory layout (1024-aligned)
@@ -59,17 +64,19 @@ constexpr int kOffV16 = kOffStage + 2 * kStageBytes;
 constexpr int kOffP = kOffV16 + 4 * kChunk16;
 constexpr int kTiles = kOffP + 2 * kPChunk;
 
-struct Barriers {
+struct alignas(16) Barriers {
   uint64_t q_full, q_ready;
-  uint64_t st_full[2], st_free[2];
-  uint64_t kv_ready;  // K in TMEM and V in shared memory for tile j
-  uint64_t qk_done;   // S^T_j ready, K free
-  uint64_t p_full;    // P^T_j written, O^T rescaled
-  uint64_t pv_done;   // PV_j complete
+  uint64_t st_full[2], st_free[2];  // stage ring (freed by the converter and the softmax warps)
+  uint64_t k_ready[2], k_free[2];   // K_j in TMEM buffer j%2; QK_j done with it
+  uint64_t v_ready;                 // V_j widened into shared memory
+  uint64_t s_full[2];               // S^T_j in TMEM buffer j%2
+  uint64_t p_full;                  // P^T_j written, O^T rescaled
+  uint64_t pv_done;                 // PV_j complete (V and P^T buffers free, O^T current)
   uint32_t tmem_base;
   int abort;
-  uint32_t bad[2];          // per stage: segments whose block id was out of range
-  float red[2][4][kNQ];     // per-warp column partials
+  uint32_t bad[2];                  // per stage: segments whose block id was out of range
+  alignas(16) float red[2][4][kNQ]; // per-warp column maxima (and the final column sums); read as float4
+  float alpha[kNQ];                 // this tile's rescale factors (the same in every softmax thread)
 };
 
 struct Params {
@@ -78,6 +85,11 @@ struct Params {
   CUtensorMap v8map;
   CUtensorMap ksmap;  // fp32 scales: dims {Hkv, bs, nb}, box {4, G, 1}
   CUtensorMap vsmap;
+  CUtensorMap k8map_big;  // box {128, 1, 128, 1}: a whole tile inside one block (bs >= 128)
+  CUtensorMap v8map_big;
+  CUtensorMap ksmap_big;  // box {4, 128, 1}
+  CUtensorMap vsmap_big;
+  int32_t big_ok;
   const int32_t* block_table;
   int64_t bt_stride, num_blocks;
   int32_t max_blocks;
@@ -175,10 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     mbar_init(&bar.q_ready, 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.st_full[s], 1);
-      mbar_init(&bar.st_free[s], 128);
+      mbar_init(&bar.st_free[s], 256);
+      mbar_init(&bar.k_ready[s], 128);
+      mbar_init(&bar.k_free[s], 1);
+      mbar_init(&bar.s_full[s], 1);
     }
-    mbar_init(&bar.kv_ready, 128);
-    mbar_init(&bar.qk_done, 1);
+    mbar_init(&bar.v_ready, 128);
     mbar_init(&bar.p_full, 128);
     mbar_init(&bar.pv_done, 1);
     bar.abort = 0;
@@ -194,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
+  const int G = p.seg;
 
   if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
-    const int G = p.seg;
     const int nseg = kBN / G;
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, 4 * kQChunk);
@@ -220,13 +234,28 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       const uint32_t bad = __ballot_sync(0xffffffffu, blk == -2);
       const uint32_t nloaded = __popc(__ballot_sync(0xffffffffu, blk >= 0));
+      const int blk0 = __shfl_sync(0xffffffffu, blk, 0);
+      const int slot0 = key0 % p.block_size;
+      // the 128 keys lie in one valid block: 2 copies of 128 rows per code tensor (+ 1 per scale)
+      const bool big = p.big_ok && bad == 0 && blk0 >= 0 && slot0 + kBN <= p.block_size;
       if (lane == 0) {
         if (bad) record_error(p.dev_err, kErrDeviceBounds);
         bar.bad[st] = bad;
-        mbar_arrive_expect_tx(&bar.st_full[st], nloaded * (uint32_t)G * (kFp8 ? 4u * 128u : 4u * 128u + 2u * 16u));
+        const uint32_t rows = big ? (uint32_t)kBN : nloaded * (uint32_t)G;
+        mbar_arrive_expect_tx(&bar.st_full[st], rows * (kFp8 ? 4u * 128u : 4u * 128u + 2u * 16u));
+        if (big) {
+          for (int c = 0; c < 2; ++c) {
+            tma_load_4d(stage + kStageK8 + c * kChunk8, &p.k8map_big, &bar.st_full[st], c * 128, kvh, slot0, blk0);
+            tma_load_4d(stage + kStageV8 + c * kChunk8, &p.v8map_big, &bar.st_full[st], c * 128, kvh, slot0, blk0);
+          }
+          if (!kFp8) {
+            tma_load_3d(stage + kStageKS, &p.ksmap_big, &bar.st_full[st], (kvh & ~3), slot0, blk0);
+            tma_load_3d(stage + kStageVS, &p.vsmap_big, &bar.st_full[st], (kvh & ~3), slot0, blk0);
+          }
+        }
       }
       __syncwarp();
-      if (blk >= 0) {
+      if (!big && blk >= 0) {
         const int slot = (key0 + lane * G) % p.block_size;
         for (int c = 0; c < 2; ++c) {
           tma_load_4d(stage + kStageK8 + c * kChunk8 + lane * G * 128, &p.k8map, &bar.st_full[st], c * 128, kvh,
@@ -246,37 +275,43 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       constexpr uint32_t id_qk = idesc_f16(128, kNQ, false, false, false);
       constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
       const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
-      bool ok = mbar_wait(&bar.q_ready, 0, abort);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (!mbar_wait(&bar.kv_ready, j & 1, abort)) break;
-        tc_fence_after();
-        for (int ks = 0; ks < 16; ++ks)
-          umma_f16_ts(tmem + kColS, tmem + kColK + ks * 8,
-                      smem_desc(q_base + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
-        umma_commit(&bar.qk_done);
-        if (!mbar_wait(&bar.p_full, j & 1, abort)) break;
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(&bar.p_full, i & 1, abort)) return false;
+        if (!mbar_wait(&bar.v_ready, i & 1, abort)) return false;
         tc_fence_after();
         for (int hh = 0; hh < 2; ++hh)
           for (int ks = 0; ks < 8; ++ks)
             umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
                         smem_desc(p_base + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
-                        (j > 0 || ks > 0) ? 1u : 0u);
+                        (i > 0 || ks > 0) ? 1u : 0u);
         umma_commit(&bar.pv_done);
+        return true;
+      };
+      bool ok = mbar_wait(&bar.q_ready, 0, abort);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(&bar.k_ready[st], (j >> 1) & 1, abort)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < 16; ++ks)
+          umma_f16_ts(tmem + col_s(st), tmem + col_k(st) + ks * 8,
+                      smem_desc(q_base + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
+        umma_commit(&bar.s_full[st]);
+        umma_commit(&bar.k_free[st]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
+      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------------------------- keys / softmax
-    const int quarter = warp - 4;
-    const int k = quarter * 32 + lane;  // key row of the tile (TMEM lane k)
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------------------- converter
+    // thread k owns key row k of each tile: int8 (or e4m3) K row -> fp16 into TMEM lane k of the
+    // tile's K buffer, V row -> fp16 into the MN-major V tile; rows outside the split (or in a bad
+    // block) are written as zeros (0 * NaN would not vanish in the MMA)
+    const int quarter = warp & 3;
+    const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int G = p.seg;
-    const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
-    const float v_descale = kFp8 ? __ldg(p.v_descale) : 0.0f;
-    // Q: bf16 -> fp16 in place (32 rows x 256)
-    bool ok = mbar_wait(&bar.q_full, 0, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    bool dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
+    if (!dead) {  // Q: bf16 -> fp16 in place (32 rows x 256); row k & 31, chunk k >> 5
       const int row = k & 31, c = k >> 5;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -293,34 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       fence_proxy_async_smem();
       mbar_arrive(&bar.q_ready);
     }
-    float m_run[kNQ], l_part[kNQ];
-#pragma unroll
-    for (int q = 0; q < kNQ; ++q) {
-      m_run[q] = -INFINITY;
-      l_part[q] = 0.0f;
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
+    for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
       const uint8_t* stage = smem + kOffStage + st * kStageBytes;
       bool got = mbar_wait(&bar.st_full[st], (j >> 1) & 1, abort);
-      if (got && j > 0) got = mbar_wait(&bar.qk_done, (j - 1) & 1, abort) && mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      if (got && j >= 2) got = mbar_wait(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int key = k_begin + j * kBN + k;
-      const bool bad = (bar.bad[st] >> (k / G)) & 1u;
-      const bool in_range = key < k_end;
-      float ks = 0.0f, vs = 0.0f;
-      const bool live = in_range && !bad;  // a key of this split with a valid block
-      if (live) {
-        if (kFp8) {
-          ks = k_descale;
-          vs = v_descale;
-        } else {
-          ks = reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)];
-          vs = reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)];
-        }
-      }
-      // K row -> fp16 into TMEM lane k; V row -> fp16 into the MN-major V tile
+      const bool live = (k_begin + j * kBN + k < k_end) && !((bar.bad[st] >> (k / G)) & 1u);
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t kv[32];
@@ -334,8 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 #pragma unroll
           for (int e = 0; e < 8; ++e) kv[8 * i + e] = live ? o[e] : 0u;
         }
-        tmem_st_32x32b_x32(tmem + lane_off + kColK + 32 * w4, kv);
+        tmem_st_32x32b_x32(tmem + lane_off + col_k(st) + 32 * w4, kv);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar.k_ready[st]);
+      // V waits until PV_{j-1} has finished reading the V tile
+      got = j == 0 || mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      if (!__all_sync(0xffffffffu, got)) break;
 #pragma unroll 1
       for (int c8 = 0; c8 < 2; ++c8) {
 #pragma unroll
@@ -345,101 +366,154 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           uint32_t o[8];
           widen16<kFp8>(v, o);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = live ? o[e] : 0u;  // rows past the split: zero (0 * NaN != 0)
+          for (int e = 0; e < 8; ++e) o[e] = live ? o[e] : 0u;
           uint8_t* row = sV16 + (2 * c8 + (q8 >> 2)) * kChunk16 + k * 128;
           const uint32_t piece = 2u * (q8 & 3);
           *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<uint4*>(row + (((piece + 1) ^ (k & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
-      tc_fence_before();
+      mbar_arrive(&bar.v_ready);
       mbar_arrive(&bar.st_free[st]);
-      mbar_arrive(&bar.kv_ready);
-      // scores of key k against the 32 query columns
-      got = mbar_wait(&bar.qk_done, j & 1, abort);
-      if (!__all_sync(0xffffffffu, got)) break;
-      tc_fence_after();
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------------------- softmax
+    // thread k holds key k's scores against the 32 query columns (TMEM lane k of S^T); column
+    // maxima by redux.sync per warp and shared memory across the four warps; every thread keeps
+    // the same running maxima
+    const int quarter = warp & 3;
+    const int k = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
+    const float v_descale = kFp8 ? __ldg(p.v_descale) : 0.0f;
+    float m_run[kNQ], l_part[kNQ];
+#pragma unroll
+    for (int q = 0; q < kNQ; ++q) {
+      m_run[q] = -INFINITY;
+      l_part[q] = 0.0f;
+    }
+    bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.st_full[st], (j >> 1) & 1, abort));
+      const int key = k_begin + j * kBN + k;
+      const bool bad = (bar.bad[st] >> (k / G)) & 1u;
+      const bool in_range = key < k_end;
+      float ks = 0.0f, vs = 0.0f;
+      if (!dead && in_range && !bad) {
+        if (kFp8) {
+          ks = k_descale;
+          vs = v_descale;
+        } else {
+          ks = reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)];
+          vs = reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)];
+        }
+      }
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
       float s[kNQ];
       {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + kColS, v);
-        tmem_wait_ld();
+        if (!dead) {
+          tc_fence_after();
+          tmem_ld_32x32b_x32(tmem + lane_off + col_s(st), v);
+          tmem_wait_ld();
+        }
         const float f = p.scale_log2 * ks;
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
-          const int t = q / p.group;
-          const bool vis = in_range && key <= prefix + t;
+          const bool vis = !dead && in_range && key <= prefix + q / p.group;
           s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
         }
       }
-      float red[kNQ];
+      // column maxima: one redux.sync per column gives the warp maximum to every lane; lane q keeps
+      // column q's and publishes it
+      float mine = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) red[q] = s[q];
-      bar.red[st][quarter][lane] = warp_reduce_columns<true>(red, lane);
+      for (int q = 0; q < kNQ; ++q) {
+        float cm;
+        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(cm) : "f"(s[q]));
+        if (lane == q) mine = cm;
+      }
+      bar.red[st][quarter][lane] = mine;
       named_bar_sync(1, 128);
-      float alpha[kNQ];
+      // P^T and O^T are touched only once PV_{j-1} has completed
+      if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
+      if (!dead) tc_fence_after();
       bool any_rescale = false;
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const float mt = fmaxf(fmaxf(bar.red[st][0][q], bar.red[st][1][q]), fmaxf(bar.red[st][2][q], bar.red[st][3][q]));
-        alpha[q] = 1.0f;
-        if (m_run[q] == -INFINITY || mt > m_run[q] + kRescaleThreshold) {
-          const float m_new = fmaxf(m_run[q], mt);
-          if (m_new != -INFINITY) {
-            const bool had = m_run[q] != -INFINITY;
-            alpha[q] = had ? ex2_approx(m_run[q] - m_new) : 0.0f;
-            any_rescale |= had;
-            m_run[q] = m_new;
+      for (int q4 = 0; q4 < kNQ / 4; ++q4) {
+        float4 w[4];
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) w[ww] = *reinterpret_cast<const float4*>(&bar.red[st][ww][4 * q4]);
+        const float mt4[4] = {fmaxf(fmaxf(w[0].x, w[1].x), fmaxf(w[2].x, w[3].x)),
+                              fmaxf(fmaxf(w[0].y, w[1].y), fmaxf(w[2].y, w[3].y)),
+                              fmaxf(fmaxf(w[0].z, w[1].z), fmaxf(w[2].z, w[3].z)),
+                              fmaxf(fmaxf(w[0].w, w[1].w), fmaxf(w[2].w, w[3].w))};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = 4 * q4 + u;
+          float alpha = 1.0f;
+          if (m_run[q] == -INFINITY || mt4[u] > m_run[q] + kRescaleThreshold) {
+            const float m_new = fmaxf(m_run[q], mt4[u]);
+            if (m_new != -INFINITY) {
+              const bool had = m_run[q] != -INFINITY;
+              alpha = had ? ex2_approx(m_run[q] - m_new) : 0.0f;
+              any_rescale |= had;
+              m_run[q] = m_new;
+            }
           }
+          // every thread computes the same alphas; each writes them and reads back its own
+          bar.alpha[q] = alpha;
+          const float mu = m_run[q] == -INFINITY ? 0.0f : m_run[q];
+          const float e = ex2_approx(s[q] - mu);
+          l_part[q] = l_part[q] * alpha + e;
+          if (!dead)  // P^T column for key k: p * v_scale, fp16
+            *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = __float2half_rn(e * vs);
         }
       }
-      // P^T column for key k: p = exp2(s - m) * v_scale, fp16; per-thread column sums
-#pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const float mu = m_run[q] == -INFINITY ? 0.0f : m_run[q];
-        const float e = ex2_approx(s[q] - mu);
-        l_part[q] = l_part[q] * alpha[q] + e;
-        const __half h = __float2half_rn(e * vs);
-        *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = h;
-      }
-      if (any_rescale) {  // identical in every thread: all hold the same running maxima
+      if (!dead) {
+        if (any_rescale) {  // identical in every thread: all hold the same running maxima
 #pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
-          tmem_wait_ld();
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < kNQ; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * alpha[q]);
-          tmem_st_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+            for (int q = 0; q < kNQ; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * bar.alpha[q]);
+            tmem_st_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+          }
+          tmem_wait_st();
         }
-        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+        mbar_arrive(&bar.st_free[st]);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bar.p_full);
     }
     // epilogue: column sums, O^T / l, log-sum-exp
-    bool fin = ok && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    bool fin = !dead && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
+    named_bar_sync(1, 128);  // every warp is past its last read of bar.red / bar.alpha
+    bar.red[0][quarter][lane] = warp_reduce_columns<false>(l_part, lane);
+    named_bar_sync(1, 128);
+    if (quarter == 0) {  // lane q: column q's sum, 1 / l and log-sum-exp
+      const float l = bar.red[0][0][lane] + bar.red[0][1][lane] + bar.red[0][2][lane] + bar.red[0][3][lane];
+      bar.alpha[lane] = l > 0.0f ? 1.0f / l : 0.0f;
+      float mq = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q)
+        if (lane == q) mq = m_run[q];
+      if (fin) {
+        const int t = lane / p.group, hh = lane % p.group;
+        const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
+        p.part_lse[(int64_t)split * p.rows + row] = l > 0.0f ? (mq + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    named_bar_sync(1, 128);
     if (fin) {
       tc_fence_after();
-      named_bar_sync(1, 128);  // every warp is past its last read of bar.red
-      bar.red[0][quarter][lane] = warp_reduce_columns<false>(l_part, lane);
-      named_bar_sync(1, 128);
-      float inv_l[kNQ];
-#pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        const float l = bar.red[0][0][q] + bar.red[0][1][q] + bar.red[0][2][q] + bar.red[0][3][q];
-        inv_l[q] = l > 0.0f ? 1.0f / l : 0.0f;
-        if (k == q) {
-          const int t = q / p.group, hh = q % p.group;
-          const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
-          p.part_lse[(int64_t)split * p.rows + row] =
-              l > 0.0f ? (m_run[q] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        }
-      }
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[32];
@@ -450,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         for (int q = 0; q < kNQ; ++q) {
           const int t = q / p.group, h2 = q % p.group;
           const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + h2;
-          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * inv_l[q];
+          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.alpha[q];
         }
       }
     }
@@ -538,6 +612,14 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
     if (s != PKV_OK) return s;
     s = encode_tiled(&p.v8map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v_cache, dims, strides, box, "v_cache");
     if (s != PKV_OK) return s;
+    p.big_ok = block_size >= kBN;
+    if (p.big_ok) {
+      const uint32_t big[4] = {128, 1, (uint32_t)kBN, 1};
+      s = encode_tiled(&p.k8map_big, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, k_cache, dims, strides, big, "k_cache");
+      if (s != PKV_OK) return s;
+      s = encode_tiled(&p.v8map_big, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, v_cache, dims, strides, big, "v_cache");
+      if (s != PKV_OK) return s;
+    }
   }
   if (!kFp8) {
     const uint64_t dims[3] = {(uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
@@ -548,6 +630,13 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
     if (s != PKV_OK) return s;
     s = encode_tiled(&p.vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_sc, dims, strides, box, "v_scale", false);
     if (s != PKV_OK) return s;
+    if (block_size >= kBN) {
+      const uint32_t big[3] = {4, (uint32_t)kBN, 1};
+      s = encode_tiled(&p.ksmap_big, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_sc, dims, strides, big, "k_scale", false);
+      if (s != PKV_OK) return s;
+      s = encode_tiled(&p.vsmap_big, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_sc, dims, strides, big, "v_scale", false);
+      if (s != PKV_OK) return s;
+    }
   } else {
     p.k_descale = k_sc;
     p.v_descale = v_sc;
