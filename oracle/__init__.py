@@ -51,6 +51,8 @@ def lib():
         L.orc_f32_to_bf16_rne.restype = C.c_uint16
         L.orc_e4m3_to_f32.argtypes = [C.c_uint8]
         L.orc_e4m3_to_f32.restype = f32
+        L.orc_f32_to_e4m3_sat.argtypes = [f32]
+        L.orc_f32_to_e4m3_sat.restype = C.c_uint8
         L.orc_set_offset_mode_for_testing.argtypes = [C.c_int]
         L.orc_quant_row_i8.argtypes = [vp, C.c_int, vp, vp]
         L.orc_kv_int8_stats_quant.argtypes = [vp, i64, i64, i64, i64, vp, i64, vp, vp, i32, i32, i32,
@@ -70,11 +72,14 @@ def lib():
                                                i32, i32, i32, i32, f32, i32, i32, vp]
         L.orc_spec_verify_partial_fp8.argtypes = [vp, vp, vp, f32, f32, i64, i64, i64, i64, vp, i64, vp, i32,
                                                   i32, i32, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp]
+        L.orc_kv_cache_write.argtypes = [C.c_int, vp, vp, vp, i64, vp, vp, i32, i64, i64, i64, i64, i32, i32, i32,
+                                         vp, vp, vp, vp, i64, i64, f32, f32]
         for name in ("orc_quant_row_i8", "orc_set_offset_mode_for_testing"):
             getattr(L, name).restype = None
         for name in ("orc_kv_int8_stats_quant", "orc_kv_fp8_dequant_dense", "orc_paged_prefill_attn",
                      "orc_dense_attn", "orc_spec_verify_attn", "orc_spec_verify_partial",
-                     "orc_spec_verify_combine", "orc_spec_verify_attn_fp8", "orc_spec_verify_partial_fp8"):
+                     "orc_spec_verify_combine", "orc_spec_verify_attn_fp8", "orc_spec_verify_partial_fp8",
+                     "orc_kv_cache_write"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -99,6 +104,11 @@ def e4m3_to_f32(code: int) -> float:
     return lib().orc_e4m3_to_f32(int(code))
 
 
+def f32_to_e4m3(x: float) -> int:
+    """OCP E4M3 code of x: round to nearest even, +-448 for larger magnitudes, 0x7F for NaN."""
+    return int(lib().orc_f32_to_e4m3_sat(float(x)))
+
+
 def f32_to_bf16(x: float) -> int:
     return lib().orc_f32_to_bf16_rne(float(x))
 
@@ -114,6 +124,43 @@ def quant_row(x_bf16: np.ndarray):
     scale = np.zeros(1, dtype=np.float32)
     lib().orc_quant_row_i8(_p(x), x.size, _p(codes), _p(scale))
     return codes, float(scale[0])
+
+
+# ---- cache write ----------------------------------------------------------------------------
+
+KV_BF16, KV_INT8, KV_FP8 = 0, 1, 2
+
+
+def kv_cache_write(kv_dtype, k_new, v_new, block_table, seq_lens, query_start_loc, k_pool, v_pool,
+                   k_scale_pool=None, v_scale_pool=None, k_scale=1.0, v_scale=1.0, inplace=False):
+    """Store the new rows k_new / v_new (uint16 bf16 bits [total][hkv][D]) into the pools (uint16
+    [nb][bs][hkv][D] for bf16, int8 / uint8 for the int8 / fp8 caches; scale pools float32
+    [nb][bs][hkv]), copies of them unless inplace (then they must be C-contiguous of that dtype);
+    returns (k_pool, v_pool, k_scale_pool, v_scale_pool) after the write and the oracle status (0,
+    or 4 when a table entry was outside the pool)."""
+    dt = {KV_BF16: np.uint16, KV_INT8: np.int8, KV_FP8: np.uint8}[kv_dtype]
+
+    def own(a, t):
+        if inplace:
+            assert a.dtype == t and a.flags.c_contiguous
+            return a
+        return np.array(a, dtype=t, copy=True)
+
+    kp, vp_ = own(k_pool, dt), own(v_pool, dt)
+    nb, bs, hkv, d = kp.shape
+    ksp = vsp = None
+    if kv_dtype == KV_INT8:
+        ksp = own(k_scale_pool, np.float32)
+        vsp = own(v_scale_pool, np.float32)
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    bt = _c(block_table, np.int32)
+    sl, qsl = _c(seq_lens, np.int32), _c(query_start_loc, np.int32)
+    rc = lib().orc_kv_cache_write(int(kv_dtype), _p(kn), _p(vn), _p(bt), bt.shape[1], _p(sl), _p(qsl), sl.size,
+                                  nb, bs * hkv * d, hkv * d, d, bs, hkv, d, _p(kp), _p(vp_), _p(ksp), _p(vsp),
+                                  bs * hkv, hkv, float(k_scale), float(v_scale))
+    if rc not in (0, 4):
+        _check(rc, "kv_cache_write")
+    return kp, vp_, ksp, vsp, rc
 
 
 # ---- A1 -----------------------------------------------------------------------------------

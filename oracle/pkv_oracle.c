@@ -18,6 +18,10 @@
  *   [P3360] vllm.cpp PR #3360 "serve fp8 KV prefill through the bf16 dense dequant": "What
  *          changed" (dequantize once per layer into a dense bf16 scratch with an identity
  *          block table and block_size = max_seq).
+ *   [P91r] the same PR #91 page, the tester's report of the int8 route (a cache stored as
+ *          int8 per token and head with its scales, "--kv-cache-dtype int8_per_token_head")
+ *          and the fp8 store with a per-tensor descale (k_descale); these are the formats the
+ *          cache write below produces.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - cache layout [num_blocks][block_size][num_kv_heads][head_dim] with explicit strides;
@@ -29,6 +33,9 @@
  *     fp32 multiply per element, ties to even; an all-zero row gives scale 0 and codes 0;
  *   - e4m3 is the OCP FP8 E4M3 format (bias 7, subnormals, no infinities, S.1111.111 = NaN);
  *   - split s of a verify request covers key positions [s*split_tokens, (s+1)*split_tokens).
+ *   - a cache write stores request r's new rows (its last q_len positions, as above) through the
+ *     block table; the int8 cache uses the quantizer above per (token, head) row, the fp8 cache
+ *     stores e4m3_rn_satfinite(x / scale) with one fp32 divide per element.
  *
  * Precision: attention is computed with double accumulators from the stored bf16 / int8 /
  * e4m3 values (at least as precise as the pages' fp32 reference); the quantizers and the fp8
@@ -77,6 +84,30 @@ float orc_e4m3_to_f32(uint8_t code) {
   else
     mag = ldexpf((float)(8 + m), e - 10);
   return s ? -mag : mag;
+}
+
+/* fp32 -> OCP E4M3, round to nearest with ties to even, saturating: every finite or infinite
+ * magnitude above the largest finite value 448 becomes +-448, NaN becomes 0x7F. Written from the
+ * format: normal numbers have a quantum of 2^(e-3) for 2^e <= |x| < 2^(e+1) (e >= -6), subnormals
+ * a quantum of 2^-9; the scaled magnitude |x| / quantum is exact, so rintf (ties to even in the
+ * default rounding mode) rounds it once. */
+uint8_t orc_f32_to_e4m3_sat(float x) {
+  if (isnan(x)) return 0x7Fu;
+  uint8_t sign = signbit(x) ? 0x80u : 0x00u;
+  float a = fabsf(x);
+  if (a >= 448.0f) return sign | 0x7Eu; /* includes infinity */
+  if (a < ldexpf(1.0f, -6)) {          /* subnormal range: code = multiple of 2^-9 */
+    int m = (int)rintf(ldexpf(a, 9));  /* 0..8; 8 is the smallest normal, code 0x08 */
+    return sign | (uint8_t)m;
+  }
+  int e2;
+  frexpf(a, &e2); /* a = f * 2^e2, f in [0.5, 1) -> 2^(e2-1) <= a < 2^e2 */
+  int e = e2 - 1;
+  int m = (int)rintf(ldexpf(a, 3 - e)); /* 8..16 */
+  if (m == 16) { m = 8; e += 1; }
+  int code = ((e + 7) << 3) | (m - 8);
+  if (code > 0x7E) code = 0x7E; /* 480 does not exist: saturate */
+  return sign | (uint8_t)code;
 }
 
 /* ---------------------------------------------------------------------------------------- */
@@ -212,6 +243,64 @@ int orc_kv_fp8_dequant_dense(const uint8_t* k_fp8, const uint8_t* v_fp8, int64_t
           for (int d = 0; d < head_dim; ++d) {
             float x = off < 0 ? NAN : orc_e4m3_to_f32(src[off + d]);
             out[d] = orc_f32_to_bf16_rne(x * scale);
+          }
+        }
+      }
+    }
+  }
+  return bad ? ORC_ERR_BOUNDS : ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* cache write: a chunk's new K/V rows stored into the paged pool through the block table    */
+/* [P109 item 1 addressing; P91r cache formats]                                              */
+/* ---------------------------------------------------------------------------------------- */
+
+/* kv_dtype 0: bf16 copy. 1: int8 per (token, head) row with the quantizer above; the scale goes to
+ * scale_cache[blk * scale_stride_blk + slot * scale_stride_tok + h]. 2: e4m3 per tensor,
+ * code = orc_f32_to_e4m3_sat(x / scale). Row t of k_new / v_new ([total_tokens][hkv][D]) belongs
+ * to the request r with qsl[r] <= t < qsl[r+1] and lands at position seq_len[r] - q_len[r] +
+ * (t - qsl[r]). Rows whose table entry is outside [0, num_blocks) are not written (bounds status).
+ */
+int orc_kv_cache_write(int kv_dtype, const uint16_t* k_new, const uint16_t* v_new,
+                       const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                       const int32_t* qsl, int32_t num_reqs, int64_t num_blocks, int64_t stride_blk,
+                       int64_t stride_tok, int64_t stride_head, int32_t block_size,
+                       int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                       float* k_scale_cache, float* v_scale_cache, int64_t scale_stride_blk,
+                       int64_t scale_stride_tok, float k_scale, float v_scale) {
+  if (kv_dtype < 0 || kv_dtype > 2) return ORC_ERR_ARG;
+  int bad = 0;
+  for (int which = 0; which < 2; ++which) {
+    const uint16_t* src = which == 0 ? k_new : v_new;
+    void* dst = which == 0 ? k_cache : v_cache;
+    float* sdst = which == 0 ? k_scale_cache : v_scale_cache;
+    float tscale = which == 0 ? k_scale : v_scale;
+    paged_view v = make_view(dst, num_blocks, stride_blk, stride_tok, stride_head, block_table,
+                             bt_stride, block_size);
+    for (int r = 0; r < num_reqs; ++r) {
+      int64_t q_len = (int64_t)qsl[r + 1] - qsl[r];
+      if (q_len < 0 || q_len > seq_lens[r]) return ORC_ERR_ARG;
+      for (int64_t i = 0; i < q_len; ++i) {
+        int64_t pos = seq_lens[r] - q_len + i;
+        int64_t t = qsl[r] + i;
+        for (int h = 0; h < num_kv_heads; ++h) {
+          const uint16_t* row = src + (t * num_kv_heads + h) * head_dim;
+          int row_bad = 0;
+          int64_t off = paged_offset(&v, r, pos, h, &row_bad);
+          if (row_bad) { bad = 1; continue; }
+          if (off < 0) continue; /* planted 32-bit product left the pool: nothing written */
+          if (kv_dtype == 0) {
+            memcpy((uint16_t*)dst + off, row, sizeof(uint16_t) * head_dim);
+          } else if (kv_dtype == 1) {
+            int64_t blk = (int64_t)block_table[(int64_t)r * bt_stride + pos / block_size];
+            int64_t soff = block_base(blk, scale_stride_blk) + (pos % block_size) * scale_stride_tok + h;
+            float sc;
+            orc_quant_row_i8(row, head_dim, (int8_t*)dst + off, &sc);
+            if (soff >= 0 && soff < num_blocks * scale_stride_blk) sdst[soff] = sc;
+          } else {
+            for (int d = 0; d < head_dim; ++d)
+              ((uint8_t*)dst)[off + d] = orc_f32_to_e4m3_sat(orc_bf16_to_f32(row[d]) / tscale);
           }
         }
       }

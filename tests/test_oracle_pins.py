@@ -469,3 +469,208 @@ def test_verify_fp8_split_combine_equals_unsplit(split):
     S = int(math.ceil(p.seq_lens.max() / split))
     po, pl = oracle.spec_verify_partial_fp8(*args, T, p.num_q_heads, p.softmax_scale, split, S)
     np.testing.assert_allclose(oracle.spec_verify_combine(po, pl, p.seq_lens, T, split), full, atol=1e-6, rtol=1e-5)
+
+
+# --------------------------------------------------------------------------------------------
+# cache write (bf16 copy, int8 per token-head, e4m3 per tensor) and the e4m3 encoder
+# --------------------------------------------------------------------------------------------
+
+
+def test_e4m3_encode_round_trips_every_finite_code():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert oracle.f32_to_e4m3(oracle.e4m3_to_f32(c)) == c, hex(c)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    # torch's float32 -> float8_e4m3fn cast rounds to nearest even; below 464 it never overflows
+    vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    mids = np.array([(vals[c] + vals[c + 1]) / 2 for c in range(0x7E)], dtype=np.float32)  # exact ties
+    rng = np.random.default_rng(5)
+    x = np.concatenate([mids, -mids, rng.standard_normal(4000).astype(np.float32) * np.float32(60),
+                        rng.standard_normal(2000).astype(np.float32) * np.float32(3e-3),
+                        np.array([463.9, -463.9, 0.0, -0.0, 1e-30], dtype=np.float32)])
+    x = x[np.abs(x) < 464]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.f32_to_e4m3(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_saturates_to_448():
+    # the saturating ("satfinite") reading: every magnitude past 448, infinity included, becomes 448
+    for v in (448.0, 449.0, 464.0, 480.0, 1e6, float("inf")):
+        assert oracle.f32_to_e4m3(v) == 0x7E and oracle.f32_to_e4m3(-v) == 0xFE, v
+    assert oracle.f32_to_e4m3(float("nan")) == 0x7F
+
+
+def _write_problem(kv_dtype="bf16", q_lens=(70, 45, 33), seq_lens=(70, 80, 200), seed=31, bs=16, nb=40,
+                   hkv=2, d=32):
+    return W.make_problem("w", seed=seed, seq_lens=list(seq_lens), q_lens=list(q_lens), num_blocks=nb,
+                          block_size=bs, num_q_heads=4, num_kv_heads=hkv, head_dim=d, kv_dtype=kv_dtype)
+
+
+def _pool_shape(p):
+    return (p.num_blocks, p.block_size, p.num_kv_heads, p.head_dim)
+
+
+def test_cache_write_whole_context_rebuilds_the_pool():
+    # every position written (q_len == seq_len): the pool equals the fixture's own placement, and
+    # slots no table points at keep their poison
+    p = _write_problem(q_lens=(70, 80, 200))
+    poison = 0x7FC1
+    empty = np.full(_pool_shape(p), poison, dtype=np.uint16)
+    kp, vp, _, _, rc = oracle.kv_cache_write(oracle.KV_BF16, W.new_rows(p, "k"), W.new_rows(p, "v"),
+                                             p.block_table(), p.seq_lens, p.query_start_loc, empty, empty)
+    assert rc == 0
+    assert np.array_equal(kp, p.pool_numpy("k", fill=poison))
+    assert np.array_equal(vp, p.pool_numpy("v", fill=poison))
+
+
+def test_cache_write_chunks_compose():
+    # a context written chunk by chunk (each chunk at positions seq_len - q_len ..) equals the
+    # context written at once
+    p_all = _write_problem(q_lens=(70, 80, 200))
+    kp = np.zeros(_pool_shape(p_all), dtype=np.uint16)
+    vp = kp.copy()
+    bounds = [(0, 30), (30, 64), (64, 200)]
+    for lo, hi in bounds:
+        ends = [min(hi, L) for L in p_all.seq_lens]
+        q_lens = [max(0, e - min(lo, e)) for e in ends]
+        rows_k = np.concatenate([r.k_tok[e - q: e] for r, e, q in zip(p_all.requests, ends, q_lens)])
+        rows_v = np.concatenate([r.v_tok[e - q: e] for r, e, q in zip(p_all.requests, ends, q_lens)])
+        qsl = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+        kp, vp, _, _, rc = oracle.kv_cache_write(oracle.KV_BF16, rows_k, rows_v, p_all.block_table(),
+                                                 np.array(ends, np.int32), qsl, kp, vp)
+        assert rc == 0
+    assert np.array_equal(kp, p_all.pool_numpy("k"))
+    assert np.array_equal(vp, p_all.pool_numpy("v"))
+
+
+def test_cache_write_then_attend_equals_attention_on_the_fixture_pool():
+    # a partial chunk written into a pool that holds only the older rows: attention over the written
+    # pool is bit-identical to attention over the fixture's full pool
+    p = _write_problem()
+    owner = W.slot_owner_pool(p)
+    kfull, vfull = p.pool_numpy("k"), p.pool_numpy("v")
+    kold, vold = kfull.copy(), vfull.copy()
+    kold[owner != 0] = 0x7FC0  # NaN where the chunk's rows go
+    vold[owner != 0] = 0x7FC0
+    kp, vp, _, _, rc = oracle.kv_cache_write(oracle.KV_BF16, W.new_rows(p, "k"), W.new_rows(p, "v"),
+                                             p.block_table(), p.seq_lens, p.query_start_loc, kold, vold)
+    assert rc == 0
+    assert np.array_equal(_run_paged(p, kp, vp), _run_paged(p, kfull, vfull))
+
+
+def test_cache_write_int8_rows_are_the_quantized_new_rows():
+    p = _write_problem()
+    owner = W.slot_owner_pool(p)
+    kn, vn = W.new_rows(p, "k"), W.new_rows(p, "v")
+    z8 = np.zeros(_pool_shape(p), dtype=np.int8)
+    zs = np.full(_pool_shape(p)[:3], -1.0, dtype=np.float32)
+    kp, vp, ksp, vsp, rc = oracle.kv_cache_write(oracle.KV_INT8, kn, vn, p.block_table(), p.seq_lens,
+                                                 p.query_start_loc, z8, z8, zs, zs)
+    assert rc == 0
+    hkv = p.num_kv_heads
+    for pool, sp, rows in ((kp, ksp, kn), (vp, vsp, vn)):
+        assert np.array_equal(sp[owner == 0], zs[owner == 0])  # untouched slots keep their values
+        assert not pool[owner == 0].any()
+        for b, s, h in zip(*np.nonzero(owner)):
+            t, hh = divmod(int(owner[b, s, h]) - 1, hkv)
+            assert hh == h
+            codes, scale = oracle.quant_row(rows[t, h])
+            assert np.array_equal(pool[b, s, h], codes) and sp[b, s, h] == np.float32(scale)
+            x = W.bf16_bits_to_f32(rows[t, h]).astype(np.float64)
+            assert np.abs(x - pool[b, s, h].astype(np.float64) * scale).max() <= scale * 0.5 * (1 + 1e-5) + 1e-30
+
+
+@pytest.mark.parametrize("scale", [0.5, 2.0])
+def test_cache_write_fp8_recovers_representable_values(scale):
+    # rows that are e4m3 values times a power-of-two scale are stored exactly: the code is the
+    # original byte, and dense dequantization gives the row back bit for bit
+    p = _write_problem(kv_dtype="e4m3", q_lens=(70, 80, 200))
+    codes_k = np.concatenate([r.k_tok for r in p.requests])
+    codes_v = np.concatenate([r.v_tok for r in p.requests])
+    codes_k[(codes_k & 0x7F) == 0x7F] = 0x01  # no NaN inputs
+    codes_v[(codes_v & 0x7F) == 0x7F] = 0x01
+    codes_k[codes_k == 0x80] = 0  # -0 stores as -0 but compare the positive zero only
+    codes_v[codes_v == 0x80] = 0
+    dec = torch.from_numpy(np.stack([codes_k, codes_v])).view(torch.float8_e4m3fn).float() * scale
+    rows = dec.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16).float(), dec)  # exact bf16
+    z = np.zeros(_pool_shape(p), dtype=np.uint8)
+    kp, vp, _, _, rc = oracle.kv_cache_write(oracle.KV_FP8, rows[0], rows[1], p.block_table(), p.seq_lens,
+                                             p.query_start_loc, z, z, k_scale=scale, v_scale=scale)
+    assert rc == 0
+    off = np.concatenate([[0], np.cumsum(p.seq_lens)])
+    for i, r in enumerate(p.requests):
+        place_k = np.zeros_like(z)
+        W.place_tokens(place_k, r.blocks, codes_k[off[i]: off[i + 1]], p.block_size)
+        used = np.zeros(_pool_shape(p)[:2], dtype=bool)
+        used[np.asarray(r.blocks)[np.arange(r.seq_len) // p.block_size], np.arange(r.seq_len) % p.block_size] = True
+        assert np.array_equal(kp[used], place_k[used])
+    kd, vd = oracle.kv_fp8_dequant_dense(kp, vp, p.block_table(), p.seq_lens, 256, scale, scale)
+    for i, r in enumerate(p.requests):
+        assert np.array_equal(kd[i, : r.seq_len], rows[0][off[i]: off[i + 1]])
+        assert np.array_equal(vd[i, : r.seq_len], rows[1][off[i]: off[i + 1]])
+
+
+def test_cache_write_fp8_error_bound():
+    # general values: |decode(code) * s - x| is at most half an e4m3 step (relative 2^-4 for normals,
+    # 2^-10 absolute in the subnormal range), after the scale
+    p = _write_problem(q_lens=(30, 20, 40))
+    kn, vn = W.new_rows(p, "k"), W.new_rows(p, "v")
+    s = 0.37
+    z = np.zeros(_pool_shape(p), dtype=np.uint8)
+    kp, _, _, _, rc = oracle.kv_cache_write(oracle.KV_FP8, kn, vn, p.block_table(), p.seq_lens,
+                                            p.query_start_loc, z, z, k_scale=s, v_scale=s)
+    assert rc == 0
+    owner = W.slot_owner_pool(p)
+    dec = torch.from_numpy(kp).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    for b, sl, h in zip(*np.nonzero(owner)):
+        t, _ = divmod(int(owner[b, sl, h]) - 1, p.num_kv_heads)
+        x = W.bf16_bits_to_f32(kn[t, h]).astype(np.float64) / np.float32(s)
+        tol = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10) * (1 + 1e-6)
+        assert (np.abs(dec[b, sl, h] - x) <= tol).all()
+
+
+def test_cache_write_bad_table_entry_is_reported_and_skipped():
+    p = _write_problem()
+    bt = p.block_table()
+    bt[1, 2] = p.num_blocks + 5  # request 1, positions 32..47 (inside its new rows 35..79)
+    z = np.zeros(_pool_shape(p), dtype=np.uint16)
+    kp, _, _, _, rc = oracle.kv_cache_write(oracle.KV_BF16, W.new_rows(p, "k"), W.new_rows(p, "v"), bt,
+                                            p.seq_lens, p.query_start_loc, z, z)
+    assert rc == 4
+    good = p.block_table()
+    kref, _, _, _, _ = oracle.kv_cache_write(oracle.KV_BF16, W.new_rows(p, "k"), W.new_rows(p, "v"), good,
+                                             p.seq_lens, p.query_start_loc, z, z)
+    lost = good[1, 2]
+    kref[lost] = 0  # only the rows of the bad entry are missing
+    assert np.array_equal(kp, kref)
+
+
+def test_planted_int32_offset_breaks_top_placement_write():
+    # the last 2,048 rows of the 20,000-token request written into the 2,600-block pool: with the
+    # planted 32-bit product the top placement's rows do not land in their blocks
+    p = W.bigpool(top=True, q_len=2048)
+    kn, vn = W.new_rows(p, "k"), W.new_rows(p, "v")
+    shape = _pool_shape(p)
+    blocks = np.asarray(p.requests[0].blocks)
+    want = p.pool_numpy("k")[blocks]
+    outs = {}
+    for mode in (0, 1):
+        try:
+            oracle.set_offset_mode_for_testing(mode)
+            z = np.zeros(shape, dtype=np.uint16)
+            zv = np.zeros(shape, dtype=np.uint16)
+            kp, _, _, _, rc = oracle.kv_cache_write(oracle.KV_BF16, kn, vn, p.block_table(), p.seq_lens,
+                                                    p.query_start_loc, z, zv, inplace=True)
+        finally:
+            oracle.set_offset_mode_for_testing(0)
+        got = kp[blocks]
+        # compare only the chunk's slots: positions 17,952 .. 19,999
+        pos = np.arange(p.seq_lens[0] - 2048, p.seq_lens[0])
+        outs[mode] = np.array_equal(got[pos // p.block_size, pos % p.block_size],
+                                    want[pos // p.block_size, pos % p.block_size])
+    assert outs[0] and not outs[1]

@@ -231,6 +231,29 @@ def make_problem(name: str, *, seed: int, seq_lens, q_lens, num_blocks: int, blo
     return p
 
 
+def new_rows(p: Problem, which: str) -> np.ndarray:
+    """The chunk's new K or V rows in query order: each request's last q_len token rows,
+    concatenated as [total_q][Hkv][D] (the input of a cache write)."""
+    parts = [(r.k_tok if which == "k" else r.v_tok)[r.seq_len - r.q_len: r.seq_len] for r in p.requests]
+    return np.ascontiguousarray(np.concatenate(parts, axis=0))
+
+
+def slot_owner_pool(p: Problem) -> np.ndarray:
+    """int64 [num_blocks][bs][Hkv]: for every pool slot, 1 + the index (token row, head) of
+    new_rows() stored there, 0 where no new row lands (fixture bookkeeping for cache-write tests)."""
+    pool = np.zeros((p.num_blocks, p.block_size, p.num_kv_heads), dtype=np.int64)
+    base = 0
+    for r in p.requests:
+        ids = np.zeros((r.seq_len, p.num_kv_heads), dtype=np.int64)
+        rows = np.arange(r.q_len, dtype=np.int64)[:, None] * p.num_kv_heads + np.arange(p.num_kv_heads)
+        ids[r.seq_len - r.q_len:] = 1 + base * p.num_kv_heads + rows
+        tmp = np.zeros_like(pool)
+        place_tokens(tmp, r.blocks, ids, p.block_size)
+        pool = np.where(tmp != 0, tmp, pool)
+        base += r.q_len
+    return pool
+
+
 # ---------------------------------------------------------------------------------------------
 # The five workloads (sizes from the pages; values seeded and synthetic)
 # ---------------------------------------------------------------------------------------------
