@@ -143,10 +143,11 @@ class Workload:
         self.out = [torch.empty_like(self.q) for _ in range(3)]
         self.k8 = torch.zeros((1, L, HKV, D), dtype=torch.int8, device=dev)
         self.k8s = torch.zeros((1, L, HKV), dtype=torch.float32, device=dev)
+        self.k16 = torch.zeros((1, L, HKV, D), dtype=torch.float16, device=dev)  # fp16 copy of the codes
         self.pos_begin = torch.tensor([L - CHUNK], dtype=torch.int32, device=dev)
         self.zero = torch.zeros(1, dtype=torch.int32, device=dev)
         # the earlier chunks' int8 K rows (quantized by previous steps of a real prefill)
-        pkv.kv_int8_stats_quant(self.k, self.bt, self.zero, self.sl, L, self.k8, self.k8s)
+        pkv.kv_int8_stats_quant(self.k, self.bt, self.zero, self.sl, L, self.k8, self.k8s, k16=self.k16)
         # (3): the same request as e4m3 codes (values N(0,1)*0.5: codes of N(0,1), per-tensor scale 0.5)
         pf = W.make_problem("bench_fp8", seed=2, seq_lens=[L], q_lens=[CHUNK], num_blocks=W.BIGPOOL_BLOCKS,
                             block_size=BS, kv_dtype="e4m3", placement="explicit",
@@ -191,10 +192,10 @@ class Workload:
         rec("prefill_bf16", lambda: pkv.paged_prefill_attn(self.q, self.k, self.v, self.bt, self.sl, self.qsl, CHUNK,
                                                            s, self.out[0]))
         rec("int8_quant", lambda: pkv.kv_int8_stats_quant(self.k, self.bt, self.pos_begin, self.sl, CHUNK, self.k8,
-                                                          self.k8s))
+                                                          self.k8s, k16=self.k16))
         rec("prefill_int8", lambda: pkv.paged_prefill_attn(self.q, None, self.v, self.bt, self.sl, self.qsl, CHUNK, s,
-                                                           self.out[1], qk_mode=pkv.PKV_QK_INT8, k8=self.k8,
-                                                           k8_scale=self.k8s))
+                                                           self.out[1], qk_mode=pkv.PKV_QK_INT8, k8_scale=self.k8s,
+                                                           k16=self.k16))
         rec("fp8_dequant", lambda: pkv.kv_fp8_dequant_dense(self.kf, self.vf, self.bt, self.sl, self.fscale,
                                                             self.fscale, self.kd, self.vd))
         rec("prefill_fp8_dense", lambda: pkv.paged_prefill_attn(self.q, self.kd, self.vd, self.ident, self.sl,
@@ -212,7 +213,7 @@ def algorithmic():
     pairs = prefill_pairs(L, CHUNK)
     return {
         "prefill_flops": pairs * FLOP_PER_PAIR,
-        "int8_quant_bytes": CHUNK * HKV * (2 * D + D + 4),
+        "int8_quant_bytes": CHUNK * HKV * (2 * D + D + 4 + 2 * D),  # bf16 in; int8 + scale + fp16 copy out
         "fp8_dequant_bytes": L * HKV * D * 2 * (1 + 2),
         "verify_bytes": verify_bytes([L + T_VERIFY]),
     }
@@ -574,16 +575,17 @@ def run_ncu_case(args):
         k8s = torch.zeros((1, L, HKV), dtype=torch.float32, device=dev)
         zero = torch.zeros(1, dtype=torch.int32, device=dev)
         pb = torch.tensor([L - CHUNK], dtype=torch.int32, device=dev)
+        k16 = torch.zeros((1, L, HKV, D), dtype=torch.float16, device=dev)
         if case == "prefill_int8":
-            pkv.kv_int8_stats_quant(k, bt, zero, sl, L, k8, k8s)
+            pkv.kv_int8_stats_quant(k, bt, zero, sl, L, k8, k8s, k16=k16)
         kd = torch.empty((1, L, HKV, D), dtype=torch.bfloat16, device=dev)
         vd = torch.empty_like(kd)
         sc = torch.tensor([0.5], dtype=torch.float32, device=dev)
         fns = {
             "prefill_bf16": lambda: pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, CHUNK, p.softmax_scale, out),
             "prefill_int8": lambda: pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, CHUNK, p.softmax_scale, out,
-                                                           qk_mode=pkv.PKV_QK_INT8, k8=k8, k8_scale=k8s),
-            "int8_quant": lambda: pkv.kv_int8_stats_quant(k, bt, pb, sl, CHUNK, k8, k8s),
+                                                           qk_mode=pkv.PKV_QK_INT8, k8_scale=k8s, k16=k16),
+            "int8_quant": lambda: pkv.kv_int8_stats_quant(k, bt, pb, sl, CHUNK, k8, k8s, k16=k16),
             "fp8_dequant": lambda: pkv.kv_fp8_dequant_dense(k, v, bt, sl, sc, sc, kd, vd),
         }
         fn = fns[case]

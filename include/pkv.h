@@ -70,11 +70,18 @@ typedef enum pkv_qk_mode {
                       scaled by q_scale * k_scale [P109 review, int8_qk=True] */
 } pkv_qk_mode;
 
+typedef enum pkv_kv_dtype {
+  PKV_KV_BF16 = 0, /* bf16 rows */
+  PKV_KV_INT8 = 1, /* int8 per (token, head) row with an fp32 scale per row [P91 review:
+                      "int8_per_token_head"] */
+  PKV_KV_FP8 = 2   /* OCP e4m3 bytes with one fp32 scale per tensor [P91 review: k_descale] */
+} pkv_kv_dtype;
+
 /* Message of the last failed call on this host thread ("" if none). Never NULL. */
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version of this header (incremented on any signature change). */
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 3
 PKV_API int32_t pkv_abi_version(void);
 
 /*
@@ -92,14 +99,18 @@ PKV_API int32_t pkv_abi_version(void);
  * pos_begin / pos_end: device int32 [num_reqs], 0 <= pos_begin <= pos_end <= max_ctx.
  * max_tokens: host upper bound on pos_end[r] - pos_begin[r] (sizes the grid).
  * max_blocks: columns of the block table (pos_end <= max_blocks * block_size).
+ * k16 (nullable): fp16 [num_reqs][max_ctx][num_kv_heads][head_dim]; when given, the same codes are
+ *   also written there as fp16 values (exact). GB300's tensor cores have no int8 MMA, so the
+ *   int8-QK prefill multiplies the codes as fp16; passing k16 to pkv_paged_prefill_attn lets it
+ *   read them with TMA instead of widening every K row in every query tile.
  */
 PKV_API pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_blocks, int64_t stride_blk,
                                    int64_t stride_tok, int64_t stride_head,
                                    const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                                    const int32_t* pos_begin, const int32_t* pos_end, int32_t num_reqs,
                                    int32_t max_tokens, int32_t block_size, int32_t num_kv_heads,
-                                   int32_t head_dim, int8_t* k8, float* k8_scale, int64_t max_ctx,
-                                   int32_t* dev_err, void* stream);
+                                   int32_t head_dim, int8_t* k8, float* k8_scale, void* k16,
+                                   int64_t max_ctx, int32_t* dev_err, void* stream);
 
 /*
  * kv_fp8_dequant_dense - per-tensor fp8 e4m3 K/V cache to a dense bf16 scratch, once per layer
@@ -137,7 +148,9 @@ PKV_API pkv_status pkv_kv_fp8_dequant_dense(const uint8_t* k_fp8, const uint8_t*
  *   out = sum_{j<=p} exp(s_j - m) v_j / sum_{j<=p} exp(s_j - m),   v_j from the bf16 V cache.
  * PKV_QK_INT8 reads k8 / k8_scale ([num_reqs][max_ctx][num_kv_heads][head_dim] / [...][kvh], as
  * written by pkv_kv_int8_stats_quant, covering positions 0..seq_len-1) instead of the K cache;
- * k_cache may then be NULL. PKV_QK_BF16 ignores k8, k8_scale and max_ctx.
+ * k_cache may then be NULL. When k16 (the fp16 copy of the codes that pkv_kv_int8_stats_quant
+ * writes on request) is given it is read instead of k8 (same result, faster); k8 may then be NULL.
+ * PKV_QK_BF16 ignores k8, k8_scale, k16 and max_ctx.
  * max_q_len: host upper bound on any request's q_len. total_q: host, = query_start_loc[num_reqs].
  * Requirements: head_dim == 256; block_size a multiple of 8; q, caches and strides 16-byte
  * aligned; num_q_heads a multiple of num_kv_heads.
@@ -150,7 +163,8 @@ PKV_API pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, co
                                   int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t block_size, float softmax_scale,
                                   int32_t qk_mode, const int8_t* k8, const float* k8_scale,
-                                  int64_t max_ctx, void* out, int32_t* dev_err, void* stream);
+                                  const void* k16, int64_t max_ctx, void* out, int32_t* dev_err,
+                                  void* stream);
 
 /*
  * spec_verify_attn_partial - speculative-decode verify attention over an int8 per-token-head
@@ -218,6 +232,42 @@ PKV_API pkv_status pkv_spec_verify_combine(const float* part_o, const float* par
                                    const int32_t* seq_lens, int32_t num_reqs, int32_t T,
                                    int32_t num_q_heads, int32_t head_dim, int32_t split_tokens,
                                    int32_t max_splits, void* out, void* stream);
+
+/*
+ * kv_cache_write - store a chunk's new K and V rows into the paged cache through the block table
+ * [P109 item 1 and P91 kernel excerpt: block id widened to int64 before the stride product, the
+ * int8 scales addressed by the same block id; P91 review: the int8-per-token-head and per-tensor
+ * fp8 cache formats]. The pages do not print the writer; it is the step that fills the caches the
+ * other calls read.
+ *   k_new, v_new  bf16 [total_q][num_kv_heads][head_dim]; token t at k_new + t*new_stride_tok
+ *                 (elements; >= num_kv_heads*head_dim, a multiple of 8), heads contiguous.
+ *   Row t of request r (query_start_loc[r] <= t < query_start_loc[r+1]) goes to position
+ *   seq_lens[r] - q_len + (t - query_start_loc[r]) with q_len = query_start_loc[r+1] -
+ *   query_start_loc[r] (the attention calls' chunk convention), i.e. block
+ *   block_table[r*bt_stride + pos/block_size], slot pos % block_size.
+ *   kv_dtype PKV_KV_BF16: the row is copied. PKV_KV_INT8: codes = clamp(rint(x * (127/absmax)),
+ *   -127, 127) and scale = absmax/127 (fp32 divides, ties to even; an all-zero row stores scale 0
+ *   and zero codes, a row holding a NaN a NaN scale and zero codes) into the int8 caches and
+ *   k_scale_cache / v_scale_cache [num_blocks][block_size][num_kv_heads] fp32 (element offset
+ *   blk*scale_stride_blk + slot*scale_stride_tok + h). PKV_KV_FP8: code = e4m3(x / scale) with
+ *   one fp32 divide, round to nearest even, magnitudes past 448 (infinity included) stored as
+ *   +-448, NaN as a NaN code; k_scale / v_scale are device pointers to one fp32 each.
+ *   Caches: element strides as for the other calls (elements of the cache dtype); bases 16-byte
+ *   aligned, strides multiples of 8 elements. Scale pointers of the unused formats may be NULL.
+ *   max_q_len >= every request's q_len (sizes the grid). Rows whose table entry is outside
+ *   [0, num_blocks) or past max_blocks, and every row of a request whose q_len > seq_len, are not
+ *   written and set PKV_ERR_DEVICE_BOUNDS in dev_err. Slots not addressed by a new row are untouched.
+ */
+PKV_API pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, int64_t new_stride_tok,
+                                      const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                      const int32_t* seq_lens, const int32_t* query_start_loc,
+                                      int32_t num_reqs, int32_t max_q_len, int32_t kv_dtype, void* k_cache,
+                                      void* v_cache, int64_t num_blocks, int64_t stride_blk,
+                                      int64_t stride_tok, int64_t stride_head, float* k_scale_cache,
+                                      float* v_scale_cache, int64_t scale_stride_blk,
+                                      int64_t scale_stride_tok, const float* k_scale, const float* v_scale,
+                                      int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t* dev_err, void* stream);
 
 /*
  * spec_verify_attn_noalloc - pkv_spec_verify_attn_partial followed by pkv_spec_verify_combine, with

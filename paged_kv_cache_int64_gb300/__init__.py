@@ -18,19 +18,20 @@ from . import _build
 
 __all__ = [
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA", "PKV_ERR_DEVICE_BOUNDS",
-    "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PkvError", "lib", "library_path",
-    "kv_int8_stats_quant", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
+    "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PKV_KV_BF16", "PKV_KV_INT8", "PKV_KV_FP8", "PkvError", "lib",
+    "library_path", "kv_cache_write", "kv_int8_stats_quant", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
     "spec_verify_attn_partial", "spec_verify_attn_partial_fp8", "spec_verify_combine", "EXPORTED_SYMBOLS",
 ]
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA, PKV_ERR_DEVICE_BOUNDS, PKV_ERR_TIMEOUT = range(6)
 PKV_QK_BF16, PKV_QK_INT8 = 0, 1
+PKV_KV_BF16, PKV_KV_INT8, PKV_KV_FP8 = 0, 1, 2
 
 EXPORTED_SYMBOLS = (
     "pkv_last_error", "pkv_abi_version", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense",
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
     "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
-    "pkv_spec_verify_attn_noalloc",
+    "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write",
 )
 
 library_path = _build.LIB
@@ -51,11 +52,11 @@ def _load():
     L.pkv_last_error.restype = C.c_char_p
     L.pkv_abi_version.restype = i32
     L.pkv_kv_int8_stats_quant.argtypes = [vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32, i32, i32, i32,
-                                          vp, vp, i64, vp, vp]
+                                          vp, vp, vp, i64, vp, vp]
     L.pkv_kv_fp8_dequant_dense.argtypes = [vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp]
     L.pkv_paged_prefill_attn.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32, i32, i32,
-                                         i32, i32, i32, f32, i32, vp, vp, i64, vp, vp, vp]
+                                         i32, i32, i32, f32, i32, vp, vp, vp, i64, vp, vp, vp]
     L.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.pkv_spec_verify_workspace_bytes.restype = sz
     L.pkv_spec_verify_attn_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
@@ -68,7 +69,9 @@ def _load():
     L.pkv_spec_verify_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
                                                i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp]
     L.pkv_spec_verify_attn_noalloc.restype = i32
-    for name in ("pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
+    L.pkv_kv_cache_write.argtypes = [vp, vp, i64, vp, i64, i32, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, i64,
+                                     vp, vp, i64, i64, vp, vp, i32, i32, i32, vp, vp]
+    for name in ("pkv_kv_cache_write", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
                  "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8"):
         getattr(L, name).restype = i32
     return L
@@ -108,17 +111,44 @@ def _i32(t):
 # the five calls (names of the C ABI without the pkv_ prefix)
 # ---------------------------------------------------------------------------------------------
 
+def kv_cache_write(k_new, v_new, block_table, seq_lens, query_start_loc, max_q_len, k_cache, v_cache,
+                   kv_dtype=PKV_KV_BF16, k_scale_cache=None, v_scale_cache=None, k_scale=None, v_scale=None,
+                   dev_err=None, stream=None):
+    """Store the chunk's new rows k_new / v_new (bf16 [total_q][hkv][D], token stride free) into the paged
+    caches ([nb][bs][hkv][D]: bf16, int8 with fp32 scale caches [nb][bs][hkv], or uint8 e4m3 with device
+    scalar scales k_scale / v_scale) at positions seq_lens[r] - q_len + i."""
+    nb, bs, hkv, d, sb, st, sh = _cache_strides(k_cache)
+    assert v_cache.stride() == k_cache.stride() and v_cache.shape == k_cache.shape
+    want = {PKV_KV_BF16: torch.bfloat16, PKV_KV_INT8: torch.int8, PKV_KV_FP8: torch.uint8}[kv_dtype]
+    assert k_cache.dtype == want and v_cache.dtype == want, f"cache dtype must be {want}"
+    assert k_new.dtype == torch.bfloat16 and v_new.dtype == torch.bfloat16 and k_new.stride() == v_new.stride()
+    assert k_new.dim() == 3 and k_new.stride(2) == 1 and k_new.stride(1) == d, "new rows: [total][hkv][D], heads contiguous"
+    ssb = sst = 0
+    if kv_dtype == PKV_KV_INT8:
+        assert k_scale_cache.dtype == torch.float32 and k_scale_cache.stride() == v_scale_cache.stride()
+        assert k_scale_cache.stride(2) == 1
+        ssb, sst = k_scale_cache.stride(0), k_scale_cache.stride(1)
+    _i32(block_table)
+    R = block_table.shape[0]
+    _check(lib.pkv_kv_cache_write(_ptr(k_new), _ptr(v_new), k_new.stride(0), _ptr(block_table), block_table.stride(0),
+                                  block_table.shape[1], _ptr(_i32(seq_lens)), _ptr(_i32(query_start_loc)), R,
+                                  int(max_q_len), int(kv_dtype), _ptr(k_cache), _ptr(v_cache), nb, sb, st, sh,
+                                  _ptr(k_scale_cache), _ptr(v_scale_cache), ssb, sst, _ptr(k_scale), _ptr(v_scale), bs,
+                                  hkv, d, _ptr(dev_err), _stream(stream)))
+
+
 def kv_int8_stats_quant(k_cache, block_table, pos_begin, pos_end, max_tokens, k8, k8_scale, dev_err=None,
-                        stream=None):
+                        stream=None, k16=None):
     """Per-token-head int8 quantization of the paged bf16 K cache into k8 [R][max_ctx][hkv][D] int8 and
-    k8_scale [R][max_ctx][hkv] fp32 for positions [pos_begin[r], pos_end[r])."""
+    k8_scale [R][max_ctx][hkv] fp32 for positions [pos_begin[r], pos_end[r]); k16 (optional, fp16, same
+    shape as k8) also receives the codes as fp16 values."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_cache)
     _i32(block_table)
     R = block_table.shape[0]
     assert k8.dtype == torch.int8 and k8.is_contiguous() and k8_scale.dtype == torch.float32
     _check(lib.pkv_kv_int8_stats_quant(_ptr(k_cache), nb, sb, st, sh, _ptr(block_table), block_table.stride(0),
                                        block_table.shape[1], _ptr(_i32(pos_begin)), _ptr(_i32(pos_end)), R,
-                                       int(max_tokens), bs, hkv, d, _ptr(k8), _ptr(k8_scale), k8.shape[1],
+                                       int(max_tokens), bs, hkv, d, _ptr(k8), _ptr(k8_scale), _ptr(k16), k8.shape[1],
                                        _ptr(dev_err), _stream(stream)))
 
 
@@ -137,21 +167,22 @@ def kv_fp8_dequant_dense(k_fp8, v_fp8, block_table, seq_lens, k_scale, v_scale, 
 
 
 def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_q_len, softmax_scale,
-                       out, qk_mode=PKV_QK_BF16, k8=None, k8_scale=None, dev_err=None, stream=None):
+                       out, qk_mode=PKV_QK_BF16, k8=None, k8_scale=None, dev_err=None, stream=None, k16=None):
     """Chunked causal prefill attention. q/out bf16 [total_q][Hq][D]; caches bf16 [nb][bs][hkv][D]
-    (k_cache may be None in int8 mode, which reads k8 / k8_scale from kv_int8_stats_quant)."""
+    (k_cache may be None in int8 mode, which reads k8 (or its fp16 copy k16) and k8_scale from
+    kv_int8_stats_quant)."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(v_cache)
     if k_cache is not None:
         assert k_cache.stride() == v_cache.stride() and k_cache.shape == v_cache.shape
     assert q.is_contiguous() and out.is_contiguous() and q.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
     _i32(block_table)
     R = block_table.shape[0]
-    max_ctx = 0 if k8 is None else k8.shape[1]
+    max_ctx = 0 if k8 is None and k16 is None else (k8 if k8 is not None else k16).shape[1]
     _check(lib.pkv_paged_prefill_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, sb, st, sh, _ptr(block_table),
                                       block_table.stride(0), block_table.shape[1], _ptr(_i32(seq_lens)),
                                       _ptr(_i32(query_start_loc)), R, q.shape[0], int(max_q_len), q.shape[1],
                                       hkv, d, bs, float(softmax_scale), int(qk_mode), _ptr(k8), _ptr(k8_scale),
-                                      max_ctx, _ptr(out), _ptr(dev_err), _stream(stream)))
+                                      _ptr(k16), max_ctx, _ptr(out), _ptr(dev_err), _stream(stream)))
 
 
 def spec_verify_workspace_bytes(num_tokens, num_q_heads, head_dim, max_splits) -> int:

@@ -6,10 +6,16 @@
 // int8 K into a dense scratch indexed by position with one scale per (token, head); the block id
 // is widened to int64 before it multiplies the cache stride (description item 1).
 //
-// One pass, HBM-bound: 512 B read + 256 B + 4 B written per (token, head) row. One warp per row,
+// Optionally the same codes are also written as fp16 values (exact) to a second scratch: the
+// tensor cores of sm_103a have no int8 MMA, so the int8-QK prefill multiplies the codes as fp16;
+// widening each K row once here serves the 64 query tiles that read it.
+//
+// One pass, HBM-bound: 512 B read + 256 B + 4 B written per (token, head) row (+ 512 B with the fp16
+// copy). One warp per row,
 // 16 contiguous bytes per lane (coalesced 512-byte row), the absmax reduced with warp shuffles,
 // four rows in flight per warp.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "host_common.h"
 #include "sm103.cuh"
@@ -33,6 +39,7 @@ struct QuantArgs {
   int32_t block_size, num_kv_heads;
   int8_t* k8;
   float* k8_scale;
+  __half* k16;  // optional fp16 copy of the codes
   int64_t max_ctx;
   int* dev_err;
 };
@@ -98,6 +105,7 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
       nan = __any_sync(0xffffffffu, nan);
       float scale;
       uint32_t lo = 0, hi = 0;
+      uint4 wide = make_uint4(0, 0, 0, 0);
       if (nan) {
         scale = __int_as_float(0x7fc00000);  // a NaN row: NaN scale, zero codes
       } else if (amax == 0.0f) {
@@ -106,12 +114,16 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
         scale = __fdiv_rn(amax, 127.0f);
         const float inv = __fdiv_rn(127.0f, amax);
         uint32_t b[8];
+        uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           int c = __float2int_rn(__fmul_rn(x[i], inv));
           c = max(-127, min(127, c));
           b[i] = (uint32_t)(c & 0xff);
+          const uint32_t hbits = __half_as_ushort(__int2half_rn(c));  // exact: |c| <= 127
+          if (i & 1) w[i >> 1] |= hbits << 16; else w[i >> 1] = hbits;
         }
+        wide = make_uint4(w[0], w[1], w[2], w[3]);
         lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
         hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
       }
@@ -119,6 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
       const int h = (int)(row % a.num_kv_heads);
       const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
       reinterpret_cast<uint2*>(a.k8 + o * kD)[lane] = make_uint2(lo, hi);
+      if (a.k16) reinterpret_cast<uint4*>(a.k16 + o * kD)[lane] = wide;
       if (lane == 0) a.k8_scale[o] = scale;
     }
   }
@@ -134,7 +147,7 @@ extern "C" pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_b
                                               int32_t max_blocks, const int32_t* pos_begin,
                                               const int32_t* pos_end, int32_t num_reqs, int32_t max_tokens,
                                               int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
-                                              int8_t* k8, float* k8_scale, int64_t max_ctx,
+                                              int8_t* k8, float* k8_scale, void* k16, int64_t max_ctx,
                                               int32_t* dev_err, void* stream) {
   using namespace pkv;
   clear_error();
@@ -147,10 +160,11 @@ extern "C" pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_b
   PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0, "kv_int8_stats_quant: strides must be positive");
   PKV_ARG(aligned16(k_cache) && stride_blk % 8 == 0 && stride_tok % 8 == 0 && stride_head % 8 == 0,
           "kv_int8_stats_quant: k_cache rows must be 16-byte aligned");
+  PKV_ARG(!k16 || aligned16(k16), "kv_int8_stats_quant: k16 must be 16-byte aligned");
   if (num_reqs == 0 || max_tokens == 0) return PKV_OK;
   QuantArgs a{static_cast<const __nv_bfloat16*>(k_cache), num_blocks, stride_blk, stride_tok, stride_head,
               block_table, bt_stride, max_blocks, pos_begin, pos_end, block_size, num_kv_heads,
-              k8, k8_scale, max_ctx, dev_err};
+              k8, k8_scale, static_cast<__half*>(k16), max_ctx, dev_err};
   const int64_t rows = (int64_t)max_tokens * num_kv_heads;
   const int64_t per_cta = (int64_t)kWarps * kRowsPerIter;
   int64_t want = (rows + per_cta - 1) / per_cta;

@@ -16,12 +16,14 @@
 //   warp 1      MMA issuer (one thread): S = Q K^T (tcgen05.mma kind::f16, M=128 N=128 K=256,
 //               both operands in shared memory, f32 accumulator in tensor memory), then
 //               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
-//   warp 2      tensor-memory allocation (512 columns: O 256, two S buffers of 128).
+//   warp 2      tensor-memory allocation (512 columns: O 256, S 128, two P buffers of 64). S is
+//               single-buffered and released as soon as both softmax halves hold it in registers;
+//               P (bf16 pairs) is double-buffered, so QK_{j+1} never waits for PV_{j-1}.
 //   warps 4-11  softmax, two warpgroups that split every row (score columns 0-63 / 64-127, O
 //               columns 0-127 / 128-255; row i lives in TMEM lane i): one tensor-memory read of S
 //               per tile, scale, causal mask, row maximum shared through shared memory, running
 //               max moved only when it grows by more than 2^8 (so O is rarely rescaled), exp2, P
-//               packed to bf16 into the consumed S columns, row sums of the rounded P; the
+//               packed to bf16 into its tensor-memory buffer, row sums of the rounded P; the
 //               epilogue normalises O and stores bf16.
 //   warps 12-15 int8-QK only: read the int8 K rows (dense scratch of kv_int8_stats_quant) and
 //               widen them to fp16 integers in the K tile; half 0 of the softmax quantizes the Q
@@ -47,8 +49,9 @@ constexpr int kChunkBytes = 128 * 128;  // one [128 rows][64 x 16-bit] swizzled 
 constexpr int kTileBytes = 4 * kChunkBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS0 = 256;
-constexpr uint32_t kColS1 = 384;
+constexpr uint32_t kColS = 256;   // S: 128 fp32 columns (one buffer)
+constexpr uint32_t kColP0 = 384;  // P: two buffers of 64 columns (128 bf16 keys packed in pairs)
+constexpr uint32_t kColP1 = 448;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // dynamic shared memory layout (1024-byte aligned base)
@@ -64,9 +67,13 @@ struct Barriers {
   uint64_t k_empty[4];  // chunk c of K tile j consumed by the QK MMAs
   uint64_t v_full;      // V tile j ready
   uint64_t fix;         // producer-private: copies of a tile that needs zero-filled rows
-  uint64_t s_full[2];   // S_j in TMEM
-  uint64_t p_full;      // P_j in TMEM and O rescaled
-  uint64_t pv_done;     // PV_j complete (V free, O current)
+  uint64_t s_full;      // S_j in TMEM
+  uint64_t s_free;      // S_j copied to registers by both softmax halves: QK_{j+1} may overwrite it
+  // P_j / PV_j barriers, one per tile parity: the MMA issuer waits for P_{j-1} after QK_j and the
+  // softmax for PV_{j-2}, so one barrier per kind could be two phases ahead of the phase waited
+  // for, which a parity wait cannot tell apart from the phase itself
+  uint64_t p_full[2];   // P_j in TMEM and O rescaled (256 softmax arrivals), tile parity j & 1
+  uint64_t pv_done[2];  // PV_j complete (V free, O current), tile parity j & 1
   uint32_t tmem_base;
   int abort;
   float kscale[2][kBN];  // int8: per-key scales of the tile
@@ -82,6 +89,7 @@ struct Params {
   CUtensorMap vmap_big;
   int32_t big_ok;        // block_size >= 128
   const int8_t* k8;   // int8 scratch [R][max_ctx][Hkv][D] (read row by row by the converter)
+  CUtensorMap k16map; // fp16 copy of the codes: dims {D, Hkv, R*max_ctx}, box {64, 1, 128}
   const int32_t* block_table;
   int64_t bt_stride;
   int64_t num_blocks;
@@ -98,9 +106,11 @@ struct Params {
   int* dev_err;
 };
 
-template <bool kInt8>
+// kMode 0: exact QK (bf16 K from the pool); 1: int8 QK with K widened from the int8 scratch by
+// converter warps; 2: int8 QK with K read by TMA from the fp16 copy of the codes.
+template <int kMode>
 struct Cfg {
-  static constexpr int kThreads = kInt8 ? 512 : 384;
+  static constexpr int kThreads = kMode == 1 ? 512 : 384;
   static constexpr int kTiles = kTilesEnd;
   static constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
 };
@@ -185,15 +195,17 @@ __device__ __forceinline__ void zero_rows(uint8_t* tile, int n_valid, uint32_t b
   }
 }
 
-template <bool kInt8>
-__global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
+template <int kMode>
+__global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     paged_prefill_attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kInt8>::kTiles);
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kMode>::kTiles);
+  constexpr bool kInt8 = kMode != 0;   // int8 QK (quantized Q, per-key K scales, f16 MMA)
+  constexpr bool kConv = kMode == 1;   // K widened by the converter warps
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -215,15 +227,17 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_ready, 128);
     for (int c = 0; c < 4; ++c) {
-      mbar_init(&bar.k_full[c], kInt8 ? 128 : 1);
+      mbar_init(&bar.k_full[c], kConv ? 128 : 1);
       mbar_init(&bar.k_empty[c], 1);
     }
     mbar_init(&bar.v_full, 1);
     mbar_init(&bar.fix, 1);
-    mbar_init(&bar.s_full[0], 1);
-    mbar_init(&bar.s_full[1], 1);
-    mbar_init(&bar.p_full, 256);
-    mbar_init(&bar.pv_done, 1);
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar.p_full[b], 256);
+      mbar_init(&bar.pv_done[b], 1);
+    }
     bar.abort = 0;
     fence_mbar_init();
   }
@@ -246,6 +260,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       prefetch_tensormap(&p.qmap);
       prefetch_tensormap(&p.vmap);
       if (!kInt8) prefetch_tensormap(&p.kmap);
+      if (kMode == 2) prefetch_tensormap(&p.k16map);
       if (p.big_ok) {
         prefetch_tensormap(&p.vmap_big);
         if (!kInt8) prefetch_tensormap(&p.kmap_big);
@@ -297,7 +312,19 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
     // so such a tile goes through the private barrier, is patched, then published.
     auto load_k = [&](int j, const TileInfo& t) {
       const int key0 = j * kBN;
-      if (kInt8) return;  // the converter warps read the int8 K rows themselves
+      if (kConv) return;  // the converter warps read the int8 K rows themselves
+      if (kMode == 2) {   // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
+        if (lane == 0) {
+          const int row = (int)((int64_t)r * p.max_ctx + key0);
+          for (int c = 0; c < 4; ++c) {
+            if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
+            mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+            tma_load_3d(sK + c * kChunkBytes, &p.k16map, &bar.k_full[c], c * 64, kvh, row);
+          }
+        }
+        __syncwarp();
+        return;
+      }
       if (t.bad) {
         if (lane == 0) {
           for (int c = 0; c < 4 && j > 0; ++c)
@@ -354,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       __syncwarp();
       if (*abort) break;
       // V_j once PV_{j-1} has released the V tile
-      if (lane == 0 && j > 0) mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      if (lane == 0 && j > 0) mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
       __syncwarp();
       if (*abort) break;
       if (!cur.fix) {
@@ -390,19 +417,21 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
       bool ok = mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, 0, abort);
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&bar.p_full, i & 1, abort)) return false;
+        if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
         if (!mbar_wait(&bar.v_full, i & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t a = tmem + ((i & 1) ? kColS1 : kColS0);
+        const uint32_t a = tmem + ((i & 1) ? kColP1 : kColP0);
         for (int ks = 0; ks < 8; ++ks)
           umma_f16_ts(tmem + kColO, a + ks * 8, smem_desc(v_base + ks * 2048, 16384, 1024), id_pv,
                       (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&bar.pv_done);
+        umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
       for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j >= 2 && !mbar_wait(&bar.pv_done, (j - 2) & 1, abort)) break;
-        const uint32_t dS = tmem + ((j & 1) ? kColS1 : kColS0);
+        // S is single-buffered: QK_j overwrites it once both softmax halves hold S_{j-1} in
+        // registers (PV_{j-2}, queued before QK_j, keeps the tensor pipe busy meanwhile)
+        if (j >= 1 && !mbar_wait(&bar.s_free, (j - 1) & 1, abort)) break;
+        const uint32_t dS = tmem + kColS;
         for (int c = 0; c < 4; ++c) {
           if (!mbar_wait(&bar.k_full[c], j & 1, abort)) {
             ok = false;
@@ -417,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
           umma_commit(&bar.k_empty[c]);
         }
         if (!ok) break;
-        umma_commit(&bar.s_full[j & 1]);
+        umma_commit(&bar.s_full);
         if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
       if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
@@ -457,8 +486,9 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         if (key < seq_len) v = __ldg(p.k8_scale + ((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh);
         bar.kscale[j & 1][i] = v;
       }
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[j & 1], (j >> 1) & 1, abort));
-      const uint32_t sb = tmem + lane_off + ((j & 1) ? kColS1 : kColS0);
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1, abort));
+      const uint32_t sb = tmem + lane_off + kColS;
+      const uint32_t pb = tmem + lane_off + ((j & 1) ? kColP1 : kColP0);
       uint32_t sv[64];
       if (!dead) {
         tc_fence_after();
@@ -467,6 +497,8 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         tmem_ld_32x32b_x32(sb + 64 * h, a);
         tmem_ld_32x32b_x32(sb + 64 * h + 32, b);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar.s_free);  // S may now be overwritten by QK_{j+1}
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[e] = 0u;
@@ -486,12 +518,9 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         mx = fmaxf(mx, v);
       }
       mx *= sc;  // sc > 0 (or NaN for a NaN q row)
-      // both halves of a row agree on its maximum through shared memory; the barrier also orders
-      // this tile's S reads (both halves) before the P writes that overwrite S columns 0-63
+      // both halves of a row agree on its maximum through shared memory
       bar.rowmax[j & 1][h][i] = mx;
-      tc_fence_before();
       named_bar_sync(1, 256);
-      tc_fence_after();
       mx = fmaxf(mx, bar.rowmax[j & 1][h ^ 1][i]);
       bool rescale = false;
       float alpha = 1.0f;
@@ -519,15 +548,16 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
       }
       l_run += lsum;
-      if (!dead) {
-        tmem_st_32x32b_x32(sb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
-        tmem_wait_st();
-        // O may be touched only once PV_{j-1} has completed
-        if (j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
-      }
+      // P buffer j%2 was last read by PV_{j-2}; O may be rescaled only once PV_{j-1} is done
+      if (!dead && j >= 2)
+        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
+      const bool need_o = __any_sync(0xffffffffu, rescale);
+      if (!dead && need_o && j >= 1)
+        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
       if (!dead) {
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        tmem_st_32x32b_x32(pb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
+        if (need_o) {
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t v[32];
@@ -538,15 +568,16 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
             tmem_st_32x32b_x32(oa, v);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bar.p_full);
+        mbar_arrive(&bar.p_full[j & 1]);
       }
     }
     // epilogue: O / l -> bf16, each half writes its 128 output columns of the row
     bool fin = !dead && !*abort && n_tiles > 0;
-    fin = fin && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    if (n_tiles >= 2) fin = fin && mbar_wait(&bar.pv_done[n_tiles & 1], ((n_tiles - 2) >> 1) & 1, abort);
+    fin = fin && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
     bar.rowmax[n_tiles & 1][h][i] = l_run;  // the slots of the parity no later tile reads
     named_bar_sync(1, 256);
@@ -573,7 +604,7 @@ __global__ void __launch_bounds__(Cfg<kInt8>::kThreads, 1)
         }
       }
     }
-  } else if (kInt8 && warp >= 12) {
+  } else if (kConv && warp >= 12) {
     // ---------------------------------------------------------------------------- int8 K widening
     // thread t owns key row t of each tile: its 256 int8 codes come straight from the dense scratch
     // (16 x 16-byte loads, issued before waiting for the K tile to be free), are widened to fp16
@@ -643,7 +674,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
                                              int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
                                              int32_t head_dim, int32_t block_size, float softmax_scale,
                                              int32_t qk_mode, const int8_t* k8, const float* k8_scale,
-                                             int64_t max_ctx, void* out, int32_t* dev_err, void* stream) {
+                                             const void* k16, int64_t max_ctx, void* out, int32_t* dev_err,
+                                             void* stream) {
   using namespace pkv;
   clear_error();
   PKV_UNSUP(head_dim == kD, "paged_prefill_attn: head_dim must be 256 (got %d)", head_dim);
@@ -652,7 +684,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;  // nothing to do, nothing read
   PKV_ARG(q && v_cache && block_table && seq_lens && query_start_loc && out,
           "paged_prefill_attn: null pointer argument");
-  PKV_ARG(int8 ? (k8 && k8_scale && max_ctx > 0) : (k_cache != nullptr),
+  PKV_ARG(int8 ? ((k8 || k16) && k8_scale && max_ctx > 0) : (k_cache != nullptr),
           "paged_prefill_attn: missing K source for the selected qk_mode");
   PKV_ARG(num_reqs >= 0 && total_q >= 0 && max_q_len >= 0 && num_blocks > 0 && block_size > 0 &&
               max_blocks > 0 && bt_stride >= max_blocks && num_q_heads > 0 && num_kv_heads > 0,
@@ -661,7 +693,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   PKV_UNSUP(block_size % 8 == 0, "paged_prefill_attn: block_size must be a multiple of 8 (got %d)", block_size);
   PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0, "paged_prefill_attn: strides must be positive");
   PKV_ARG(aligned16(q) && aligned16(v_cache) && aligned16(out) && (int8 || aligned16(k_cache)) &&
-              (!int8 || aligned16(k8)) && stride_blk % 8 == 0 && stride_tok % 8 == 0 && stride_head % 8 == 0,
+              (!int8 || k16 || aligned16(k8)) && (!int8 || !k16 || aligned16(k16)) && stride_blk % 8 == 0 && stride_tok % 8 == 0 && stride_head % 8 == 0,
           "paged_prefill_attn: q, caches, out and strides must be 16-byte aligned");
   PKV_ARG(softmax_scale > 0.0f, "paged_prefill_attn: softmax_scale must be positive");
   PKV_UNSUP(!int8 || (int64_t)num_reqs * max_ctx < (1ll << 31), "paged_prefill_attn: int8 scratch too large");
@@ -718,22 +750,24 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
 
   dim3 grid((unsigned)p.n_mtiles, (unsigned)num_q_heads, (unsigned)num_reqs);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (int8) {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(paged_prefill_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<true>::kSmem);
-      attr = true;
-    }
-    paged_prefill_attn_kernel<true><<<grid, Cfg<true>::kThreads, Cfg<true>::kSmem, st>>>(p);
-  } else {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(paged_prefill_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<false>::kSmem);
-      attr = true;
-    }
-    paged_prefill_attn_kernel<false><<<grid, Cfg<false>::kThreads, Cfg<false>::kSmem, st>>>(p);
+  const int mode = !int8 ? 0 : (k16 ? 2 : 1);
+  if (mode == 2) {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_kv_heads, (uint64_t)num_reqs * (uint64_t)max_ctx};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)num_kv_heads * kD * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kBN};
+    pkv_status s = encode_tiled(&p.k16map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k16, dims, strides, box, "k16");
+    if (s != PKV_OK) return s;
   }
+  auto launch = [&](auto kernel, int threads, int smem_bytes, bool& attr) {
+    if (!attr) {
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+      attr = true;
+    }
+    kernel<<<grid, threads, smem_bytes, st>>>(p);
+  };
+  static bool attr0 = false, attr1 = false, attr2 = false;
+  if (mode == 0) launch(paged_prefill_attn_kernel<0>, Cfg<0>::kThreads, Cfg<0>::kSmem, attr0);
+  else if (mode == 1) launch(paged_prefill_attn_kernel<1>, Cfg<1>::kThreads, Cfg<1>::kSmem, attr1);
+  else launch(paged_prefill_attn_kernel<2>, Cfg<2>::kThreads, Cfg<2>::kSmem, attr2);
   return check_launch("paged_prefill_attn");
 }

@@ -9,10 +9,10 @@
 // sm_103a design, one CTA = (split, KV head, request); the T tokens x g query heads that share the
 // KV head form N = 32 query columns, and the MMAs are "swapped" so the 128 keys of a tile are the
 // M dimension (the verify step is HBM-bound at ~63 flop per cache byte, beyond CUDA cores):
-//   warp 0     TMA producer: Q once; per 128-key tile, int8 K, int8 V (4-D maps over the paged
-//              pool, block id as a coordinate) and the fp32 K/V scales (3-D maps, same block id)
-//              into a double-buffered stage: 6 copies for a tile inside one block, per-segment
-//              copies (gcd(block_size, 128) keys) for a tile across blocks.
+//   warps 0, 3 TMA producers (K and V): Q once; per 128-key tile, the int8 codes (4-D maps over the
+//              paged pool, block id as a coordinate) and fp32 scales (3-D maps, same block id) of K
+//              (warp 0) and of V (warp 3), each into its own two-stage ring: 3 copies for a tile
+//              inside one block, per-segment copies (gcd(block_size, 128) keys) across blocks.
 //   warp 1     MMA issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
 //              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory),
 //              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
@@ -52,29 +52,30 @@ __host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; 
 constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
 constexpr float kRescaleThreshold = 8.0f;
 
-// shared memory layout (1024-aligned)
+// shared memory layout (1024-aligned). K and V stages are separate rings, so the K codes of tile
+// j+2 can stream in as soon as tile j's K is widened, without waiting for its V.
 constexpr int kOffQ = 0;                         // 4 x kQChunk = 16 KB
-constexpr int kStageK8 = 0;                      // within a stage
-constexpr int kStageV8 = 2 * kChunk8;
-constexpr int kStageKS = 4 * kChunk8;            // [128 keys][4] fp32
-constexpr int kStageVS = kStageKS + kBN * 16;
-constexpr int kStageBytes = kStageVS + kBN * 16;  // 68 KB
-constexpr int kOffStage = kOffQ + 4 * kQChunk;
-constexpr int kOffV16 = kOffStage + 2 * kStageBytes;
+constexpr int kStageCodes = 0;                   // within a K or V stage: [2 chunks][128 rows][128 B]
+constexpr int kStageScales = 2 * kChunk8;        // then [128 keys][4] fp32
+constexpr int kStageBytes = kStageScales + kBN * 16;  // 34 KB
+constexpr int kOffKStage = kOffQ + 4 * kQChunk;
+constexpr int kOffVStage = kOffKStage + 2 * kStageBytes;
+constexpr int kOffV16 = kOffVStage + 2 * kStageBytes;
 constexpr int kOffP = kOffV16 + 4 * kChunk16;
 constexpr int kTiles = kOffP + 2 * kPChunk;
 
 struct alignas(16) Barriers {
   uint64_t q_full, q_ready;
-  uint64_t st_full[2], st_free[2];  // stage ring (freed by the converter and the softmax warps)
-  uint64_t k_ready[2], k_free[2];   // K_j in TMEM buffer j%2; QK_j done with it
-  uint64_t v_ready;                 // V_j widened into shared memory
-  uint64_t s_full[2];               // S^T_j in TMEM buffer j%2
-  uint64_t p_full;                  // P^T_j written, O^T rescaled
-  uint64_t pv_done;                 // PV_j complete (V and P^T buffers free, O^T current)
+  uint64_t kst_full[2], kst_free[2];  // K stage ring (freed by the converter and the softmax warps)
+  uint64_t vst_full[2], vst_free[2];  // V stage ring (same)
+  uint64_t k_ready[2], k_free[2];     // K_j in TMEM buffer j%2; QK_j done with it
+  uint64_t v_ready;                   // V_j widened into shared memory
+  uint64_t s_full[2];                 // S^T_j in TMEM buffer j%2
+  uint64_t p_full;                    // P^T_j written, O^T rescaled
+  uint64_t pv_done;                   // PV_j complete (V and P^T buffers free, O^T current)
   uint32_t tmem_base;
   int abort;
-  uint32_t bad[2];                  // per stage: segments whose block id was out of range
+  uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
   alignas(16) float red[2][4][kNQ]; // per-warp column maxima (and the final column sums); read as float4
   float alpha[kNQ];                 // this tile's rescale factors (the same in every softmax thread)
 };
@@ -186,8 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_ready, 128);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar.st_full[s], 1);
-      mbar_init(&bar.st_free[s], 256);
+      mbar_init(&bar.kst_full[s], 1);
+      mbar_init(&bar.kst_free[s], 256);
+      mbar_init(&bar.vst_full[s], 1);
+      mbar_init(&bar.vst_free[s], 256);
       mbar_init(&bar.k_ready[s], 128);
       mbar_init(&bar.k_free[s], 1);
       mbar_init(&bar.s_full[s], 1);
@@ -210,18 +213,28 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
   volatile int* abort = &bar.abort;
   const int G = p.seg;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------------------- producer
+  if (warp == 0 || warp == 3) {
+    // ---------------------------------------------------------------------------- producers
+    // warp 0 streams the K codes and K scales, warp 3 the V codes and V scales, each through its
+    // own two-stage ring; both read the block table for their tiles
+    const bool is_k = warp == 0;
     const int nseg = kBN / G;
-    if (lane == 0) {
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, 4 * kQChunk);
       for (int c = 0; c < 4; ++c)
         tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T);
     }
+    uint64_t* full = is_k ? bar.kst_full : bar.vst_full;
+    uint64_t* freeb = is_k ? bar.kst_free : bar.vst_free;
+    uint32_t* badw = is_k ? bar.kbad : bar.vbad;
+    const CUtensorMap* codes = is_k ? &p.k8map : &p.v8map;
+    const CUtensorMap* codes_big = is_k ? &p.k8map_big : &p.v8map_big;
+    const CUtensorMap* scales = is_k ? &p.ksmap : &p.vsmap;
+    const CUtensorMap* scales_big = is_k ? &p.ksmap_big : &p.vsmap_big;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
-      uint8_t* stage = smem + kOffStage + st * kStageBytes;
-      if (lane == 0 && j >= 2) mbar_wait(&bar.st_free[st], ((j >> 1) - 1) & 1, abort);
+      uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
+      if (lane == 0 && j >= 2) mbar_wait(&freeb[st], ((j >> 1) - 1) & 1, abort);
       __syncwarp();
       if (*abort) break;
       const int key0 = k_begin + j * kBN;
@@ -236,37 +249,25 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const uint32_t nloaded = __popc(__ballot_sync(0xffffffffu, blk >= 0));
       const int blk0 = __shfl_sync(0xffffffffu, blk, 0);
       const int slot0 = key0 % p.block_size;
-      // the 128 keys lie in one valid block: 2 copies of 128 rows per code tensor (+ 1 per scale)
+      // the 128 keys lie in one valid block: 2 copies of 128 rows for the codes (+ 1 for scales)
       const bool big = p.big_ok && bad == 0 && blk0 >= 0 && slot0 + kBN <= p.block_size;
       if (lane == 0) {
         if (bad) record_error(p.dev_err, kErrDeviceBounds);
-        bar.bad[st] = bad;
+        badw[st] = bad;
         const uint32_t rows = big ? (uint32_t)kBN : nloaded * (uint32_t)G;
-        mbar_arrive_expect_tx(&bar.st_full[st], rows * (kFp8 ? 4u * 128u : 4u * 128u + 2u * 16u));
+        mbar_arrive_expect_tx(&full[st], rows * (kFp8 ? 2u * 128u : 2u * 128u + 16u));
         if (big) {
-          for (int c = 0; c < 2; ++c) {
-            tma_load_4d(stage + kStageK8 + c * kChunk8, &p.k8map_big, &bar.st_full[st], c * 128, kvh, slot0, blk0);
-            tma_load_4d(stage + kStageV8 + c * kChunk8, &p.v8map_big, &bar.st_full[st], c * 128, kvh, slot0, blk0);
-          }
-          if (!kFp8) {
-            tma_load_3d(stage + kStageKS, &p.ksmap_big, &bar.st_full[st], (kvh & ~3), slot0, blk0);
-            tma_load_3d(stage + kStageVS, &p.vsmap_big, &bar.st_full[st], (kvh & ~3), slot0, blk0);
-          }
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(stage + kStageCodes + c * kChunk8, codes_big, &full[st], c * 128, kvh, slot0, blk0);
+          if (!kFp8) tma_load_3d(stage + kStageScales, scales_big, &full[st], (kvh & ~3), slot0, blk0);
         }
       }
       __syncwarp();
       if (!big && blk >= 0) {
         const int slot = (key0 + lane * G) % p.block_size;
-        for (int c = 0; c < 2; ++c) {
-          tma_load_4d(stage + kStageK8 + c * kChunk8 + lane * G * 128, &p.k8map, &bar.st_full[st], c * 128, kvh,
-                      slot, blk);
-          tma_load_4d(stage + kStageV8 + c * kChunk8 + lane * G * 128, &p.v8map, &bar.st_full[st], c * 128, kvh,
-                      slot, blk);
-        }
-        if (!kFp8) {
-          tma_load_3d(stage + kStageKS + lane * G * 16, &p.ksmap, &bar.st_full[st], (kvh & ~3), slot, blk);
-          tma_load_3d(stage + kStageVS + lane * G * 16, &p.vsmap, &bar.st_full[st], (kvh & ~3), slot, blk);
-        }
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(stage + kStageCodes + c * kChunk8 + lane * G * 128, codes, &full[st], c * 128, kvh, slot, blk);
+        if (!kFp8) tma_load_3d(stage + kStageScales + lane * G * 16, scales, &full[st], (kvh & ~3), slot, blk);
       }
     }
   } else if (warp == 1) {
@@ -330,19 +331,21 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
     for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
-      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
-      bool got = mbar_wait(&bar.st_full[st], (j >> 1) & 1, abort);
+      const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
+      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
+      bool got = mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort);
       if (got && j >= 2) got = mbar_wait(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const bool live = (k_begin + j * kBN + k < k_end) && !((bar.bad[st] >> (k / G)) & 1u);
+      const bool in_range = k_begin + j * kBN + k < k_end;
+      bool live = in_range && !((bar.kbad[st] >> (k / G)) & 1u);
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t kv[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int q8 = 4 * (w4 & 1) + i;
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageK8 + (w4 >> 1) * kChunk8 + k * 128 +
+          const uint4 v = *reinterpret_cast<const uint4*>(kstage + kStageCodes + (w4 >> 1) * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
           widen16<kFp8>(v, o);
@@ -354,14 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar.k_ready[st]);
+      mbar_arrive(&bar.kst_free[st]);
       // V waits until PV_{j-1} has finished reading the V tile
       got = j == 0 || mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
+      live = in_range && !((bar.vbad[st] >> (k / G)) & 1u);
 #pragma unroll 1
       for (int c8 = 0; c8 < 2; ++c8) {
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + kStageV8 + c8 * kChunk8 + k * 128 +
+          const uint4 v = *reinterpret_cast<const uint4*>(vstage + kStageCodes + c8 * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
           widen16<kFp8>(v, o);
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       fence_proxy_async_smem();
       mbar_arrive(&bar.v_ready);
-      mbar_arrive(&bar.st_free[st]);
+      mbar_arrive(&bar.vst_free[st]);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------------------- softmax
@@ -396,20 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
-      const uint8_t* stage = smem + kOffStage + st * kStageBytes;
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.st_full[st], (j >> 1) & 1, abort));
+      const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
+      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
       const int key = k_begin + j * kBN + k;
-      const bool bad = (bar.bad[st] >> (k / G)) & 1u;
       const bool in_range = key < k_end;
-      float ks = 0.0f, vs = 0.0f;
-      if (!dead && in_range && !bad) {
-        if (kFp8) {
-          ks = k_descale;
-          vs = v_descale;
-        } else {
-          ks = reinterpret_cast<const float*>(stage + kStageKS)[k * 4 + (kvh & 3)];
-          vs = reinterpret_cast<const float*>(stage + kStageVS)[k * 4 + (kvh & 3)];
-        }
+      float ks = 0.0f;
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort));
+      if (!dead) {  // the K scale, then release this tile's K stage
+        if (in_range && !((bar.kbad[st] >> (k / G)) & 1u))
+          ks = kFp8 ? k_descale : reinterpret_cast<const float*>(kstage + kStageScales)[k * 4 + (kvh & 3)];
+        mbar_arrive(&bar.kst_free[st]);
       }
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
       float s[kNQ];
@@ -438,6 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       bar.red[st][quarter][lane] = mine;
       named_bar_sync(1, 128);
+      // the V scale, then release this tile's V stage
+      float vs = 0.0f;
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort));
+      if (!dead) {
+        if (in_range && !((bar.vbad[st] >> (k / G)) & 1u))
+          vs = kFp8 ? v_descale : reinterpret_cast<const float*>(vstage + kStageScales)[k * 4 + (kvh & 3)];
+        mbar_arrive(&bar.vst_free[st]);
+      }
       // P^T and O^T are touched only once PV_{j-1} has completed
       if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
       if (!dead) tc_fence_after();
@@ -489,7 +499,6 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar.p_full);
-        mbar_arrive(&bar.st_free[st]);
       }
     }
     // epilogue: column sums, O^T / l, log-sum-exp

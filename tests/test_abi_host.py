@@ -57,7 +57,7 @@ def test_library_targets_sm103a(libpath):
 
 
 def test_abi_version(pkv):
-    assert pkv.lib.pkv_abi_version() == 1
+    assert pkv.lib.pkv_abi_version() == 3
 
 
 def test_workspace_bytes(pkv):
@@ -69,12 +69,12 @@ def test_workspace_bytes(pkv):
 
 def _prefill_args(**kw):
     a = dict(q=16, k=16, v=16, nb=4, sb=16384, st=1024, sh=256, bt=16, bts=1, mb=1, sl=16, qsl=16, R=1, total_q=1,
-             max_q=1, hq=16, hkv=4, d=256, bs=16, scale=0.0625, mode=0, k8=None, k8s=None, max_ctx=0, out=16,
-             err=None, stream=None)
+             max_q=1, hq=16, hkv=4, d=256, bs=16, scale=0.0625, mode=0, k8=None, k8s=None, k16=None, max_ctx=0,
+             out=16, err=None, stream=None)
     a.update(kw)
     return [a[k] for k in ("q", "k", "v", "nb", "sb", "st", "sh", "bt", "bts", "mb", "sl", "qsl", "R", "total_q",
-                           "max_q", "hq", "hkv", "d", "bs", "scale", "mode", "k8", "k8s", "max_ctx", "out", "err",
-                           "stream")]
+                           "max_q", "hq", "hkv", "d", "bs", "scale", "mode", "k8", "k8s", "k16", "max_ctx", "out",
+                           "err", "stream")]
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -106,8 +106,8 @@ def test_verify_rejects_unsupported_geometry(pkv):
 
 
 def test_quant_and_dequant_reject_bad_arguments(pkv):
-    rc = pkv.lib.pkv_kv_int8_stats_quant(16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 4, 16, 4, 128, 16, 16, 8,
-                                         None, None)
+    rc = pkv.lib.pkv_kv_int8_stats_quant(16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 4, 16, 4, 128, 16, 16, None,
+                                         8, None, None)
     assert rc == 2
     rc = pkv.lib.pkv_kv_fp8_dequant_dense(16, 16, 4, 16384, 1024, 256, None, 1, 1, 16, 1, 16, 16, 4, 256, 16, 16,
                                           16, 16, None, None)
@@ -120,3 +120,35 @@ def test_empty_batches_launch_nothing(pkv):
     # num_reqs == 0 returns before any CUDA call (none is available here)
     assert pkv.lib.pkv_paged_prefill_attn(*_prefill_args(R=0, total_q=0, max_q=0)) == 0
     assert pkv.lib.pkv_spec_verify_combine(16, 16, 16, 0, 8, 16, 256, 128, 2, 16, None) == 0
+
+
+def _write_args(**kw):
+    a = dict(kn=16, vn=16, nst=1024, bt=16, bts=1, mb=1, sl=16, qsl=16, R=1, max_q=1, dt=0, kc=16, vc=16, nb=4,
+             sb=16384, st=1024, sh=256, ksc=None, vsc=None, ssb=0, sst=0, ks=None, vs=None, bs=16, hkv=4, d=256,
+             err=None, stream=None)
+    a.update(kw)
+    return [a[k] for k in ("kn", "vn", "nst", "bt", "bts", "mb", "sl", "qsl", "R", "max_q", "dt", "kc", "vc", "nb",
+                           "sb", "st", "sh", "ksc", "vsc", "ssb", "sst", "ks", "vs", "bs", "hkv", "d", "err",
+                           "stream")]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=128), 2),                 # head_dim != 256 -> unsupported
+    (dict(dt=3), 1),                  # unknown cache dtype
+    (dict(kn=None), 1),               # null pointer
+    (dict(dt=1), 1),                  # int8 cache without scale caches
+    (dict(dt=2), 1),                  # e4m3 cache without per-tensor scales
+    (dict(nst=512), 1),               # token stride shorter than a token's rows
+    (dict(kc=24), 1),                 # misaligned cache
+    (dict(st=1020), 1),               # stride not a multiple of 8 elements
+    (dict(dt=1, ksc=16, vsc=16, ssb=64, sst=2), 1),  # scale token stride < num_kv_heads
+])
+def test_cache_write_rejects_bad_arguments(pkv, kw, status):
+    rc = pkv.lib.pkv_kv_cache_write(*_write_args(**kw))
+    assert rc == status
+    assert pkv.lib.pkv_last_error().decode()
+
+
+def test_cache_write_empty_batch_launches_nothing(pkv):
+    assert pkv.lib.pkv_kv_cache_write(*_write_args(R=0)) == 0
+    assert pkv.lib.pkv_kv_cache_write(*_write_args(max_q=0, kn=None)) == 0

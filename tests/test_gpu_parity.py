@@ -114,7 +114,7 @@ def test_kv_fp8_dequant_dense_bit_exact(pkv, bs, scale):
 # A3: paged prefill attention
 # ---------------------------------------------------------------------------------------------
 
-def _run_prefill(pkv, p, mode=0, k_pool=None, v_pool=None):
+def _run_prefill(pkv, p, mode=0, k_pool=None, v_pool=None, use_k16=False):
     k = device_pool(p, "k") if k_pool is None else k_pool
     v = device_pool(p, "v") if v_pool is None else v_pool
     bt, sl, qsl = device_meta(p)
@@ -127,10 +127,18 @@ def _run_prefill(pkv, p, mode=0, k_pool=None, v_pool=None):
         k8 = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads, 256), dtype=torch.int8, device="cuda")
         ks = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads), dtype=torch.float32, device="cuda")
         pb = torch.zeros(p.num_reqs, dtype=torch.int32, device="cuda")
-        pkv.kv_int8_stats_quant(k, bt, pb, sl, max_ctx, k8, ks, dev_err=err)
+        k16 = torch.full((p.num_reqs, max_ctx, p.num_kv_heads, 256), float("nan"), dtype=torch.float16,
+                         device="cuda") if use_k16 else None
+        pkv.kv_int8_stats_quant(k, bt, pb, sl, max_ctx, k8, ks, dev_err=err, k16=k16)
+        if use_k16:  # the fp16 copy holds exactly the int8 codes of the quantized positions; the
+            # rest of the buffer is not written
+            for r, L in enumerate(p.seq_lens.tolist()):
+                assert torch.equal(k16[r, :L].float(), k8[r, :L].float())
+                assert torch.isnan(k16[r, L:]).all()
     max_q = max(r.q_len for r in p.requests)
     pkv.paged_prefill_attn(q, None if mode == 1 else k, v, bt, sl, qsl, max_q, p.softmax_scale, out,
-                           qk_mode=mode, k8=k8, k8_scale=ks, dev_err=err)
+                           qk_mode=mode, k8=None if use_k16 else k8, k8_scale=ks, dev_err=err,
+                           k16=k16 if mode == 1 and use_k16 else None)
     torch.cuda.synchronize()
     assert err.item() == 0, f"device status {err.item()}"
     return bf16_to_u16(out), (k8, ks)
@@ -154,7 +162,7 @@ def test_prefill_tiny_config_bf16(pkv):
     _close(got, ref, TOL_BF16)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])  # 2: int8 QK reading the fp16 copy of the codes
 @pytest.mark.parametrize("case", ["ragged", "gqa6", "from_scratch", "bs880"])
 def test_prefill_ragged_cases(pkv, mode, case):
     if case == "ragged":     # several requests, q_len and seq_len off every tile boundary
@@ -167,8 +175,8 @@ def test_prefill_ragged_cases(pkv, mode, case):
         p = W.make_problem("s", seed=7, seq_lens=[333], q_lens=[333], num_blocks=32, block_size=16)
     else:                    # block 880, tiles straddle blocks in 16-key segments
         p = W.make_problem("b", seed=8, seq_lens=[2000, 1000], q_lens=[300, 1000], num_blocks=40, block_size=880)
-    got, _ = _run_prefill(pkv, p, mode)
-    ref = _oracle_prefill(p, mode)
+    got, _ = _run_prefill(pkv, p, min(mode, 1), use_k16=mode == 2)
+    ref = _oracle_prefill(p, min(mode, 1))
     _close(got, ref, _edge_tol(p, TOL_INT8 if mode else TOL_BF16))
 
 
@@ -188,28 +196,30 @@ def bigpool_gpu(pkv):
     for top in (True, False):
         p = W.bigpool(top=top)
         k, v = device_pool(p, "k"), device_pool(p, "v")
-        for mode in (0, 1):
-            out[(top, mode)], _ = _run_prefill(pkv, p, mode, k_pool=k, v_pool=v)
+        for mode in (0, 1, 2):
+            out[(top, mode)], _ = _run_prefill(pkv, p, min(mode, 1), k_pool=k, v_pool=v, use_k16=mode == 2)
         del k, v
         torch.cuda.empty_cache()
         out[("p", top)] = p
     return out
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_bigpool_top_equals_bottom_bit_exact(bigpool_gpu, mode):
     top, bot = bigpool_gpu[(True, mode)], bigpool_gpu[(False, mode)]
     assert np.isfinite(W.bf16_bits_to_f32(top)).all()
     assert np.array_equal(top, bot)
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_bigpool_sampled_rows_vs_oracle(bigpool_gpu, mode):
     p = bigpool_gpu[("p", True)]
     got = bigpool_gpu[(True, mode)]
+    if mode == 2:  # the fp16 copy of the codes must give the very bytes of the converter path
+        assert np.array_equal(got, bigpool_gpu[(True, 1)])
     worst = 0.0
     for t in (0, 1, 127, 128, 1000, 2047):
-        ref = _oracle_prefill(p, mode, tok_begin=t, tok_end=t + 1)
+        ref = _oracle_prefill(p, min(mode, 1), tok_begin=t, tok_end=t + 1)
         worst = max(worst, _close(got[t:t + 1], ref, TOL_INT8 if mode else TOL_BF16))
     assert worst <= (TOL_INT8 if mode else TOL_BF16)
 
@@ -225,6 +235,7 @@ def test_int8_prefill_chunked_context(pkv):
     q_all = device_q(p)
     k8 = torch.zeros((1, ctx, 4, 256), dtype=torch.int8, device="cuda")
     ks = torch.zeros((1, ctx, 4), dtype=torch.float32, device="cuda")
+    k16 = torch.zeros((1, ctx, 4, 256), dtype=torch.float16, device="cuda")
     err = dev_err()
     outs = {}
     sched = W.chunk_schedule(ctx)
@@ -232,11 +243,11 @@ def test_int8_prefill_chunked_context(pkv):
         sl = torch.tensor([L], dtype=torch.int32, device="cuda")
         pb = torch.tensor([L - ql], dtype=torch.int32, device="cuda")
         qsl = torch.tensor([0, ql], dtype=torch.int32, device="cuda")
-        pkv.kv_int8_stats_quant(k, bt, pb, sl, ql, k8, ks, dev_err=err)
+        pkv.kv_int8_stats_quant(k, bt, pb, sl, ql, k8, ks, dev_err=err, k16=k16)
         q = q_all[L - ql:L].contiguous()
         out = torch.empty_like(q)
-        pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, ql, p.softmax_scale, out, qk_mode=1, k8=k8, k8_scale=ks,
-                               dev_err=err)
+        pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, ql, p.softmax_scale, out, qk_mode=1, k8_scale=ks,
+                               dev_err=err, k16=k16)
         if ci in (0, len(sched) // 2, len(sched) - 1):
             outs[ci] = bf16_to_u16(out)
     torch.cuda.synchronize()
