@@ -17,16 +17,19 @@
 //              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory),
 //              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
 //              and P^T fp16 in shared memory).
-//   warps 8-11 converter: thread k owns key row k: widens its K row into the tile's tensor-memory
-//              K buffer (two buffers, so tile j+1 is widened while tile j is scored) and, once the
-//              previous PV has read the V tile, its V row into shared memory. int8 -> fp16 by byte
-//              permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one subtraction of 1152
-//              gives b exactly - the int8->fp16 method of Kim et al. 2022, "Who Says Elephants
-//              Can't Run"); e4m3 -> fp16 by the hardware conversion (exact).
+//   warps 8-11 K converter: thread k owns key row k and widens it into the tile's tensor-memory K
+//              buffer (two buffers, so tile j+1 is widened while tile j is scored).
+//   warps 12-15 V converter: once the previous PV has read the V tile, thread k widens V row k into
+//              it (shared memory, MN-major). Splitting the widening keeps the K side running while
+//              the V side waits for PV. int8 -> fp16 by byte permute (fp16 bits 0x6400|(b^0x80)
+//              equal 1024 + b + 128, so one subtraction of 1152 gives b exactly - the int8->fp16
+//              method of Kim et al. 2022, "Who Says Elephants Can't Run"); e4m3 -> fp16 by the
+//              hardware conversion (exact).
 //   warps 4-7  softmax: thread k owns key k's 32 scores (TMEM lane k of S^T); the K scale folds
-//              into its scores and the V scale into its P^T entry; column maxima by redux.sync per
-//              warp and shared memory across the four warps; the running max moves only when it
-//              grows by more than 2^8; at the end, column sums, normalised partial O and its
+//              into its scores and the V scale into its P^T entry; column maxima by a shuffle
+//              reduce-scatter per warp and shared memory across the four warps, after which lane l
+//              keeps column l's running max (moved only when it grows by more than 2^8) and
+//              broadcasts it by shuffles; at the end, column sums, normalised partial O and its
 //              log-sum-exp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,7 +44,7 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
@@ -76,8 +79,8 @@ struct alignas(16) Barriers {
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
-  alignas(16) float red[2][4][kNQ]; // per-warp column maxima (and the final column sums); read as float4
-  float alpha[kNQ];                 // this tile's rescale factors (the same in every softmax thread)
+  float red[2][4][kNQ];  // per-warp column maxima (and the final column sums)
+  float inv_l[kNQ];      // epilogue: 1 / column sum
 };
 
 struct Params {
@@ -156,6 +159,22 @@ __device__ __forceinline__ float warp_reduce_columns(float (&v)[kNQ], int lane) 
     }
   }
   return v[0];
+}
+
+// Reduce-scatter of 16 columns: on entry every lane holds 16 column values; on exit every lane holds
+// the warp maximum of column (lane & 15). 16 shuffles.
+__device__ __forceinline__ float reduce_scatter16_max(float (&v)[16], int lane) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float keep = upper ? v[q + o] : v[q];
+      const float send = upper ? v[q] : v[q + o];
+      v[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
 }
 
 template <bool kFp8>
@@ -303,16 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
     }
     __syncwarp();
-  } else if (warp >= 8) {
-    // ---------------------------------------------------------------------------- converter
-    // thread k owns key row k of each tile: int8 (or e4m3) K row -> fp16 into TMEM lane k of the
-    // tile's K buffer, V row -> fp16 into the MN-major V tile; rows outside the split (or in a bad
-    // block) are written as zeros (0 * NaN would not vanish in the MMA)
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------------------------------------------------------------------- K converter
+    // thread k owns key row k of each tile: its int8 (or e4m3) K row -> fp16 into TMEM lane k of the
+    // tile's K buffer; rows outside the split (or in a bad block) are written as zeros (0 * NaN
+    // would not vanish in the MMA). First, Q bf16 -> fp16 in place (32 rows x 256).
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
-    if (!dead) {  // Q: bf16 -> fp16 in place (32 rows x 256); row k & 31, chunk k >> 5
+    if (!dead) {  // row k & 31, chunk k >> 5
       const int row = k & 31, c = k >> 5;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -332,13 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
       const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
-      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
       bool got = mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort);
       if (got && j >= 2) got = mbar_wait(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const bool in_range = k_begin + j * kBN + k < k_end;
-      bool live = in_range && !((bar.kbad[st] >> (k / G)) & 1u);
+      const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t kv[32];
@@ -358,11 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       tc_fence_before();
       mbar_arrive(&bar.k_ready[st]);
       mbar_arrive(&bar.kst_free[st]);
-      // V waits until PV_{j-1} has finished reading the V tile
-      got = j == 0 || mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+    }
+  } else if (warp >= 12) {
+    // ---------------------------------------------------------------------------- V converter
+    // thread k owns key row k: once PV_{j-1} has read the V tile, its V row -> fp16 into the
+    // MN-major V tile (zeros outside the split or in a bad block)
+    const int k = (warp & 3) * 32 + lane;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
+      bool got = j == 0 || mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
       if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
-      live = in_range && !((bar.vbad[st] >> (k / G)) & 1u);
+      const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
 #pragma unroll 1
       for (int c8 = 0; c8 < 2; ++c8) {
 #pragma unroll
@@ -385,26 +410,26 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------------------- softmax
-    // thread k holds key k's scores against the 32 query columns (TMEM lane k of S^T); column
-    // maxima by redux.sync per warp and shared memory across the four warps; every thread keeps
-    // the same running maxima
+    // thread k holds key k's 32 scores (TMEM lane k of S^T). Column maxima: a shuffle
+    // reduce-scatter leaves column l's warp maximum in lane l, shared memory combines the four
+    // warps; lane l then keeps column l's running max (the same in all four warps) and hands it
+    // to the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T.
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
     const float v_descale = kFp8 ? __ldg(p.v_descale) : 0.0f;
-    float m_run[kNQ], l_part[kNQ];
+    float l_part[kNQ];
 #pragma unroll
-    for (int q = 0; q < kNQ; ++q) {
-      m_run[q] = -INFINITY;
-      l_part[q] = 0.0f;
-    }
+    for (int q = 0; q < kNQ; ++q) l_part[q] = 0.0f;
+    float m_col = -INFINITY;  // lane l: running maximum of column l
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
-      const int key = k_begin + j * kBN + k;
+      const int key0 = k_begin + j * kBN;
+      const int key = key0 + k;
       const bool in_range = key < k_end;
       float ks = 0.0f;
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort));
@@ -423,20 +448,28 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           tmem_wait_ld();
         }
         const float f = p.scale_log2 * ks;
+        if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
 #pragma unroll
-        for (int q = 0; q < kNQ; ++q) {
-          const bool vis = !dead && in_range && key <= prefix + q / p.group;
-          s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
+          for (int q = 0; q < kNQ; ++q) s[q] = (!dead && in_range) ? __uint_as_float(v[q]) * f : -INFINITY;
+        } else {  // causal limit of column q (token q / group): key <= prefix + q / group
+#pragma unroll
+          for (int q = 0; q < kNQ; ++q) {
+            const bool vis = !dead && in_range && key <= prefix + q / p.group;
+            s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
+          }
         }
       }
-      // column maxima: one redux.sync per column gives the warp maximum to every lane; lane q keeps
-      // column q's and publishes it
-      float mine = -INFINITY;
+      // column maxima over the warp: two 16-column reduce-scatters, lane l ends with column l's
+      float mine;
+      {
+        float t[16];
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
-        float cm;
-        asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(cm) : "f"(s[q]));
-        if (lane == q) mine = cm;
+        for (int q = 0; q < 16; ++q) t[q] = s[q];
+        const float lo = reduce_scatter16_max(t, lane);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) t[q] = s[16 + q];
+        const float hi = reduce_scatter16_max(t, lane);
+        mine = lane < 16 ? lo : hi;
       }
       bar.red[st][quarter][lane] = mine;
       named_bar_sync(1, 128);
@@ -448,50 +481,42 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           vs = kFp8 ? v_descale : reinterpret_cast<const float*>(vstage + kStageScales)[k * 4 + (kvh & 3)];
         mbar_arrive(&bar.vst_free[st]);
       }
-      // P^T and O^T are touched only once PV_{j-1} has completed
-      if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
-      if (!dead) tc_fence_after();
-      bool any_rescale = false;
-#pragma unroll
-      for (int q4 = 0; q4 < kNQ / 4; ++q4) {
-        float4 w[4];
-#pragma unroll
-        for (int ww = 0; ww < 4; ++ww) w[ww] = *reinterpret_cast<const float4*>(&bar.red[st][ww][4 * q4]);
-        const float mt4[4] = {fmaxf(fmaxf(w[0].x, w[1].x), fmaxf(w[2].x, w[3].x)),
-                              fmaxf(fmaxf(w[0].y, w[1].y), fmaxf(w[2].y, w[3].y)),
-                              fmaxf(fmaxf(w[0].z, w[1].z), fmaxf(w[2].z, w[3].z)),
-                              fmaxf(fmaxf(w[0].w, w[1].w), fmaxf(w[2].w, w[3].w))};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int q = 4 * q4 + u;
-          float alpha = 1.0f;
-          if (m_run[q] == -INFINITY || mt4[u] > m_run[q] + kRescaleThreshold) {
-            const float m_new = fmaxf(m_run[q], mt4[u]);
-            if (m_new != -INFINITY) {
-              const bool had = m_run[q] != -INFINITY;
-              alpha = had ? ex2_approx(m_run[q] - m_new) : 0.0f;
-              any_rescale |= had;
-              m_run[q] = m_new;
-            }
-          }
-          // every thread computes the same alphas; each writes them and reads back its own
-          bar.alpha[q] = alpha;
-          const float mu = m_run[q] == -INFINITY ? 0.0f : m_run[q];
-          const float e = ex2_approx(s[q] - mu);
-          l_part[q] = l_part[q] * alpha + e;
-          if (!dead)  // P^T column for key k: p * v_scale, fp16
-            *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = __float2half_rn(e * vs);
+      // lane l: column l's tile maximum, running maximum and rescale factor
+      const float cmax = fmaxf(fmaxf(bar.red[st][0][lane], bar.red[st][1][lane]),
+                               fmaxf(bar.red[st][2][lane], bar.red[st][3][lane]));
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (m_col == -INFINITY || cmax > m_col + kRescaleThreshold) {
+        const float m_new = fmaxf(m_col, cmax);
+        if (m_new != -INFINITY) {
+          rescale = m_col != -INFINITY;
+          alpha = rescale ? ex2_approx(m_col - m_new) : 0.0f;
+          m_col = m_new;
         }
       }
+      const float mu = m_col == -INFINITY ? 0.0f : m_col;
+      const bool any_rescale = __any_sync(0xffffffffu, rescale);  // the same in all four warps
+      // P^T and O^T are touched only once PV_{j-1} has completed
+      if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
+#pragma unroll
+      for (int q = 0; q < kNQ; ++q) {
+        const float e = ex2_approx(s[q] - __shfl_sync(0xffffffffu, mu, q));
+        if (any_rescale) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e;
+        else l_part[q] += e;
+        if (!dead)  // P^T column for key k: p * v_scale, fp16
+          *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = __float2half_rn(e * vs);
+      }
       if (!dead) {
-        if (any_rescale) {  // identical in every thread: all hold the same running maxima
+        tc_fence_after();
+        if (any_rescale) {  // O^T lane k (head_dim index) times column q's factor
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kNQ; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * bar.alpha[q]);
+            for (int q = 0; q < kNQ; ++q)
+              v[q] = __float_as_uint(__uint_as_float(v[q]) * __shfl_sync(0xffffffffu, alpha, q));
             tmem_st_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
           }
           tmem_wait_st();
@@ -504,20 +529,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // epilogue: column sums, O^T / l, log-sum-exp
     bool fin = !dead && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
-    named_bar_sync(1, 128);  // every warp is past its last read of bar.red / bar.alpha
+    named_bar_sync(1, 128);  // every warp is past its last read of bar.red
     bar.red[0][quarter][lane] = warp_reduce_columns<false>(l_part, lane);
     named_bar_sync(1, 128);
     if (quarter == 0) {  // lane q: column q's sum, 1 / l and log-sum-exp
       const float l = bar.red[0][0][lane] + bar.red[0][1][lane] + bar.red[0][2][lane] + bar.red[0][3][lane];
-      bar.alpha[lane] = l > 0.0f ? 1.0f / l : 0.0f;
-      float mq = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < kNQ; ++q)
-        if (lane == q) mq = m_run[q];
+      bar.inv_l[lane] = l > 0.0f ? 1.0f / l : 0.0f;
       if (fin) {
         const int t = lane / p.group, hh = lane % p.group;
         const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
-        p.part_lse[(int64_t)split * p.rows + row] = l > 0.0f ? (mq + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.part_lse[(int64_t)split * p.rows + row] = l > 0.0f ? (m_col + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
     named_bar_sync(1, 128);
@@ -533,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         for (int q = 0; q < kNQ; ++q) {
           const int t = q / p.group, h2 = q % p.group;
           const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + h2;
-          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.alpha[q];
+          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.inv_l[q];
         }
       }
     }
