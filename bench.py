@@ -52,10 +52,10 @@ def prefill_pairs(seq_len, q_len):
     return q_len * s + q_len * (q_len + 1) // 2
 
 
-def verify_bytes(seq_lens, T=T_VERIFY):
+def verify_bytes(seq_lens, T=T_VERIFY, hq=HQ):
     """algorithmic HBM bytes of a verify batch: int8 K and V (2*Hkv*D per token), their fp32
     per-token-head scales (2*Hkv*4), q and out bf16 (T*Hq*D*2 each) per request."""
-    return sum(int(s) * (2 * HKV * D + 2 * HKV * 4) + 2 * T * HQ * D * 2 for s in seq_lens)
+    return sum(int(s) * (2 * HKV * D + 2 * HKV * 4) + 2 * T * hq * D * 2 for s in seq_lens)
 
 
 def load_peaks():
@@ -397,46 +397,54 @@ def run_e2e(torch, pkv, wl, args, dev):
 
 
 def run_verify_batch(torch, pkv, dev, flush, args):
-    """32-request verify batch (distinct blocks): HBM GB/s of partial + combine."""
-    from _devsetup import device_meta, device_pool, device_q, device_scale_pool
+    """32-request verify batch (distinct blocks): HBM GB/s of partial + combine. The same cache also
+    serves two other query geometries: a one-token decode step (T = 1, 16/4 heads) and the pages'
+    24/4 heads with T = 8 (48 query columns per KV head, two CTAs per key range)."""
+    from _devsetup import device_meta, device_pool, device_q, device_scale_pool, u16_to_bf16
     p = W.verify_batch()
     k, v = device_pool(p, "k"), device_pool(p, "v")
     ks, vs = device_scale_pool(p, "k"), device_scale_pool(p, "v")
-    bt, sl, _ = device_meta(p)
-    q = device_q(p)
-    S = pkv.splits_needed(int(p.seq_lens.max()), SPLIT)
-    po = torch.empty((S, q.shape[0], HQ, D), dtype=torch.float32, device=dev)
-    pl = torch.empty((S, q.shape[0], HQ), dtype=torch.float32, device=dev)
-    out = torch.empty_like(q)
-
-    def run():
-        pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sl, T_VERIFY, p.softmax_scale, SPLIT, po, pl)
-        pkv.spec_verify_combine(po, pl, sl, T_VERIFY, SPLIT, out)
-
-    for _ in range(max(3, args.warmup)):
-        run()
-    times, tp, tc = [], [], []
-    for _ in range(max(5, args.steps)):
-        flush.zero_()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record()
-        pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sl, T_VERIFY, p.softmax_scale, SPLIT, po, pl)
-        e[1].record()
-        pkv.spec_verify_combine(po, pl, sl, T_VERIFY, SPLIT, out)
-        e[2].record()
-        e[2].synchronize()
-        times.append(e[0].elapsed_time(e[2]))
-        tp.append(e[0].elapsed_time(e[1]))
-        tc.append(e[1].elapsed_time(e[2]))
+    bt, _, _ = device_meta(p)
     peaks = load_peaks()
-    nbytes = verify_bytes(p.seq_lens)
-    ms = statistics.mean(times)
-    g = nbytes / (ms * 1e-3) / 1e9
-    gp = nbytes / (statistics.mean(tp) * 1e-3) / 1e9
-    return {"requests": p.num_reqs, "sum_seq_len": int(p.seq_lens.sum()), "algorithmic_bytes": int(nbytes),
-            "ms": round(ms, 4), "gbs": round(g, 1), "frac_hbm": round(g / peaks["hbm_gbs"], 4),
-            "partial_ms": round(statistics.mean(tp), 4), "partial_gbs": round(gp, 1),
-            "combine_ms": round(statistics.mean(tc), 4), "split_tokens": SPLIT}
+
+    def measure(q, seq_lens, T, hq):
+        sld = torch.from_numpy(np.asarray(seq_lens, dtype=np.int32)).to(dev)
+        S = pkv.splits_needed(int(max(seq_lens)), SPLIT)
+        po = torch.empty((S, q.shape[0], hq, D), dtype=torch.float32, device=dev)
+        pl = torch.empty((S, q.shape[0], hq), dtype=torch.float32, device=dev)
+        out = torch.empty_like(q)
+        for _ in range(max(3, args.warmup)):
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, SPLIT, po, pl)
+            pkv.spec_verify_combine(po, pl, sld, T, SPLIT, out)
+        times, tp, tc = [], [], []
+        for _ in range(max(5, args.steps)):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, SPLIT, po, pl)
+            e[1].record()
+            pkv.spec_verify_combine(po, pl, sld, T, SPLIT, out)
+            e[2].record()
+            e[2].synchronize()
+            times.append(e[0].elapsed_time(e[2]))
+            tp.append(e[0].elapsed_time(e[1]))
+            tc.append(e[1].elapsed_time(e[2]))
+        nbytes = verify_bytes(seq_lens, T, hq)
+        ms = statistics.mean(times)
+        g = nbytes / (ms * 1e-3) / 1e9
+        gp = nbytes / (statistics.mean(tp) * 1e-3) / 1e9
+        return {"requests": p.num_reqs, "T": T, "q_heads": hq, "sum_seq_len": int(np.sum(seq_lens)),
+                "algorithmic_bytes": int(nbytes), "ms": round(ms, 4), "gbs": round(g, 1),
+                "frac_hbm": round(g / peaks["hbm_gbs"], 4), "partial_ms": round(statistics.mean(tp), 4),
+                "partial_gbs": round(gp, 1), "combine_ms": round(statistics.mean(tc), 4), "split_tokens": SPLIT}
+
+    res = measure(device_q(p), p.seq_lens, T_VERIFY, HQ)
+    # decode: the first token of each request's verify window, alone
+    dec_lens = p.seq_lens - (T_VERIFY - 1)
+    res["decode_t1"] = measure(u16_to_bf16(W.bf16_normal(7, (p.num_reqs, HQ, D))).to(dev), dec_lens, 1, HQ)
+    q24 = u16_to_bf16(W.bf16_normal(8, (p.num_reqs * T_VERIFY, 24, D))).to(dev)
+    res["heads_24x4"] = measure(q24, p.seq_lens, T_VERIFY, 24)
+    return res
 
 
 # ----------------------------------------------------------------------------------------------

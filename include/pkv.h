@@ -183,8 +183,11 @@ PKV_API pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, co
  * [max_splits][num_reqs*T][num_q_heads]: caller-allocated, pkv_spec_verify_workspace_bytes()
  * bytes in total (part_o first, part_lse right after, each 256-byte aligned when carved from
  * one allocation). split_tokens must be a positive multiple of 128.
- * Requirements: head_dim == 256; T * (num_q_heads / num_kv_heads) == 32 (8 tokens x 4 query
- * heads per KV head, the pages' geometry); num_kv_heads a multiple of 4; block_size a multiple
+ * Requirements: head_dim == 256; group = num_q_heads / num_kv_heads <= 32. A CTA serves 32 query
+ * columns: floor(32 / group) tokens x group heads (the pages' 8 tokens x 4 heads fill it exactly; a
+ * one-token decode step runs with padding columns); when T * group > 32 (e.g. 24/4 heads with
+ * T = 8) the tokens are spread over adjacent CTAs that read the same keys. num_kv_heads a
+ * multiple of 4; block_size a multiple
  * of 8; scale strides multiples of 4 elements; q, caches and scales 16-byte aligned. Keys in a
  * block whose id is out of range read as zero (k = v = 0) and PKV_ERR_DEVICE_BOUNDS is recorded.
  */

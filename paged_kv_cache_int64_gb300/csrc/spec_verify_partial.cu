@@ -6,9 +6,11 @@
 // with the block id widened to int64, and the int8 per-token-head scales are addressed with the
 // same block id; the key range is cut into splits whose partials are merged by log-sum-exp.
 //
-// sm_103a design, one CTA = (split, KV head, request); the T tokens x g query heads that share the
-// KV head form N = 32 query columns, and the MMAs are "swapped" so the 128 keys of a tile are the
-// M dimension (the verify step is HBM-bound at ~63 flop per cache byte, beyond CUDA cores):
+// sm_103a design, one CTA = (split, KV head, request, token group); the tokens x g query heads that
+// share the KV head form N = 32 query columns (floor(32 / g) tokens per CTA: with T * g > 32 the
+// tokens are spread over adjacent CTAs that read the same keys; columns past the CTA's tokens are
+// zero padding, so a T = 1 decode step runs on the same kernel), and the MMAs are "swapped" so the
+// 128 keys of a tile are the M dimension (the verify step is HBM-bound at ~63 flop per cache byte):
 //   warps 0, 3 TMA producers (K and V): Q once; per 128-key tile, the int8 codes (4-D maps over the
 //              paged pool, block id as a coordinate) and fp32 scales (3-D maps, same block id) of K
 //              (warp 0) and of V (warp 3), each into its own two-stage ring: 3 copies for a tile
@@ -18,19 +20,22 @@
 //              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
 //              and P^T fp16 in shared memory).
 //   warps 8-11 K converter: thread k owns key row k and widens it into the tile's tensor-memory K
-//              buffer (two buffers, so tile j+1 is widened while tile j is scored).
-//   warps 12-15 V converter: once the previous PV has read the V tile, thread k widens V row k into
-//              it (shared memory, MN-major). Splitting the widening keeps the K side running while
-//              the V side waits for PV. int8 -> fp16 by byte permute (fp16 bits 0x6400|(b^0x80)
-//              equal 1024 + b + 128, so one subtraction of 1152 gives b exactly - the int8->fp16
-//              method of Kim et al. 2022, "Who Says Elephants Can't Run"); e4m3 -> fp16 by the
-//              hardware conversion (exact).
-//   warps 4-7  softmax: thread k owns key k's 32 scores (TMEM lane k of S^T); the K scale folds
-//              into its scores and the V scale into its P^T entry; column maxima by a shuffle
-//              reduce-scatter per warp and shared memory across the four warps, after which lane l
-//              keeps column l's running max (moved only when it grows by more than 2^8) and
-//              broadcasts it by shuffles; at the end, column sums, normalised partial O and its
-//              log-sum-exp.
+//              buffer (two buffers, so tile j+1 is widened while tile j is scored); the key's K
+//              scale goes to a 4-deep ring of TMEM columns read by the softmax, and the K stage is
+//              released at once.
+//   warps 12-15 V converter: once the previous PV has read the V tile, thread k hands its key's V
+//              scale to the softmax (a 2-deep ring of TMEM columns), widens V row k into the tile
+//              (shared memory, MN-major) and releases the V stage. The stages thus never wait for
+//              the softmax, and the K side keeps running while the V side waits for PV. int8 ->
+//              fp16 by byte permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one
+//              subtraction of 1152 gives b exactly - the int8->fp16 method of Kim et al. 2022,
+//              "Who Says Elephants Can't Run"); e4m3 -> fp16 by the hardware conversion (exact;
+//              the per-tensor scales multiply the scores and the output).
+//   warps 4-7  softmax: thread k owns key k's 32 scores (TMEM lane k of S^T), scaled by the key's
+//              K scale; column maxima by a shuffle reduce-scatter per warp and shared memory
+//              across the four warps, after which lane l keeps column l's running max (moved only
+//              when it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale
+//              in fp16; at the end, column sums, normalised partial O and its log-sum-exp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,6 +58,8 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; }    // 2 x 128: fp16 K rows
 __host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
 constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
+constexpr uint32_t kColKs = 384;          // 4 x 1 column: the K scale of each key, tile j in column j % 4
+constexpr uint32_t kColVs = 388;          // 2 x 1 column: the V scale of each key, tile j in column j % 2
 constexpr float kRescaleThreshold = 8.0f;
 
 // shared memory layout (1024-aligned). K and V stages are separate rings, so the K codes of tile
@@ -69,10 +76,11 @@ constexpr int kTiles = kOffP + 2 * kPChunk;
 
 struct alignas(16) Barriers {
   uint64_t q_full, q_ready;
-  uint64_t kst_full[2], kst_free[2];  // K stage ring (freed by the converter and the softmax warps)
-  uint64_t vst_full[2], vst_free[2];  // V stage ring (same)
+  uint64_t kst_full[2], kst_free[2];  // K stage ring (freed by the K converter)
+  uint64_t vst_full[2], vst_free[2];  // V stage ring (freed by the V converter)
   uint64_t k_ready[2], k_free[2];     // K_j in TMEM buffer j%2; QK_j done with it
   uint64_t v_ready;                   // V_j widened into shared memory
+  uint64_t vs_ready;                  // the V scales of tile j in TMEM (int8 cache)
   uint64_t s_full[2];                 // S^T_j in TMEM buffer j%2
   uint64_t p_full;                    // P^T_j written, O^T rescaled
   uint64_t pv_done;                   // PV_j complete (V and P^T buffers free, O^T current)
@@ -99,6 +107,7 @@ struct Params {
   int32_t max_blocks;
   const int32_t* seq_lens;
   int32_t T, group, num_q_heads, block_size, seg, split_tokens, max_splits;
+  int32_t tpc, n_tg;  // tokens per CTA (tpc * group <= 32 query columns) and CTAs per (split, head)
   float scale_log2;
   float* part_o;
   float* part_lse;
@@ -188,7 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
+  // blockIdx.x = split * n_tg + token group: the CTAs that share a key range are adjacent, so they
+  // run together and the later reads of the same K/V tiles hit L2
+  const int split = blockIdx.x / p.n_tg;
+  const int t_base = (blockIdx.x - split * p.n_tg) * p.tpc;  // first query token of this CTA
+  const int nq = min(p.tpc, p.T - t_base) * p.group;         // live query columns; the rest pad
   const int kvh = blockIdx.y;
   const int r = blockIdx.z;
   const int seq_len = __ldg(p.seq_lens + r);
@@ -207,14 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     mbar_init(&bar.q_ready, 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.kst_full[s], 1);
-      mbar_init(&bar.kst_free[s], 256);
+      mbar_init(&bar.kst_free[s], 128);
       mbar_init(&bar.vst_full[s], 1);
-      mbar_init(&bar.vst_free[s], 256);
+      mbar_init(&bar.vst_free[s], 128);
       mbar_init(&bar.k_ready[s], 128);
       mbar_init(&bar.k_free[s], 1);
       mbar_init(&bar.s_full[s], 1);
     }
     mbar_init(&bar.v_ready, 128);
+    mbar_init(&bar.vs_ready, 128);
     mbar_init(&bar.p_full, 128);
     mbar_init(&bar.pv_done, 1);
     bar.abort = 0;
@@ -239,9 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const bool is_k = warp == 0;
     const int nseg = kBN / G;
     if (is_k && lane == 0) {
-      mbar_arrive_expect_tx(&bar.q_full, 4 * kQChunk);
+      mbar_arrive_expect_tx(&bar.q_full, 4u * 128u * (uint32_t)(p.tpc * p.group));  // the whole box
       for (int c = 0; c < 4; ++c)
-        tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T);
+        tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T + t_base);
     }
     uint64_t* full = is_k ? bar.kst_full : bar.vst_full;
     uint64_t* freeb = is_k ? bar.kst_free : bar.vst_free;
@@ -331,12 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
-    if (!dead) {  // row k & 31, chunk k >> 5
+    if (!dead) {  // row k & 31, chunk k >> 5; padding rows (past the CTA's columns) become zeros
       const int row = k & 31, c = k >> 5;
+      const bool live_row = row < nq;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         uint4* ptr = reinterpret_cast<uint4*>(sQ + c * kQChunk + row * 128 + q * 16);
-        uint4 v = *ptr;
+        uint4 v = live_row ? *ptr : make_uint4(0, 0, 0, 0);
         uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -356,6 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
+      if (!kFp8) {  // the key's scale goes to the softmax through TMEM (0 for a dead key), so the
+                    // stage is released here and never waits for the softmax
+        const float ks = live ? reinterpret_cast<const float*>(kstage + kStageScales)[k * 4 + (kvh & 3)] : 0.0f;
+        tmem_st_32x32b_x1(tmem + lane_off + kColKs + (j & 3), __float_as_uint(ks));
+      }
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t kv[32];
@@ -381,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // thread k owns key row k: once PV_{j-1} has read the V tile, its V row -> fp16 into the
     // MN-major V tile (zeros outside the split or in a bad block)
     const int k = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
@@ -388,6 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
+      if (!kFp8) {  // the key's V scale goes to the softmax first (it scales P^T), then the codes
+        const float vs = live ? reinterpret_cast<const float*>(vstage + kStageScales)[k * 4 + (kvh & 3)] : 0.0f;
+        tmem_st_32x32b_x1(tmem + lane_off + kColVs + (j & 1), __float_as_uint(vs));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar.vs_ready);
+      }
 #pragma unroll 1
       for (int c8 = 0; c8 < 2; ++c8) {
 #pragma unroll
@@ -418,7 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
-    const float v_descale = kFp8 ? __ldg(p.v_descale) : 0.0f;
     float l_part[kNQ];
 #pragma unroll
     for (int q = 0; q < kNQ; ++q) l_part[q] = 0.0f;
@@ -426,35 +453,28 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
-      const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
-      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
       const int key0 = k_begin + j * kBN;
       const int key = key0 + k;
       const bool in_range = key < k_end;
-      float ks = 0.0f;
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort));
-      if (!dead) {  // the K scale, then release this tile's K stage
-        if (in_range && !((bar.kbad[st] >> (k / G)) & 1u))
-          ks = kFp8 ? k_descale : reinterpret_cast<const float*>(kstage + kStageScales)[k * 4 + (kvh & 3)];
-        mbar_arrive(&bar.kst_free[st]);
-      }
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
       float s[kNQ];
       {
         uint32_t v[32];
+        float ks = kFp8 ? k_descale : 0.0f;  // a dead key's K row is zero: its score is 0 either way
         if (!dead) {
           tc_fence_after();
           tmem_ld_32x32b_x32(tmem + lane_off + col_s(st), v);
+          if (!kFp8) ks = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + kColKs + (j & 3)));
           tmem_wait_ld();
         }
         const float f = p.scale_log2 * ks;
         if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
 #pragma unroll
-          for (int q = 0; q < kNQ; ++q) s[q] = (!dead && in_range) ? __uint_as_float(v[q]) * f : -INFINITY;
-        } else {  // causal limit of column q (token q / group): key <= prefix + q / group
+          for (int q = 0; q < kNQ; ++q) s[q] = (!dead && in_range && q < nq) ? __uint_as_float(v[q]) * f : -INFINITY;
+        } else {  // causal limit of column q (token t_base + q / group): key <= prefix + that token
 #pragma unroll
           for (int q = 0; q < kNQ; ++q) {
-            const bool vis = !dead && in_range && key <= prefix + q / p.group;
+            const bool vis = !dead && in_range && q < nq && key <= prefix + t_base + q / p.group;
             s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
           }
         }
@@ -473,14 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       bar.red[st][quarter][lane] = mine;
       named_bar_sync(1, 128);
-      // the V scale, then release this tile's V stage
-      float vs = 0.0f;
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort));
-      if (!dead) {
-        if (in_range && !((bar.vbad[st] >> (k / G)) & 1u))
-          vs = kFp8 ? v_descale : reinterpret_cast<const float*>(vstage + kStageScales)[k * 4 + (kvh & 3)];
-        mbar_arrive(&bar.vst_free[st]);
-      }
       // lane l: column l's tile maximum, running maximum and rescale factor
       const float cmax = fmaxf(fmaxf(bar.red[st][0][lane], bar.red[st][1][lane]),
                                fmaxf(bar.red[st][2][lane], bar.red[st][3][lane]));
@@ -498,6 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const bool any_rescale = __any_sync(0xffffffffu, rescale);  // the same in all four warps
       // P^T and O^T are touched only once PV_{j-1} has completed
       if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
+      float vs = 1.0f;  // e4m3: the per-tensor V scale multiplies the output instead
+      if (!kFp8) {
+        if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.vs_ready, j & 1, abort));
+        if (!dead) {
+          tc_fence_after();
+          vs = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + kColVs + (j & 1)));
+          tmem_wait_ld();
+        }
+      }
 #pragma unroll
       for (int q = 0; q < kNQ; ++q) {
         const float e = ex2_approx(s[q] - __shfl_sync(0xffffffffu, mu, q));
@@ -534,9 +555,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     named_bar_sync(1, 128);
     if (quarter == 0) {  // lane q: column q's sum, 1 / l and log-sum-exp
       const float l = bar.red[0][0][lane] + bar.red[0][1][lane] + bar.red[0][2][lane] + bar.red[0][3][lane];
-      bar.inv_l[lane] = l > 0.0f ? 1.0f / l : 0.0f;
-      if (fin) {
-        const int t = lane / p.group, hh = lane % p.group;
+      // e4m3: the per-tensor V scale multiplies the output once
+      bar.inv_l[lane] = l > 0.0f ? (kFp8 ? __ldg(p.v_descale) / l : 1.0f / l) : 0.0f;
+      if (fin && lane < nq) {
+        const int t = t_base + lane / p.group, hh = lane % p.group;
         const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
         p.part_lse[(int64_t)split * p.rows + row] = l > 0.0f ? (m_col + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
@@ -552,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         const int d = hh * 128 + k;
 #pragma unroll
         for (int q = 0; q < kNQ; ++q) {
-          const int t = q / p.group, h2 = q % p.group;
+          if (q >= nq) break;
+          const int t = t_base + q / p.group, h2 = q % p.group;
           const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + h2;
           p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.inv_l[q];
         }
@@ -614,7 +637,10 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
           "%s: bad size argument", name);
   PKV_UNSUP(num_q_heads % num_kv_heads == 0, "%s: num_q_heads %% num_kv_heads != 0", name);
   const int group = num_q_heads / num_kv_heads;
-  PKV_UNSUP(group * T == kNQ, "%s: T * (num_q_heads / num_kv_heads) must be 32 (got %d)", name, group * T);
+  PKV_UNSUP(group <= kNQ, "%s: num_q_heads / num_kv_heads must be at most 32 (got %d)", name, group);
+  const int tpc = T < kNQ / group ? T : kNQ / group;  // tokens per CTA
+  const int n_tg = (T + tpc - 1) / tpc;                // CTAs per (split, KV head, request)
+  PKV_ARG((int64_t)max_splits * n_tg < (1ll << 31), "%s: grid too large", name);
   PKV_UNSUP(kFp8 || num_kv_heads % 4 == 0, "%s: num_kv_heads must be a multiple of 4", name);
   PKV_UNSUP(block_size % 8 == 0, "%s: block_size must be a multiple of 8", name);
   PKV_UNSUP(split_tokens % kBN == 0, "%s: split_tokens must be a multiple of 128", name);
@@ -630,7 +656,7 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_q_heads, (uint64_t)num_reqs * (uint64_t)T};
     const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)num_q_heads * kD * 2};
-    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)T};
+    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)tpc};
     pkv_status s = encode_tiled(&p.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, "q");
     if (s != PKV_OK) return s;
   }
@@ -678,6 +704,8 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   p.seq_lens = seq_lens;
   p.T = T;
   p.group = group;
+  p.tpc = tpc;
+  p.n_tg = n_tg;
   p.num_q_heads = num_q_heads;
   p.block_size = block_size;
   p.seg = G;
@@ -694,7 +722,7 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
     cudaFuncSetAttribute(spec_verify_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     attr = true;
   }
-  dim3 grid((unsigned)max_splits, (unsigned)num_kv_heads, (unsigned)num_reqs);
+  dim3 grid((unsigned)(max_splits * n_tg), (unsigned)num_kv_heads, (unsigned)num_reqs);
   spec_verify_partial_kernel<kFp8><<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
   return check_launch(name);
 }

@@ -95,8 +95,8 @@ def test_prefill_rejects_bad_arguments(pkv, kw, status):
 
 def test_verify_rejects_unsupported_geometry(pkv):
     f = pkv.lib.pkv_spec_verify_attn_partial
-    # T * group = 6 * 4 = 24 != 32
-    rc = f(16, 16, 16, 16, 16, 4, 16384, 1024, 256, 64, 4, 16, 1, 1, 16, 1, 6, 16, 4, 256, 16, 0.1, 128, 2, 16, 16,
+    # a group of 33 query heads per KV head exceeds the 32 query columns of a CTA
+    rc = f(16, 16, 16, 16, 16, 4, 16384, 1024, 256, 64, 4, 16, 1, 1, 16, 1, 8, 132, 4, 256, 16, 0.1, 128, 2, 16, 16,
            None, None)
     assert rc == 2 and "32" in pkv.lib.pkv_last_error().decode()
     # split_tokens not a multiple of 128

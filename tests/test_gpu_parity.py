@@ -357,6 +357,28 @@ def test_verify_partials_and_combine(pkv, split):
         assert max_abs(a[fin], b[fin]) <= 1e-3
 
 
+@pytest.mark.parametrize("T,hq,hkv", [(1, 16, 4), (4, 24, 4), (5, 16, 4), (2, 32, 4), (8, 24, 4), (11, 16, 4)])
+def test_verify_other_query_geometries(pkv, T, hq, hkv):
+    """T * group other than 32 query columns: a T = 1 decode step; the pages' 24/4 heads with T = 4
+    (24 columns, padded) and T = 8 (48 columns: two CTAs per key range); odd T; T = 11 with 4 heads
+    (44 columns). Padding columns must not leak into live ones, and only live rows are written."""
+    p = W.make_problem("vq", seed=53 + T, seq_lens=[L + T for L in (700, 64, 2100)], q_lens=[T] * 3,
+                       num_blocks=60, block_size=64, num_q_heads=hq, num_kv_heads=hkv, kv_dtype="int8",
+                       softmax_scale=1.0 / 16.0)
+    split = 256
+    got, po, pl = _run_verify(pkv, p, split, T)
+    args = _verify_oracle_args(p)
+    ref = oracle.spec_verify_attn(*args, T, p.num_q_heads, p.softmax_scale)
+    _close(got, ref, TOL_BF16)
+    rpo, rpl = oracle.spec_verify_partial(*args, T, p.num_q_heads, p.softmax_scale, split, po.shape[0])
+    for r, L in enumerate(p.seq_lens):
+        ns = math.ceil(L / split)
+        rows = slice(r * T, (r + 1) * T)
+        assert _partial_err(po[:ns, rows], rpo[:ns, rows]) <= 1e-3
+        fin = np.isfinite(rpl[:ns, rows])
+        assert max_abs(pl[:ns, rows][fin], rpl[:ns, rows][fin]) <= 1e-3
+
+
 def test_verify_bigpool_top_equals_bottom(pkv):
     """int8 per-token-head cache, 2,600-block pool (bs 880), request of L = 20,000 + 8 tokens on the top
     blocks and on the bottom blocks with identical bytes: bit-identical outputs, and the oracle."""
