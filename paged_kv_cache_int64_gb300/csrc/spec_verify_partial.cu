@@ -31,11 +31,12 @@
 //              subtraction of 1152 gives b exactly - the int8->fp16 method of Kim et al. 2022,
 //              "Who Says Elephants Can't Run"); e4m3 -> fp16 by the hardware conversion (exact;
 //              the per-tensor scales multiply the scores and the output).
-//   warps 4-7  softmax: thread k owns key k's 32 scores (TMEM lane k of S^T), scaled by the key's
-//              K scale; column maxima by a shuffle reduce-scatter per warp and shared memory
-//              across the four warps, after which lane l keeps column l's running max (moved only
-//              when it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale
-//              in fp16; at the end, column sums, normalised partial O and its log-sum-exp.
+//   warps 4-7, 16-19 softmax, two warpgroups of 16 query columns each: thread k owns key k's 16
+//              scores of its group (TMEM lane k of S^T), scaled by the key's K scale; column
+//              maxima by a shuffle reduce-scatter per warp and shared memory across the group's
+//              four warps, after which lane l keeps column (l & 15)'s running max (moved only when
+//              it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale in fp16;
+//              at the end, column sums, normalised partial O and its log-sum-exp.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -49,7 +50,7 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
@@ -87,7 +88,7 @@ struct alignas(16) Barriers {
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
-  float red[2][4][kNQ];  // per-warp column maxima (and the final column sums)
+  float red[2][2][4][16];  // [tile parity][softmax group][warp][column]: maxima, then the final sums
   float inv_l[kNQ];      // epilogue: 1 / column sum
 };
 
@@ -152,12 +153,12 @@ __device__ __forceinline__ void widen16(uint4 in, uint32_t (&o)[8]) {
   if (kFp8) widen16_e4m3(in, o); else widen16_f16(in, o);
 }
 
-// Butterfly reduce-scatter: on entry every lane holds 32 column values; on exit lane l holds the
-// reduction over the warp of column l. 31 shuffles.
+// Reduce-scatter of 16 columns: on entry every lane holds 16 column values; on exit every lane holds
+// the warp maximum (kMax) or sum of column (lane & 15). 16 shuffles.
 template <bool kMax>
-__device__ __forceinline__ float warp_reduce_columns(float (&v)[kNQ], int lane) {
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = 8; o >= 1; o >>= 1) {
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int q = 0; q < o; ++q) {
@@ -167,23 +168,8 @@ __device__ __forceinline__ float warp_reduce_columns(float (&v)[kNQ], int lane) 
       v[q] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-  return v[0];
-}
-
-// Reduce-scatter of 16 columns: on entry every lane holds 16 column values; on exit every lane holds
-// the warp maximum of column (lane & 15). 16 shuffles.
-__device__ __forceinline__ float reduce_scatter16_max(float (&v)[16], int lane) {
-#pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int q = 0; q < o; ++q) {
-      const float keep = upper ? v[q + o] : v[q];
-      const float send = upper ? v[q] : v[q + o];
-      v[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-    }
-  }
-  return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
 template <bool kFp8>
@@ -229,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
     mbar_init(&bar.v_ready, 128);
     mbar_init(&bar.vs_ready, 128);
-    mbar_init(&bar.p_full, 128);
+    mbar_init(&bar.p_full, 256);
     mbar_init(&bar.pv_done, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -396,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_arrive(&bar.k_ready[st]);
       mbar_arrive(&bar.kst_free[st]);
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 12 && warp < 16) {
     // ---------------------------------------------------------------------------- V converter
     // thread k owns key row k: once PV_{j-1} has read the V tile, its V row -> fp16 into the
     // MN-major V tile (zeros outside the split or in a bad block)
@@ -438,18 +424,22 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------------------- softmax
-    // thread k holds key k's 32 scores (TMEM lane k of S^T). Column maxima: a shuffle
-    // reduce-scatter leaves column l's warp maximum in lane l, shared memory combines the four
-    // warps; lane l then keeps column l's running max (the same in all four warps) and hands it
-    // to the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T.
+    // two warpgroups (warps 4-7: query columns 0-15, warps 16-19: columns 16-31); thread k holds
+    // key k's 16 scores of its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter
+    // leaves column (lane & 15)'s warp maximum in the lane, shared memory combines the four warps;
+    // lane l then keeps column (l & 15)'s running max (the same in all four warps) and hands it to
+    // the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T.
+    const int grp = warp >= 16 ? 1 : 0;
+    const int c0 = 16 * grp;       // the group's first query column
+    const int cl = lane & 15;      // this lane keeps the running max of column c0 + cl
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
-    float l_part[kNQ];
+    float l_part[16];
 #pragma unroll
-    for (int q = 0; q < kNQ; ++q) l_part[q] = 0.0f;
-    float m_col = -INFINITY;  // lane l: running maximum of column l
+    for (int q = 0; q < 16; ++q) l_part[q] = 0.0f;
+    float m_col = -INFINITY;
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
@@ -457,45 +447,41 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const int key = key0 + k;
       const bool in_range = key < k_end;
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
-      float s[kNQ];
+      float s[16];
       {
-        uint32_t v[32];
+        uint32_t v[16];
         float ks = kFp8 ? k_descale : 0.0f;  // a dead key's K row is zero: its score is 0 either way
         if (!dead) {
           tc_fence_after();
-          tmem_ld_32x32b_x32(tmem + lane_off + col_s(st), v);
+          tmem_ld_32x32b_x16(tmem + lane_off + col_s(st) + c0, v);
           if (!kFp8) ks = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + kColKs + (j & 3)));
           tmem_wait_ld();
         }
         const float f = p.scale_log2 * ks;
         if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
 #pragma unroll
-          for (int q = 0; q < kNQ; ++q) s[q] = (!dead && in_range && q < nq) ? __uint_as_float(v[q]) * f : -INFINITY;
-        } else {  // causal limit of column q (token t_base + q / group): key <= prefix + that token
+          for (int q = 0; q < 16; ++q)
+            s[q] = (!dead && in_range && c0 + q < nq) ? __uint_as_float(v[q]) * f : -INFINITY;
+        } else {  // causal limit of column c (token t_base + c / group): key <= prefix + that token
 #pragma unroll
-          for (int q = 0; q < kNQ; ++q) {
-            const bool vis = !dead && in_range && q < nq && key <= prefix + t_base + q / p.group;
+          for (int q = 0; q < 16; ++q) {
+            const int c = c0 + q;
+            const bool vis = !dead && in_range && c < nq && key <= prefix + t_base + c / p.group;
             s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
           }
         }
       }
-      // column maxima over the warp: two 16-column reduce-scatters, lane l ends with column l's
-      float mine;
       {
         float t[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) t[q] = s[q];
-        const float lo = reduce_scatter16_max(t, lane);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) t[q] = s[16 + q];
-        const float hi = reduce_scatter16_max(t, lane);
-        mine = lane < 16 ? lo : hi;
+        const float mine = reduce_scatter16<true>(t, lane);
+        if (lane < 16) bar.red[st][grp][quarter][lane] = mine;
       }
-      bar.red[st][quarter][lane] = mine;
-      named_bar_sync(1, 128);
-      // lane l: column l's tile maximum, running maximum and rescale factor
-      const float cmax = fmaxf(fmaxf(bar.red[st][0][lane], bar.red[st][1][lane]),
-                               fmaxf(bar.red[st][2][lane], bar.red[st][3][lane]));
+      named_bar_sync(1 + grp, 128);
+      // column c0 + cl: tile maximum, running maximum and rescale factor
+      const float cmax = fmaxf(fmaxf(bar.red[st][grp][0][cl], bar.red[st][grp][1][cl]),
+                               fmaxf(bar.red[st][grp][2][cl], bar.red[st][grp][3][cl]));
       float alpha = 1.0f;
       bool rescale = false;
       if (m_col == -INFINITY || cmax > m_col + kRescaleThreshold) {
@@ -520,25 +506,25 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         }
       }
 #pragma unroll
-      for (int q = 0; q < kNQ; ++q) {
+      for (int q = 0; q < 16; ++q) {
         const float e = ex2_approx(s[q] - __shfl_sync(0xffffffffu, mu, q));
         if (any_rescale) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e;
         else l_part[q] += e;
         if (!dead)  // P^T column for key k: p * v_scale, fp16
-          *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(q, k & 63)) = __float2half_rn(e * vs);
+          *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(c0 + q, k & 63)) = __float2half_rn(e * vs);
       }
       if (!dead) {
         tc_fence_after();
-        if (any_rescale) {  // O^T lane k (head_dim index) times column q's factor
+        if (any_rescale) {  // O^T lane k (head_dim index) times column c0 + q's factor
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kNQ; ++q)
+            for (int q = 0; q < 16; ++q)
               v[q] = __float_as_uint(__uint_as_float(v[q]) * __shfl_sync(0xffffffffu, alpha, q));
-            tmem_st_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+            tmem_st_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
           }
           tmem_wait_st();
         }
@@ -547,37 +533,43 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         mbar_arrive(&bar.p_full);
       }
     }
-    // epilogue: column sums, O^T / l, log-sum-exp
+    // epilogue: column sums, O^T / l, log-sum-exp (each group for its 16 columns)
     bool fin = !dead && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
-    named_bar_sync(1, 128);  // every warp is past its last read of bar.red
-    bar.red[0][quarter][lane] = warp_reduce_columns<false>(l_part, lane);
-    named_bar_sync(1, 128);
-    if (quarter == 0) {  // lane q: column q's sum, 1 / l and log-sum-exp
-      const float l = bar.red[0][0][lane] + bar.red[0][1][lane] + bar.red[0][2][lane] + bar.red[0][3][lane];
+    named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
+    {
+      const float sum = reduce_scatter16<false>(l_part, lane);
+      if (lane < 16) bar.red[0][grp][quarter][lane] = sum;
+    }
+    named_bar_sync(1 + grp, 128);
+    if (quarter == 0 && lane < 16) {  // lane q: column c0 + q's sum, 1 / l and log-sum-exp
+      const int c = c0 + lane;
+      const float l = bar.red[0][grp][0][lane] + bar.red[0][grp][1][lane] + bar.red[0][grp][2][lane] +
+                      bar.red[0][grp][3][lane];
       // e4m3: the per-tensor V scale multiplies the output once
-      bar.inv_l[lane] = l > 0.0f ? (kFp8 ? __ldg(p.v_descale) / l : 1.0f / l) : 0.0f;
-      if (fin && lane < nq) {
-        const int t = t_base + lane / p.group, hh = lane % p.group;
+      bar.inv_l[c] = l > 0.0f ? (kFp8 ? __ldg(p.v_descale) / l : 1.0f / l) : 0.0f;
+      if (fin && c < nq) {
+        const int t = t_base + c / p.group, hh = c % p.group;
         const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + hh;
         p.part_lse[(int64_t)split * p.rows + row] = l > 0.0f ? (m_col + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1 + grp, 128);
     if (fin) {
       tc_fence_after();
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + kColO + hh * 32, v);
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
         tmem_wait_ld();
         const int d = hh * 128 + k;
 #pragma unroll
-        for (int q = 0; q < kNQ; ++q) {
-          if (q >= nq) break;
-          const int t = t_base + q / p.group, h2 = q % p.group;
+        for (int q = 0; q < 16; ++q) {
+          const int c = c0 + q;
+          if (c >= nq) break;
+          const int t = t_base + c / p.group, h2 = c % p.group;
           const int64_t row = ((int64_t)r * p.T + t) * p.num_q_heads + (int64_t)kvh * p.group + h2;
-          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.inv_l[q];
+          p.part_o[((int64_t)split * p.rows + row) * kD + d] = __uint_as_float(v[q]) * bar.inv_l[c];
         }
       }
     }
