@@ -273,6 +273,9 @@ def run_gpu(args):
 
     # verify batch (32 requests), measured in the same run, outside the step
     vb = run_verify_batch(torch, pkv, dev, flush, args) if not args.skip_batch else None
+    # the two fp8 prefill paths on the step's fp8 chunk: dequantize once into the dense scratch, or
+    # dequantize every tile inside the prefill
+    fp8_paths = run_fp8_paths(torch, pkv, wl, flush, args)
 
     if rank != 0:
         if world > 1:
@@ -316,6 +319,7 @@ def run_gpu(args):
                                           mean.get("verify_combine", 0), peaks),
         },
         "verify_batch": vb,
+        "fp8_prefill_paths": fp8_paths,
         "e2e": e2e,
         "gpu_launches": wl.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
@@ -394,6 +398,44 @@ def run_e2e(torch, pkv, wl, args, dev):
     ms = a.elapsed_time(b)
     return {"value": round(wl.TOKENS_PER_STEP * steps / (ms * 1e-3), 1), "unit": "tok/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def run_fp8_paths(torch, pkv, wl, flush, args):
+    """Chunk of 2,048 queries at the end of the 20,000-token e4m3 context, both fp8 prefill paths:
+    kv_fp8_dequant_dense + bf16 prefill on the scratch, against paged_prefill_attn_fp8 (per-tile
+    dequantization). CUDA events, L2 flushed before every repetition."""
+    s = wl.p.softmax_scale
+    out = torch.empty_like(wl.q)
+
+    def dense():
+        pkv.kv_fp8_dequant_dense(wl.kf, wl.vf, wl.bt, wl.sl, wl.fscale, wl.fscale, wl.kd, wl.vd)
+
+    def dense_attn():
+        pkv.paged_prefill_attn(wl.q, wl.kd, wl.vd, wl.ident, wl.sl, wl.qsl, CHUNK, s, out)
+
+    def fused():
+        pkv.paged_prefill_attn_fp8(wl.q, wl.kf, wl.vf, wl.fscale, wl.fscale, wl.bt, wl.sl, wl.qsl, CHUNK, s, out)
+
+    for _ in range(max(3, args.warmup)):
+        dense(); dense_attn(); fused()
+    t = {"dequant": [], "attn": [], "fused": []}
+    for _ in range(max(5, min(args.steps, 50))):
+        for name, fn in (("dequant", dense), ("attn", dense_attn), ("fused", fused)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            t[name].append(a.elapsed_time(b))
+    m = {k: statistics.mean(v) for k, v in t.items()}
+    flops = algorithmic()["prefill_flops"]
+    tf = lambda ms: round(flops / (ms * 1e-3) / 1e12, 2)
+    return {"dense": {"dequant_ms": round(m["dequant"], 4), "attn_ms": round(m["attn"], 4),
+                      "total_ms": round(m["dequant"] + m["attn"], 4), "attn_tflops": tf(m["attn"]),
+                      "tflops_incl_dequant": tf(m["dequant"] + m["attn"])},
+            "fused": {"ms": round(m["fused"], 4), "tflops": tf(m["fused"])},
+            "note": "each dense-path step dequantizes the request's whole context [0, seq_len) once"}
 
 
 def run_verify_batch(torch, pkv, dev, flush, args):

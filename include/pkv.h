@@ -81,7 +81,7 @@ typedef enum pkv_kv_dtype {
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version of this header (incremented on any signature change). */
-#define PKV_ABI_VERSION 3
+#define PKV_ABI_VERSION 4
 PKV_API int32_t pkv_abi_version(void);
 
 /*
@@ -186,9 +186,9 @@ PKV_API pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, co
  * Requirements: head_dim == 256; group = num_q_heads / num_kv_heads <= 32. A CTA serves 32 query
  * columns: floor(32 / group) tokens x group heads (the pages' 8 tokens x 4 heads fill it exactly; a
  * one-token decode step runs with padding columns); when T * group > 32 (e.g. 24/4 heads with
- * T = 8) the tokens are spread over adjacent CTAs that read the same keys. num_kv_heads a
- * multiple of 4; block_size a multiple
- * of 8; scale strides multiples of 4 elements; q, caches and scales 16-byte aligned. Keys in a
+ * T = 8) the tokens are spread over adjacent CTAs that read the same keys. block_size a multiple
+ * of 8; q, caches and cache strides 16-byte aligned; scale pools 4-byte aligned with
+ * scale_stride_tok >= num_kv_heads (head stride 1). Keys in a
  * block whose id is out of range read as zero (k = v = 0) and PKV_ERR_DEVICE_BOUNDS is recorded.
  */
 PKV_API size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t num_q_heads, int32_t head_dim,
@@ -271,6 +271,30 @@ PKV_API pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, int6
                                       int64_t scale_stride_tok, const float* k_scale, const float* v_scale,
                                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                                       int32_t* dev_err, void* stream);
+
+/*
+ * paged_prefill_attn_fp8 - chunked causal prefill attention read straight from a per-tensor fp8
+ * e4m3 paged cache, each K/V tile dequantized in shared memory [P3360 "What changed": the
+ * alternative it measured against - dequantizing per read instead of once per layer into a dense
+ * scratch; here both paths exist so that they can be measured against each other on GB300].
+ *   k = bf16_rn(fp32(e4m3(k_fp8[...])) * (*k_scale)), the same for v - bit for bit the values
+ *   pkv_kv_fp8_dequant_dense writes - then exactly the attention of pkv_paged_prefill_attn with
+ *   qk_mode PKV_QK_BF16 (same chunk convention, causal mask and GQA map), out bf16
+ *   [total_q][num_q_heads][head_dim].
+ * k_fp8 / v_fp8: uint8 e4m3 pools [num_blocks][block_size][num_kv_heads][head_dim] with element
+ * strides (16-byte aligned); k_scale / v_scale: device pointers to one fp32 each. Keys past
+ * seq_len or in a block whose id is out of range read as zero (PKV_ERR_DEVICE_BOUNDS for the
+ * latter). Requirements as pkv_paged_prefill_attn (head_dim == 256).
+ */
+PKV_API pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
+                                              const float* k_scale, const float* v_scale, int64_t num_blocks,
+                                              int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                              const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                              const int32_t* seq_lens, const int32_t* query_start_loc,
+                                              int32_t num_reqs, int32_t total_q, int32_t max_q_len,
+                                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t block_size, float softmax_scale, void* out,
+                                              int32_t* dev_err, void* stream);
 
 /*
  * spec_verify_attn_noalloc - pkv_spec_verify_attn_partial followed by pkv_spec_verify_combine, with

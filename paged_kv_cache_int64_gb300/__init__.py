@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA", "PKV_ERR_DEVICE_BOUNDS",
     "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PKV_KV_BF16", "PKV_KV_INT8", "PKV_KV_FP8", "PkvError", "lib",
-    "library_path", "kv_cache_write", "kv_int8_stats_quant", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
+    "library_path", "kv_cache_write", "kv_int8_stats_quant", "paged_prefill_attn_fp8", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
     "spec_verify_attn_partial", "spec_verify_attn_partial_fp8", "spec_verify_combine", "EXPORTED_SYMBOLS",
 ]
 
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "pkv_last_error", "pkv_abi_version", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense",
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
     "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
-    "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write",
+    "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write", "pkv_paged_prefill_attn_fp8",
 )
 
 library_path = _build.LIB
@@ -71,7 +71,9 @@ def _load():
     L.pkv_spec_verify_attn_noalloc.restype = i32
     L.pkv_kv_cache_write.argtypes = [vp, vp, i64, vp, i64, i32, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, i64,
                                      vp, vp, i64, i64, vp, vp, i32, i32, i32, vp, vp]
-    for name in ("pkv_kv_cache_write", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
+    L.pkv_paged_prefill_attn_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32,
+                                             i32, i32, i32, i32, i32, f32, vp, vp, vp]
+    for name in ("pkv_paged_prefill_attn_fp8", "pkv_kv_cache_write", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
                  "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8"):
         getattr(L, name).restype = i32
     return L
@@ -183,6 +185,23 @@ def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_l
                                       _ptr(_i32(query_start_loc)), R, q.shape[0], int(max_q_len), q.shape[1],
                                       hkv, d, bs, float(softmax_scale), int(qk_mode), _ptr(k8), _ptr(k8_scale),
                                       _ptr(k16), max_ctx, _ptr(out), _ptr(dev_err), _stream(stream)))
+
+
+def paged_prefill_attn_fp8(q, k_fp8, v_fp8, k_scale, v_scale, block_table, seq_lens, query_start_loc, max_q_len,
+                           softmax_scale, out, dev_err=None, stream=None):
+    """Chunked causal prefill attention read straight from per-tensor e4m3 paged K/V (uint8
+    [nb][bs][hkv][D]) with device scalar scales; each tile is dequantized in shared memory."""
+    nb, bs, hkv, d, sb, st, sh = _cache_strides(k_fp8)
+    assert v_fp8.stride() == k_fp8.stride() and v_fp8.shape == k_fp8.shape
+    assert k_fp8.dtype == torch.uint8 and v_fp8.dtype == torch.uint8
+    assert q.is_contiguous() and out.is_contiguous() and q.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
+    _i32(block_table)
+    R = block_table.shape[0]
+    _check(lib.pkv_paged_prefill_attn_fp8(_ptr(q), _ptr(k_fp8), _ptr(v_fp8), _ptr(k_scale), _ptr(v_scale), nb, sb, st,
+                                          sh, _ptr(block_table), block_table.stride(0), block_table.shape[1],
+                                          _ptr(_i32(seq_lens)), _ptr(_i32(query_start_loc)), R, q.shape[0],
+                                          int(max_q_len), q.shape[1], hkv, d, bs, float(softmax_scale), _ptr(out),
+                                          _ptr(dev_err), _stream(stream)))
 
 
 def spec_verify_workspace_bytes(num_tokens, num_q_heads, head_dim, max_splits) -> int:

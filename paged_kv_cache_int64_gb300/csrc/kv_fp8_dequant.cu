@@ -35,29 +35,6 @@ struct DequantArgs {
   int* dev_err;
 };
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
-  return r;
-}
-
-// 16 e4m3 codes -> 16 bf16 values (as 8 packed words) scaled by s.
-__device__ __forceinline__ uint4 dequant16(uint4 in, float s, uint4& hi_out) {
-  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(w[i] >> (16 * half)));
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      o[2 * i + half] = pack_bf16x2(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
-    }
-  }
-  hi_out = make_uint4(o[4], o[5], o[6], o[7]);
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 __global__ void __launch_bounds__(kThreads) kv_fp8_dequant_dense_kernel(const DequantArgs a) {
   const int r = blockIdx.y;
   const int64_t L = __ldg(a.seq_lens + r);
@@ -101,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) kv_fp8_dequant_dense_kernel(const De
       const int which = (int)(dsto[u] >> 62);
       const int64_t o = dsto[u] & ((1ll << 62) - 1);
       uint4 hi;
-      const uint4 lo = dequant16(raw[u], which ? sv : sk, hi);
+      const uint4 lo = dequant16_e4m3_bf16(raw[u], which ? sv : sk, hi);
       uint4* dst = reinterpret_cast<uint4*>(a.dst[which] + o);
       dst[0] = lo;
       dst[1] = hi;

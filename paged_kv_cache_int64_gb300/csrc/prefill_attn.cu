@@ -104,13 +104,21 @@ struct Params {
   int32_t n_mtiles;
   __nv_bfloat16* out;
   int* dev_err;
+  // fused fp8 (mode 3): the e4m3 pools, read row by row by the converter warps, and the
+  // per-tensor scales (device scalars)
+  const uint8_t* k_fp8;
+  const uint8_t* v_fp8;
+  int64_t stride_blk, stride_tok, stride_head;
+  const float* k_scale;
+  const float* v_scale;
 };
 
 // kMode 0: exact QK (bf16 K from the pool); 1: int8 QK with K widened from the int8 scratch by
-// converter warps; 2: int8 QK with K read by TMA from the fp16 copy of the codes.
+// converter warps; 2: int8 QK with K read by TMA from the fp16 copy of the codes; 3: exact QK on a
+// per-tensor e4m3 pool, K and V dequantized to bf16 tile by tile by converter warps.
 template <int kMode>
 struct Cfg {
-  static constexpr int kThreads = kMode == 1 ? 512 : 384;
+  static constexpr int kThreads = (kMode == 1 || kMode == 3) ? 512 : 384;
   static constexpr int kTiles = kTilesEnd;
   static constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
 };
@@ -204,8 +212,9 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
   Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kMode>::kTiles);
-  constexpr bool kInt8 = kMode != 0;   // int8 QK (quantized Q, per-key K scales, f16 MMA)
-  constexpr bool kConv = kMode == 1;   // K widened by the converter warps
+  constexpr bool kInt8 = kMode == 1 || kMode == 2;  // int8 QK (quantized Q, per-key K scales, f16 MMA)
+  constexpr bool kConv = kMode == 1;                 // K widened by the converter warps
+  constexpr bool kFused = kMode == 3;                // K and V dequantized by the converter warps
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,10 +236,10 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_ready, 128);
     for (int c = 0; c < 4; ++c) {
-      mbar_init(&bar.k_full[c], kConv ? 128 : 1);
+      mbar_init(&bar.k_full[c], (kConv || kFused) ? 128 : 1);
       mbar_init(&bar.k_empty[c], 1);
     }
-    mbar_init(&bar.v_full, 1);
+    mbar_init(&bar.v_full, kFused ? 128 : 1);
     mbar_init(&bar.fix, 1);
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.s_free, 256);
@@ -251,7 +260,14 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
 
-  if (warp == 0) {
+  if (warp == 0 && kFused) {
+    // ---------------------------------------------------------------------------- producer (Q)
+    if (lane == 0) {
+      prefetch_tensormap(&p.qmap);
+      mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
+      for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
+    }
+  } else if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
     const int G = p.seg;
     const int nseg = kBN / G;
@@ -604,6 +620,65 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
       }
     }
+  } else if (kFused && warp >= 12) {
+    // ---------------------------------------------------------------------------- fp8 dequant
+    // thread t owns key row t of each tile: its e4m3 K row (256 B) and V row are read straight from
+    // the paged pool through the block table (64-bit offsets), dequantized exactly as
+    // kv_fp8_dequant_dense does (bf16_rn(fp32(e4m3) * scale)) and written into the swizzled bf16
+    // tiles: K chunk by chunk as QK_{j-1} releases it, V once PV_{j-1} is done. Rows past seq_len
+    // or in an out-of-range block are zeros. The next row's loads are issued before each wait.
+    const int t = (warp - 12) * 32 + lane;
+    const float ksc = __ldg(p.k_scale), vsc = __ldg(p.v_scale);
+    auto row_src = [&](const uint8_t* pool, int key) -> const uint4* {
+      if (key >= seq_len) return nullptr;
+      const int col = key / p.block_size;
+      const int blk = col < p.max_blocks ? __ldg(p.block_table + (int64_t)r * p.bt_stride + col) : -1;
+      if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        record_error(p.dev_err, kErrDeviceBounds);
+        return nullptr;
+      }
+      return reinterpret_cast<const uint4*>(pool + (int64_t)blk * p.stride_blk +
+                                            (int64_t)(key % p.block_size) * p.stride_tok +
+                                            (int64_t)kvh * p.stride_head);
+    };
+    uint4 raw[16];
+    auto load_row = [&](const uint4* src) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) raw[q] = src ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+    };
+    // 64 codes of chunk c -> row t of chunk c of a swizzled [4][128][64 x bf16] tile
+    auto store_chunk = [&](uint8_t* tile, int c, float sc) {
+      uint8_t* row = tile + c * kChunkBytes + t * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 hi;
+        const uint4 lo = dequant16_e4m3_bf16(raw[4 * c + q], sc, hi);
+        *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
+        *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
+      }
+    };
+    load_row(row_src(p.k_fp8, t));
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // unrolled: raw[] stays in registers
+        if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        store_chunk(sK, c, ksc);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.k_full[c]);
+      }
+      if (!ok) break;
+      load_row(row_src(p.v_fp8, j * kBN + t));
+      if (j > 0 && !mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) break;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) store_chunk(sV, c, vsc);
+      fence_proxy_async_smem();
+      mbar_arrive(&bar.v_full);
+      if (j + 1 < n_tiles) load_row(row_src(p.k_fp8, (j + 1) * kBN + t));
+    }
   } else if (kConv && warp >= 12) {
     // ---------------------------------------------------------------------------- int8 K widening
     // thread t owns key row t of each tile: its 256 int8 codes come straight from the dense scratch
@@ -770,4 +845,69 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   else if (mode == 1) launch(paged_prefill_attn_kernel<1>, Cfg<1>::kThreads, Cfg<1>::kSmem, attr1);
   else launch(paged_prefill_attn_kernel<2>, Cfg<2>::kThreads, Cfg<2>::kSmem, attr2);
   return check_launch("paged_prefill_attn");
+}
+
+extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
+                                                 const float* k_scale, const float* v_scale, int64_t num_blocks,
+                                                 int64_t stride_blk, int64_t stride_tok, int64_t stride_head,
+                                                 const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                                                 const int32_t* seq_lens, const int32_t* query_start_loc,
+                                                 int32_t num_reqs, int32_t total_q, int32_t max_q_len,
+                                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                 int32_t block_size, float softmax_scale, void* out,
+                                                 int32_t* dev_err, void* stream) {
+  using namespace pkv;
+  clear_error();
+  PKV_UNSUP(head_dim == kD, "paged_prefill_attn_fp8: head_dim must be 256 (got %d)", head_dim);
+  if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;  // nothing to do, nothing read
+  PKV_ARG(q && k_fp8 && v_fp8 && k_scale && v_scale && block_table && seq_lens && query_start_loc && out,
+          "paged_prefill_attn_fp8: null pointer argument");
+  PKV_ARG(num_reqs > 0 && total_q > 0 && max_q_len > 0 && num_blocks > 0 && block_size > 0 && max_blocks > 0 &&
+              bt_stride >= max_blocks && num_q_heads > 0 && num_kv_heads > 0,
+          "paged_prefill_attn_fp8: bad size argument");
+  PKV_UNSUP(num_q_heads % num_kv_heads == 0, "paged_prefill_attn_fp8: num_q_heads %% num_kv_heads != 0");
+  PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0, "paged_prefill_attn_fp8: strides must be positive");
+  PKV_ARG(aligned16(q) && aligned16(out) && aligned16(k_fp8) && aligned16(v_fp8) && stride_blk % 16 == 0 &&
+              stride_tok % 16 == 0 && stride_head % 16 == 0,
+          "paged_prefill_attn_fp8: q, out, pools and pool strides must be 16-byte aligned");
+  PKV_ARG(softmax_scale > 0.0f, "paged_prefill_attn_fp8: softmax_scale must be positive");
+
+  Params p{};
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)num_q_heads, (uint64_t)total_q};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)num_q_heads * kD * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kBM};
+    pkv_status s = encode_tiled(&p.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, "q");
+    if (s != PKV_OK) return s;
+  }
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.num_blocks = num_blocks;
+  p.max_blocks = max_blocks;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.num_q_heads = num_q_heads;
+  p.group = num_q_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.seg = gcd_int(block_size, kBN);
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.num_kv_heads = num_kv_heads;
+  p.n_mtiles = (max_q_len + kBM - 1) / kBM;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.dev_err = dev_err;
+  p.k_fp8 = k_fp8;
+  p.v_fp8 = v_fp8;
+  p.stride_blk = stride_blk;
+  p.stride_tok = stride_tok;
+  p.stride_head = stride_head;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(paged_prefill_attn_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<3>::kSmem);
+    attr = true;
+  }
+  dim3 grid((unsigned)p.n_mtiles, (unsigned)num_q_heads, (unsigned)num_reqs);
+  paged_prefill_attn_kernel<3><<<grid, Cfg<3>::kThreads, Cfg<3>::kSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  return check_launch("paged_prefill_attn_fp8");
 }

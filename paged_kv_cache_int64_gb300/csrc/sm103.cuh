@@ -4,6 +4,7 @@
 // the shared-memory / instruction descriptors of the 5th-generation tensor core.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -273,6 +274,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 16 e4m3 codes -> 16 bf16 values (8 packed words, low 4 returned, high 4 in hi_out), each
+// bf16_rn(fp32(e4m3) * s): the hardware e4m3x2 -> f16x2 conversion (exact), widening to fp32, one
+// fp32 multiply rounded to nearest, then round-to-nearest-even to bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+__device__ __forceinline__ uint4 dequant16_e4m3_bf16(uint4 in, float s, uint4& hi_out) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(w[i] >> (16 * half)));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      o[2 * i + half] = pack_bf16x2(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
+    }
+  }
+  hi_out = make_uint4(o[4], o[5], o[6], o[7]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace pkv

@@ -11,32 +11,32 @@
 // tokens are spread over adjacent CTAs that read the same keys; columns past the CTA's tokens are
 // zero padding, so a T = 1 decode step runs on the same kernel), and the MMAs are "swapped" so the
 // 128 keys of a tile are the M dimension (the verify step is HBM-bound at ~63 flop per cache byte):
-//   warps 0, 3 TMA producers (K and V): Q once; per 128-key tile, the int8 codes (4-D maps over the
-//              paged pool, block id as a coordinate) and fp32 scales (3-D maps, same block id) of K
-//              (warp 0) and of V (warp 3), each into its own two-stage ring: 3 copies for a tile
-//              inside one block, per-segment copies (gcd(block_size, 128) keys) across blocks.
+//   warps 0, 3 TMA producers (K and V): Q once; per 128-key tile, the int8 (or e4m3) codes of K
+//              (warp 0) and of V (warp 3) through 4-D maps over the paged pool (block id as a
+//              coordinate), each into its own two-stage ring: 2 copies for a tile inside one
+//              block, per-segment copies (gcd(block_size, 128) keys) across blocks.
 //   warp 1     MMA issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
 //              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory),
 //              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
 //              and P^T fp16 in shared memory).
 //   warps 8-11 K converter: thread k owns key row k and widens it into the tile's tensor-memory K
-//              buffer (two buffers, so tile j+1 is widened while tile j is scored); the key's K
-//              scale goes to a 4-deep ring of TMEM columns read by the softmax, and the K stage is
-//              released at once.
-//   warps 12-15 V converter: once the previous PV has read the V tile, thread k hands its key's V
-//              scale to the softmax (a 2-deep ring of TMEM columns), widens V row k into the tile
-//              (shared memory, MN-major) and releases the V stage. The stages thus never wait for
-//              the softmax, and the K side keeps running while the V side waits for PV. int8 ->
-//              fp16 by byte permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one
+//              buffer (two buffers, so tile j+1 is widened while tile j is scored), then releases
+//              the K stage.
+//   warps 12-15 V converter: once the previous PV has read the V tile, thread k widens V row k into
+//              it (shared memory, MN-major) and releases the V stage. No stage waits for the
+//              softmax, and the K side keeps running while the V side waits for PV. int8 -> fp16
+//              by byte permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one
 //              subtraction of 1152 gives b exactly - the int8->fp16 method of Kim et al. 2022,
 //              "Who Says Elephants Can't Run"); e4m3 -> fp16 by the hardware conversion (exact;
 //              the per-tensor scales multiply the scores and the output).
 //   warps 4-7, 16-19 softmax, two warpgroups of 16 query columns each: thread k owns key k's 16
-//              scores of its group (TMEM lane k of S^T), scaled by the key's K scale; column
-//              maxima by a shuffle reduce-scatter per warp and shared memory across the group's
-//              four warps, after which lane l keeps column (l & 15)'s running max (moved only when
-//              it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale in fp16;
-//              at the end, column sums, normalised partial O and its log-sum-exp.
+//              scores of its group (TMEM lane k of S^T) and reads the key's K and V scales from the
+//              scale pools itself, a tile ahead; scores scaled by the K scale; column maxima by a
+//              shuffle reduce-scatter per warp and shared memory across the group's four warps,
+//              after which lane l keeps column (l & 15)'s running max (moved only when it grows by
+//              more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale in fp16 into one of
+//              two buffers, so the softmax waits for the PV two tiles back (and for the last one
+//              only to rescale O^T); at the end, column sums, normalised partial O and its LSE.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,21 +59,18 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; }    // 2 x 128: fp16 K rows
 __host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
 constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
-constexpr uint32_t kColKs = 384;          // 4 x 1 column: the K scale of each key, tile j in column j % 4
-constexpr uint32_t kColVs = 388;          // 2 x 1 column: the V scale of each key, tile j in column j % 2
 constexpr float kRescaleThreshold = 8.0f;
 
 // shared memory layout (1024-aligned). K and V stages are separate rings, so the K codes of tile
 // j+2 can stream in as soon as tile j's K is widened, without waiting for its V.
 constexpr int kOffQ = 0;                         // 4 x kQChunk = 16 KB
-constexpr int kStageCodes = 0;                   // within a K or V stage: [2 chunks][128 rows][128 B]
-constexpr int kStageScales = 2 * kChunk8;        // then [128 keys][4] fp32
-constexpr int kStageBytes = kStageScales + kBN * 16;  // 34 KB
+constexpr int kStageCodes = 0;                   // a K or V stage: [2 chunks][128 rows][128 B] codes
+constexpr int kStageBytes = 2 * kChunk8;         // 32 KB
 constexpr int kOffKStage = kOffQ + 4 * kQChunk;
 constexpr int kOffVStage = kOffKStage + 2 * kStageBytes;
 constexpr int kOffV16 = kOffVStage + 2 * kStageBytes;
 constexpr int kOffP = kOffV16 + 4 * kChunk16;
-constexpr int kTiles = kOffP + 2 * kPChunk;
+constexpr int kTiles = kOffP + 4 * kPChunk;  // P^T: two buffers of [2 chunks] (64 keys each)
 
 struct alignas(16) Barriers {
   uint64_t q_full, q_ready;
@@ -81,10 +78,11 @@ struct alignas(16) Barriers {
   uint64_t vst_full[2], vst_free[2];  // V stage ring (freed by the V converter)
   uint64_t k_ready[2], k_free[2];     // K_j in TMEM buffer j%2; QK_j done with it
   uint64_t v_ready;                   // V_j widened into shared memory
-  uint64_t vs_ready;                  // the V scales of tile j in TMEM (int8 cache)
   uint64_t s_full[2];                 // S^T_j in TMEM buffer j%2
-  uint64_t p_full;                    // P^T_j written, O^T rescaled
-  uint64_t pv_done;                   // PV_j complete (V and P^T buffers free, O^T current)
+  uint64_t p_full[2];                 // P^T_j (buffer j%2) written, O^T rescaled; per tile parity,
+                                      // since the softmax may run a tile ahead of the MMA's wait
+  uint64_t pv_done[2];                // PV_j complete (V tile and P^T buffer j%2 free, O^T current),
+                                      // one barrier per tile parity (the softmax waits two tiles back)
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
@@ -96,12 +94,8 @@ struct Params {
   CUtensorMap qmap;   // bf16 [R*T][Hq][D]: dims {D, Hq, R*T}, box {64, g, T}
   CUtensorMap k8map;  // int8 pool: dims {D, Hkv, bs, nb}, box {128, 1, G, 1}
   CUtensorMap v8map;
-  CUtensorMap ksmap;  // fp32 scales: dims {Hkv, bs, nb}, box {4, G, 1}
-  CUtensorMap vsmap;
   CUtensorMap k8map_big;  // box {128, 1, 128, 1}: a whole tile inside one block (bs >= 128)
   CUtensorMap v8map_big;
-  CUtensorMap ksmap_big;  // box {4, 128, 1}
-  CUtensorMap vsmap_big;
   int32_t big_ok;
   const int32_t* block_table;
   int64_t bt_stride, num_blocks;
@@ -116,6 +110,9 @@ struct Params {
   int* dev_err;
   const float* k_descale;  // fp8 cache: per-tensor scales (device scalars)
   const float* v_descale;
+  const float* k_scale;    // int8 cache: per-token-head scales [nb][bs][Hkv], read by the softmax
+  const float* v_scale;
+  int64_t scale_stride_blk, scale_stride_tok;
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -214,9 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_init(&bar.s_full[s], 1);
     }
     mbar_init(&bar.v_ready, 128);
-    mbar_init(&bar.vs_ready, 128);
-    mbar_init(&bar.p_full, 256);
-    mbar_init(&bar.pv_done, 1);
+    mbar_init(&bar.p_full[0], 256);
+    mbar_init(&bar.p_full[1], 256);
+    mbar_init(&bar.pv_done[0], 1);
+    mbar_init(&bar.pv_done[1], 1);
     bar.abort = 0;
     fence_mbar_init();
   }
@@ -234,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 
   if (warp == 0 || warp == 3) {
     // ---------------------------------------------------------------------------- producers
-    // warp 0 streams the K codes and K scales, warp 3 the V codes and V scales, each through its
-    // own two-stage ring; both read the block table for their tiles
+    // warp 0 streams the K codes, warp 3 the V codes, each through its own two-stage ring; both
+    // read the block table for their tiles
     const bool is_k = warp == 0;
     const int nseg = kBN / G;
     if (is_k && lane == 0) {
@@ -248,8 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     uint32_t* badw = is_k ? bar.kbad : bar.vbad;
     const CUtensorMap* codes = is_k ? &p.k8map : &p.v8map;
     const CUtensorMap* codes_big = is_k ? &p.k8map_big : &p.v8map_big;
-    const CUtensorMap* scales = is_k ? &p.ksmap : &p.vsmap;
-    const CUtensorMap* scales_big = is_k ? &p.ksmap_big : &p.vsmap_big;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
@@ -268,25 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const uint32_t nloaded = __popc(__ballot_sync(0xffffffffu, blk >= 0));
       const int blk0 = __shfl_sync(0xffffffffu, blk, 0);
       const int slot0 = key0 % p.block_size;
-      // the 128 keys lie in one valid block: 2 copies of 128 rows for the codes (+ 1 for scales)
+      // the 128 keys lie in one valid block: 2 copies of 128 rows
       const bool big = p.big_ok && bad == 0 && blk0 >= 0 && slot0 + kBN <= p.block_size;
       if (lane == 0) {
         if (bad) record_error(p.dev_err, kErrDeviceBounds);
         badw[st] = bad;
         const uint32_t rows = big ? (uint32_t)kBN : nloaded * (uint32_t)G;
-        mbar_arrive_expect_tx(&full[st], rows * (kFp8 ? 2u * 128u : 2u * 128u + 16u));
-        if (big) {
+        mbar_arrive_expect_tx(&full[st], rows * 2u * 128u);
+        if (big)
           for (int c = 0; c < 2; ++c)
             tma_load_4d(stage + kStageCodes + c * kChunk8, codes_big, &full[st], c * 128, kvh, slot0, blk0);
-          if (!kFp8) tma_load_3d(stage + kStageScales, scales_big, &full[st], (kvh & ~3), slot0, blk0);
-        }
       }
       __syncwarp();
       if (!big && blk >= 0) {
         const int slot = (key0 + lane * G) % p.block_size;
         for (int c = 0; c < 2; ++c)
           tma_load_4d(stage + kStageCodes + c * kChunk8 + lane * G * 128, codes, &full[st], c * 128, kvh, slot, blk);
-        if (!kFp8) tma_load_3d(stage + kStageScales + lane * G * 16, scales, &full[st], (kvh & ~3), slot, blk);
       }
     }
   } else if (warp == 1) {
@@ -296,15 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
       const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&bar.p_full, i & 1, abort)) return false;
+        if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
         if (!mbar_wait(&bar.v_ready, i & 1, abort)) return false;
         tc_fence_after();
+        const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
         for (int hh = 0; hh < 2; ++hh)
           for (int ks = 0; ks < 8; ++ks)
             umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
-                        smem_desc(p_base + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
+                        smem_desc(pb + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
                         (i > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&bar.pv_done);
+        umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
       bool ok = mbar_wait(&bar.q_ready, 0, abort);
@@ -357,11 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
-      if (!kFp8) {  // the key's scale goes to the softmax through TMEM (0 for a dead key), so the
-                    // stage is released here and never waits for the softmax
-        const float ks = live ? reinterpret_cast<const float*>(kstage + kStageScales)[k * 4 + (kvh & 3)] : 0.0f;
-        tmem_st_32x32b_x1(tmem + lane_off + kColKs + (j & 3), __float_as_uint(ks));
-      }
 #pragma unroll 1
       for (int w4 = 0; w4 < 4; ++w4) {
         uint32_t kv[32];
@@ -387,21 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // thread k owns key row k: once PV_{j-1} has read the V tile, its V row -> fp16 into the
     // MN-major V tile (zeros outside the split or in a bad block)
     const int k = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
-      bool got = j == 0 || mbar_wait(&bar.pv_done, (j - 1) & 1, abort);
+      bool got = j == 0 || mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
       if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
-      if (!kFp8) {  // the key's V scale goes to the softmax first (it scales P^T), then the codes
-        const float vs = live ? reinterpret_cast<const float*>(vstage + kStageScales)[k * 4 + (kvh & 3)] : 0.0f;
-        tmem_st_32x32b_x1(tmem + lane_off + kColVs + (j & 1), __float_as_uint(vs));
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bar.vs_ready);
-      }
 #pragma unroll 1
       for (int c8 = 0; c8 < 2; ++c8) {
 #pragma unroll
@@ -428,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // key k's 16 scores of its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter
     // leaves column (lane & 15)'s warp maximum in the lane, shared memory combines the four warps;
     // lane l then keeps column (l & 15)'s running max (the same in all four warps) and hands it to
-    // the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T.
+    // the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T; each
+    // thread reads its key's two scales from the cache itself, two tiles ahead (the block id three
+    // tiles ahead), so no stage buffer waits for the softmax and the HBM latency is covered.
     const int grp = warp >= 16 ? 1 : 0;
     const int c0 = 16 * grp;       // the group's first query column
     const int cl = lane & 15;      // this lane keeps the running max of column c0 + cl
@@ -436,6 +419,33 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
+    // block id of this thread's key in tile jj (-1: past the split or a bad table entry)
+    auto key_block = [&](int jj) -> int {
+      const int key = k_begin + jj * kBN + k;
+      if (jj >= n_tiles || key >= k_end) return -1;
+      const int col = key / p.block_size;
+      if (col >= p.max_blocks) return -1;
+      const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
+      return (blk < 0 || (int64_t)blk >= p.num_blocks) ? -1 : blk;
+    };
+    // the key's K and V scales in tile jj (0 for a dead key: its K and V rows are zero)
+    auto key_scales = [&](int jj, int blk, float& ks, float& vs) {
+      ks = vs = 0.0f;
+      if (blk >= 0) {
+        const int64_t off = (int64_t)blk * p.scale_stride_blk +
+                            (int64_t)((k_begin + jj * kBN + k) % p.block_size) * p.scale_stride_tok + kvh;
+        ks = __ldg(p.k_scale + off);
+        vs = __ldg(p.v_scale + off);
+      }
+    };
+    // scales of tiles j and j+1, block id of tile j+2 (e4m3: per-tensor scales on scores and output)
+    float ks_cur = 0.0f, vs_cur = 1.0f, ks_1 = 0.0f, vs_1 = 1.0f;
+    int blk_2 = -1;
+    if (!kFp8) {
+      key_scales(0, key_block(0), ks_cur, vs_cur);
+      key_scales(1, key_block(1), ks_1, vs_1);
+      blk_2 = key_block(2);
+    }
     float l_part[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) l_part[q] = 0.0f;
@@ -446,15 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const int key0 = k_begin + j * kBN;
       const int key = key0 + k;
       const bool in_range = key < k_end;
+      // tile j+2's scales and tile j+3's block id are fetched while this tile is scored
+      float ks_2 = 0.0f, vs_2 = 1.0f;
+      if (!kFp8) {
+        key_scales(j + 2, blk_2, ks_2, vs_2);
+        blk_2 = key_block(j + 3);
+      }
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
       float s[16];
       {
         uint32_t v[16];
-        float ks = kFp8 ? k_descale : 0.0f;  // a dead key's K row is zero: its score is 0 either way
+        const float ks = kFp8 ? k_descale : ks_cur;
         if (!dead) {
           tc_fence_after();
           tmem_ld_32x32b_x16(tmem + lane_off + col_s(st) + c0, v);
-          if (!kFp8) ks = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + kColKs + (j & 3)));
           tmem_wait_ld();
         }
         const float f = p.scale_log2 * ks;
@@ -494,24 +509,32 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       const float mu = m_col == -INFINITY ? 0.0f : m_col;
       const bool any_rescale = __any_sync(0xffffffffu, rescale);  // the same in all four warps
-      // P^T and O^T are touched only once PV_{j-1} has completed
-      if (!dead && j > 0) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done, (j - 1) & 1, abort));
-      float vs = 1.0f;  // e4m3: the per-tensor V scale multiplies the output instead
-      if (!kFp8) {
-        if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.vs_ready, j & 1, abort));
-        if (!dead) {
-          tc_fence_after();
-          vs = __uint_as_float(tmem_ld_32x32b_x1(tmem + lane_off + kColVs + (j & 1)));
-          tmem_wait_ld();
-        }
-      }
+      // P^T buffer j%2 was last read by PV_{j-2}; O^T may be rescaled only once PV_{j-1} is done
+      if (!dead && j >= 2)
+        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
+      if (!dead && any_rescale && j >= 1)
+        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
+      // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
+      // the running column sums and the fp16 P^T stores run as independent batches
+      float e[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float e = ex2_approx(s[q] - __shfl_sync(0xffffffffu, mu, q));
-        if (any_rescale) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e;
-        else l_part[q] += e;
-        if (!dead)  // P^T column for key k: p * v_scale, fp16
-          *reinterpret_cast<__half*>(sP + (k >> 6) * kPChunk + sw128_offset(c0 + q, k & 63)) = __float2half_rn(e * vs);
+      for (int q = 0; q < 16; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) e[q] = ex2_approx(s[q] - e[q]);
+      if (any_rescale) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) l_part[q] += e[q];
+      }
+      if (!dead) {  // P^T column for key k (rows c0..c0+15 of buffer j % 2): p * v_scale, fp16
+        const float vs = vs_cur;
+        uint8_t* pt = sP + (j & 1) * 2 * kPChunk + (k >> 6) * kPChunk + c0 * 128 + (k & 7) * 2;
+        const uint32_t kc = (uint32_t)(k & 63) >> 3;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          *reinterpret_cast<__half*>(pt + q * 128 + ((kc ^ (uint32_t)(q & 7)) * 16)) = __float2half_rn(e[q] * vs);
       }
       if (!dead) {
         tc_fence_after();
@@ -530,11 +553,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bar.p_full);
+        mbar_arrive(&bar.p_full[j & 1]);
       }
+      ks_cur = ks_1;
+      vs_cur = vs_1;
+      ks_1 = ks_2;
+      vs_1 = vs_2;
     }
     // epilogue: column sums, O^T / l, log-sum-exp (each group for its 16 columns)
-    bool fin = !dead && !*abort && mbar_wait(&bar.pv_done, (n_tiles - 1) & 1, abort);
+    bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
@@ -633,15 +660,16 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   const int tpc = T < kNQ / group ? T : kNQ / group;  // tokens per CTA
   const int n_tg = (T + tpc - 1) / tpc;                // CTAs per (split, KV head, request)
   PKV_ARG((int64_t)max_splits * n_tg < (1ll << 31), "%s: grid too large", name);
-  PKV_UNSUP(kFp8 || num_kv_heads % 4 == 0, "%s: num_kv_heads must be a multiple of 4", name);
   PKV_UNSUP(block_size % 8 == 0, "%s: block_size must be a multiple of 8", name);
   PKV_UNSUP(split_tokens % kBN == 0, "%s: split_tokens must be a multiple of 128", name);
   PKV_ARG(stride_blk > 0 && stride_tok > 0 && stride_head > 0 && (kFp8 || (scale_stride_blk > 0 && scale_stride_tok > 0)),
           "%s: strides must be positive", name);
-  PKV_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && (kFp8 || (aligned16(k_sc) && aligned16(v_sc))) &&
-              stride_blk % 16 == 0 && stride_tok % 16 == 0 && stride_head % 16 == 0 &&
-              (kFp8 || (scale_stride_blk % 4 == 0 && scale_stride_tok % 4 == 0)),
-          "%s: pointers and strides must be 16-byte aligned", name);
+  PKV_ARG(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && stride_blk % 16 == 0 && stride_tok % 16 == 0 &&
+              stride_head % 16 == 0,
+          "%s: q, caches and cache strides must be 16-byte aligned", name);
+  PKV_ARG(kFp8 || ((reinterpret_cast<uintptr_t>(k_sc) & 3) == 0 && (reinterpret_cast<uintptr_t>(v_sc) & 3) == 0 &&
+                   scale_stride_tok >= num_kv_heads),
+          "%s: scale pools must be 4-byte aligned, with scale_stride_tok >= num_kv_heads", name);
   PKV_ARG(softmax_scale > 0.0f, "%s: softmax_scale must be positive", name);
   Params p{};
   const int G = gcd_int(block_size, kBN);
@@ -670,21 +698,10 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
     }
   }
   if (!kFp8) {
-    const uint64_t dims[3] = {(uint64_t)num_kv_heads, (uint64_t)block_size, (uint64_t)num_blocks};
-    const uint64_t strides[2] = {(uint64_t)scale_stride_tok * 4, (uint64_t)scale_stride_blk * 4};
-    const uint32_t box[3] = {4, (uint32_t)G, 1};
-    pkv_status s = encode_tiled(&p.ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_sc, dims, strides, box, "k_scale",
-                                false);
-    if (s != PKV_OK) return s;
-    s = encode_tiled(&p.vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_sc, dims, strides, box, "v_scale", false);
-    if (s != PKV_OK) return s;
-    if (block_size >= kBN) {
-      const uint32_t big[3] = {4, (uint32_t)kBN, 1};
-      s = encode_tiled(&p.ksmap_big, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, k_sc, dims, strides, big, "k_scale", false);
-      if (s != PKV_OK) return s;
-      s = encode_tiled(&p.vsmap_big, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, v_sc, dims, strides, big, "v_scale", false);
-      if (s != PKV_OK) return s;
-    }
+    p.k_scale = k_sc;
+    p.v_scale = v_sc;
+    p.scale_stride_blk = scale_stride_blk;
+    p.scale_stride_tok = scale_stride_tok;
   } else {
     p.k_descale = k_sc;
     p.v_descale = v_sc;

@@ -57,7 +57,7 @@ def test_library_targets_sm103a(libpath):
 
 
 def test_abi_version(pkv):
-    assert pkv.lib.pkv_abi_version() == 3
+    assert pkv.lib.pkv_abi_version() == 4
 
 
 def test_workspace_bytes(pkv):
@@ -152,3 +152,18 @@ def test_cache_write_rejects_bad_arguments(pkv, kw, status):
 def test_cache_write_empty_batch_launches_nothing(pkv):
     assert pkv.lib.pkv_kv_cache_write(*_write_args(R=0)) == 0
     assert pkv.lib.pkv_kv_cache_write(*_write_args(max_q=0, kn=None)) == 0
+
+
+def test_fused_fp8_prefill_rejects_bad_arguments(pkv):
+    f = pkv.lib.pkv_paged_prefill_attn_fp8
+    base = [16, 16, 16, 16, 16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 1, 1, 16, 4, 256, 16, 0.0625, 16, None, None]
+    bad = list(base); bad[19] = 128   # head_dim != 256
+    assert f(*bad) == 2
+    bad = list(base); bad[1] = None   # null K pool
+    assert f(*bad) == 1
+    bad = list(base); bad[7] = 1000   # token stride not 16-byte aligned
+    assert f(*bad) == 1
+    bad = list(base); bad[17] = 15    # q heads not a multiple of kv heads
+    assert f(*bad) == 2
+    empty = list(base); empty[14] = 0  # no requests: nothing launched
+    assert f(*empty) == 0

@@ -299,6 +299,77 @@ def test_fp8_prefill_through_dense_scratch(pkv):
     assert worst <= TOL_BF16
 
 
+def _fp8_dense_then_prefill(pkv, p, k, v, scale):
+    """The dequantize-once path: dense bf16 scratch (identity table, block_size = max_seq), then the
+    bf16 prefill on it."""
+    bt, sl, qsl = device_meta(p)
+    max_seq = int(p.seq_lens.max())
+    kd = torch.zeros((p.num_reqs, max_seq, p.num_kv_heads, 256), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    err = dev_err()
+    pkv.kv_fp8_dequant_dense(k, v, bt, sl, scale, scale, kd, vd, dev_err=err)
+    ident = torch.arange(p.num_reqs, dtype=torch.int32, device="cuda").reshape(p.num_reqs, 1)
+    q = device_q(p)
+    out = torch.empty_like(q)
+    pkv.paged_prefill_attn(q, kd, vd, ident, sl, qsl, max(r.q_len for r in p.requests), p.softmax_scale, out,
+                           dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return bf16_to_u16(out)
+
+
+def _fp8_fused(pkv, p, k, v, scale, bt=None, expect_err=0):
+    b, sl, qsl = device_meta(p)
+    q = device_q(p)
+    out = torch.full_like(q, float("nan"))
+    err = dev_err()
+    pkv.paged_prefill_attn_fp8(q, k, v, scale, scale, b if bt is None else bt, sl, qsl,
+                               max(r.q_len for r in p.requests), p.softmax_scale, out, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == expect_err
+    return bf16_to_u16(out)
+
+
+@pytest.mark.parametrize("case", ["ctx32k_bs880", "ragged_bs16", "gqa6_bs80"])
+def test_fp8_fused_prefill_equals_dense_path(pkv, case):
+    """Per-tile dequantization inside the prefill against the dequantize-once dense scratch: both
+    attend over the same bf16 values with the same kernel arithmetic, so the outputs are identical
+    bit for bit; sampled rows are also checked against the oracle."""
+    if case == "ctx32k_bs880":
+        p = W.make_problem("f8f", seed=45, seq_lens=[32768], q_lens=[2048], num_blocks=200, block_size=880,
+                           kv_dtype="e4m3")
+    elif case == "ragged_bs16":
+        p = W.make_problem("f8r", seed=46, seq_lens=[300, 1000, 129], q_lens=[300, 200, 1], num_blocks=120,
+                           block_size=16, kv_dtype="e4m3")
+    else:
+        p = W.make_problem("f8g", seed=47, seq_lens=[704, 333], q_lens=[250, 333], num_blocks=40, block_size=80,
+                           num_q_heads=24, num_kv_heads=4, kv_dtype="e4m3")
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    scale = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    dense = _fp8_dense_then_prefill(pkv, p, k, v, scale)
+    fused = _fp8_fused(pkv, p, k, v, scale)
+    assert np.array_equal(fused, dense)
+    rk, rv = oracle.kv_fp8_dequant_dense(p.pool_numpy("k"), p.pool_numpy("v"), p.block_table(fill=0), p.seq_lens,
+                                         int(p.seq_lens.max()), 0.5, 0.5)
+    ident = np.arange(p.num_reqs, dtype=np.int32).reshape(p.num_reqs, 1)
+    worst = 0.0
+    for t in sorted({0, p.total_q // 2, p.total_q - 1}):
+        ref = oracle.paged_prefill_attn(p.q, rk, rv, ident, p.seq_lens, p.query_start_loc, p.num_q_heads,
+                                        p.softmax_scale, tok_begin=t, tok_end=t + 1)
+        worst = max(worst, _close(fused[t:t + 1], ref, TOL_BF16))
+    assert worst <= TOL_BF16
+
+
+def test_fp8_fused_prefill_bad_block_reads_zero(pkv):
+    p = W.make_problem("f8b", seed=48, seq_lens=[400], q_lens=[100], num_blocks=40, block_size=16, kv_dtype="e4m3")
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    scale = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    bt = p.block_table(fill=-1)
+    bt[0, 3] = p.num_blocks + 7  # keys 48..63
+    out = _fp8_fused(pkv, p, k, v, scale, bt=torch.from_numpy(bt).cuda(), expect_err=4)
+    assert np.isfinite(W.bf16_bits_to_f32(out)).all()
+
+
 # ---------------------------------------------------------------------------------------------
 # A5 / A6: speculative verify
 # ---------------------------------------------------------------------------------------------
