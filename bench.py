@@ -41,7 +41,7 @@ METRIC = "paged prefill-attn tok/s & TFLOP/s (% tensor peak); verify-attn HBM GB
 CHUNK = W.BIGPOOL_CHUNK
 L = W.BIGPOOL_L
 T_VERIFY = 8
-SPLIT = 2048
+SPLIT = 4096
 HQ, HKV, D, BS = 16, 4, 256, W.BIGPOOL_BS
 FLOP_PER_PAIR = 4 * D * HQ  # QK and PV, 2 flops per MAC, all 16 query heads
 

@@ -50,7 +50,7 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 640;
+constexpr int kThreads = 768;
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
@@ -77,7 +77,8 @@ struct alignas(16) Barriers {
   uint64_t kst_full[2], kst_free[2];  // K stage ring (freed by the K converter)
   uint64_t vst_full[2], vst_free[2];  // V stage ring (freed by the V converter)
   uint64_t k_ready[2], k_free[2];     // K_j in TMEM buffer j%2; QK_j done with it
-  uint64_t v_ready;                   // V_j widened into shared memory
+  uint64_t v_ready[2];                // half h (head_dim 128h..128h+127) of V_j widened into shared memory
+  uint64_t v_free[2];                 // half h of the V tile read by PV_j
   uint64_t s_full[2];                 // S^T_j in TMEM buffer j%2
   uint64_t p_full[2];                 // P^T_j (buffer j%2) written, O^T rescaled; per tile parity,
                                       // since the softmax may run a tile ahead of the MMA's wait
@@ -205,12 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_init(&bar.kst_full[s], 1);
       mbar_init(&bar.kst_free[s], 128);
       mbar_init(&bar.vst_full[s], 1);
-      mbar_init(&bar.vst_free[s], 128);
+      mbar_init(&bar.vst_free[s], 256);
       mbar_init(&bar.k_ready[s], 128);
       mbar_init(&bar.k_free[s], 1);
       mbar_init(&bar.s_full[s], 1);
     }
-    mbar_init(&bar.v_ready, 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bar.v_ready[h], 128);
+      mbar_init(&bar.v_free[h], 1);
+    }
     mbar_init(&bar.p_full[0], 256);
     mbar_init(&bar.p_full[1], 256);
     mbar_init(&bar.pv_done[0], 1);
@@ -290,14 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {
         if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
-        if (!mbar_wait(&bar.v_ready, i & 1, abort)) return false;
-        tc_fence_after();
         const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
-        for (int hh = 0; hh < 2; ++hh)
+        for (int hh = 0; hh < 2; ++hh) {  // each half of head_dim as soon as its V half is widened
+          if (!mbar_wait(&bar.v_ready[hh], i & 1, abort)) return false;
+          tc_fence_after();
           for (int ks = 0; ks < 8; ++ks)
             umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
                         smem_desc(pb + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
                         (i > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&bar.v_free[hh]);
+        }
         umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
@@ -352,55 +358,55 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       tc_fence_after();
       const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
 #pragma unroll 1
-      for (int w4 = 0; w4 < 4; ++w4) {
-        uint32_t kv[32];
+      for (int w8 = 0; w8 < 8; ++w8) {  // 32 codes = 16 TMEM columns per step
+        uint32_t kv[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int q8 = 4 * (w4 & 1) + i;
-          const uint4 v = *reinterpret_cast<const uint4*>(kstage + kStageCodes + (w4 >> 1) * kChunk8 + k * 128 +
+        for (int i = 0; i < 2; ++i) {
+          const int q8 = 2 * (w8 & 3) + i;
+          const uint4 v = *reinterpret_cast<const uint4*>(kstage + kStageCodes + (w8 >> 2) * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
-          widen16<kFp8>(v, o);
+          widen16<kFp8>(live ? v : make_uint4(0, 0, 0, 0), o);  // zero codes widen to zeros
 #pragma unroll
-          for (int e = 0; e < 8; ++e) kv[8 * i + e] = live ? o[e] : 0u;
+          for (int e = 0; e < 8; ++e) kv[8 * i + e] = o[e];
         }
-        tmem_st_32x32b_x32(tmem + lane_off + col_k(st) + 32 * w4, kv);
+        tmem_st_32x32b_x16(tmem + lane_off + col_k(st) + 16 * w8, kv);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar.k_ready[st]);
       mbar_arrive(&bar.kst_free[st]);
     }
-  } else if (warp >= 12 && warp < 16) {
+  } else if ((warp >= 12 && warp < 16) || warp >= 20) {
     // ---------------------------------------------------------------------------- V converter
-    // thread k owns key row k: once PV_{j-1} has read the V tile, its V row -> fp16 into the
-    // MN-major V tile (zeros outside the split or in a bad block)
+    // two warpgroups, one per half of head_dim (warps 12-15: 0-127, warps 20-23: 128-255), each with
+    // its own ready / free barriers, so half 0 of V_{j+1} is widened while PV_j still reads half 1.
+    // Thread k owns key row k: its half V row -> fp16 into the MN-major V tile (zeros outside the
+    // split or in a bad block: the codes are zeroed before widening, which maps 0 to 0).
+    const int hv = warp >= 20 ? 1 : 0;
     const int k = (warp & 3) * 32 + lane;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
-      bool got = j == 0 || mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+      bool got = j == 0 || mbar_wait(&bar.v_free[hv], (j - 1) & 1, abort);
       if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
-#pragma unroll 1
-      for (int c8 = 0; c8 < 2; ++c8) {
+      const uint8_t* src = vstage + kStageCodes + hv * kChunk8 + k * 128;
+      uint8_t* dst = sV16 + 2 * hv * kChunk16 + k * 128;
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(vstage + kStageCodes + c8 * kChunk8 + k * 128 +
-                                                          ((q8 ^ (k & 7)) * 16));
-          uint32_t o[8];
-          widen16<kFp8>(v, o);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = live ? o[e] : 0u;
-          uint8_t* row = sV16 + (2 * c8 + (q8 >> 2)) * kChunk16 + k * 128;
-          const uint32_t piece = 2u * (q8 & 3);
-          *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(row + (((piece + 1) ^ (k & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
+      for (int q8 = 0; q8 < 8; ++q8) {
+        uint4 v = *reinterpret_cast<const uint4*>(src + ((q8 ^ (k & 7)) * 16));
+        if (!live) v = make_uint4(0, 0, 0, 0);
+        uint32_t o[8];
+        widen16<kFp8>(v, o);
+        uint8_t* row = dst + (q8 >> 2) * kChunk16;
+        const uint32_t piece = 2u * (q8 & 3);
+        *reinterpret_cast<uint4*>(row + ((piece ^ (k & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(row + (((piece + 1) ^ (k & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bar.v_ready);
+      mbar_arrive(&bar.v_ready[hv]);
       mbar_arrive(&bar.vst_free[st]);
     }
   } else if (warp >= 4) {
