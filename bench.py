@@ -41,7 +41,7 @@ METRIC = "paged prefill-attn tok/s & TFLOP/s (% tensor peak); verify-attn HBM GB
 CHUNK = W.BIGPOOL_CHUNK
 L = W.BIGPOOL_L
 T_VERIFY = 8
-SPLIT = 4096
+SPLIT = 4096  # verify split for the CPU oracle's sample (any split gives the same result)
 HQ, HKV, D, BS = 16, 4, 256, W.BIGPOOL_BS
 FLOP_PER_PAIR = 4 * D * HQ  # QK and PV, 2 flops per MAC, all 16 query heads
 
@@ -50,6 +50,16 @@ def prefill_pairs(seq_len, q_len):
     """causal (query, key) pairs of a chunk: queries at seq_len-q_len .. seq_len-1."""
     s = seq_len - q_len
     return q_len * s + q_len * (q_len + 1) // 2
+
+
+def pick_split(seq_lens, n_sms, hkv=HKV):
+    """split_tokens for a verify launch: the largest of 4096, 2048, 1024, 512 that still gives at
+    least two CTAs per SM (larger splits mean fewer partials to write and combine; smaller ones fill
+    the GPU when there are few or short requests)."""
+    split = 4096
+    while split > 512 and hkv * sum(math.ceil(int(s) / split) for s in seq_lens) < 2 * n_sms:
+        split //= 2
+    return split
 
 
 def verify_bytes(seq_lens, T=T_VERIFY, hq=HQ):
@@ -168,7 +178,8 @@ class Workload:
         self.vks, self.vvs = device_scale_pool(pv, "k"), device_scale_pool(pv, "v")
         self.vbt, self.vsl, _ = device_meta(pv)
         self.vq = device_q(pv)
-        S = pkv.splits_needed(L + T_VERIFY, SPLIT)
+        self.split = pick_split([L + T_VERIFY], torch.cuda.get_device_properties(dev).multi_processor_count)
+        S = pkv.splits_needed(L + T_VERIFY, self.split)
         self.po = torch.empty((S, T_VERIFY, HQ, D), dtype=torch.float32, device=dev)
         self.pl = torch.empty((S, T_VERIFY, HQ), dtype=torch.float32, device=dev)
         self.vout = torch.empty_like(self.vq)
@@ -202,8 +213,9 @@ class Workload:
                                                                 self.qsl, CHUNK, s, self.out[2]))
         rec("verify_partial", lambda: pkv.spec_verify_attn_partial(self.vq, self.vk, self.vv, self.vks, self.vvs,
                                                                    self.vbt, self.vsl, T_VERIFY, self.pv.softmax_scale,
-                                                                   SPLIT, self.po, self.pl))
-        rec("verify_combine", lambda: pkv.spec_verify_combine(self.po, self.pl, self.vsl, T_VERIFY, SPLIT, self.vout))
+                                                                   self.split, self.po, self.pl))
+        rec("verify_combine", lambda: pkv.spec_verify_combine(self.po, self.pl, self.vsl, T_VERIFY, self.split,
+                                                              self.vout))
 
     LAUNCHES_PER_STEP = 7
     TOKENS_PER_STEP = 3 * CHUNK + T_VERIFY
@@ -276,6 +288,7 @@ def run_gpu(args):
     # the two fp8 prefill paths on the step's fp8 chunk: dequantize once into the dense scratch, or
     # dequantize every tile inside the prefill
     fp8_paths = run_fp8_paths(torch, pkv, wl, flush, args)
+    quant_full = run_quant_full_context(torch, pkv, wl, flush, args)
 
     if rank != 0:
         if world > 1:
@@ -317,6 +330,7 @@ def run_gpu(args):
             "fp8_dequant": _gbs(alg["fp8_dequant_bytes"], mean.get("fp8_dequant"), peaks),
             "verify_single_request": _gbs(alg["verify_bytes"], mean.get("verify_partial", 0) +
                                           mean.get("verify_combine", 0), peaks),
+            "int8_quant_full_context": quant_full,
         },
         "verify_batch": vb,
         "fp8_prefill_paths": fp8_paths,
@@ -400,6 +414,30 @@ def run_e2e(torch, pkv, wl, args, dev):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
+def run_quant_full_context(torch, pkv, wl, flush, args):
+    """kv_int8_stats_quant over the request's whole 20,000-token context (a from-scratch prefill's
+    quantization, 80,000 rows: 103 MB moved) rather than one 2,048-token chunk, whose 10 MB pass
+    is launch- and latency-bound."""
+    peaks = load_peaks()
+    nbytes = L * HKV * (2 * D + D + 4 + 2 * D)
+
+    def fn():
+        pkv.kv_int8_stats_quant(wl.k, wl.bt, wl.zero, wl.sl, L, wl.k8, wl.k8s, k16=wl.k16)
+
+    for _ in range(max(3, args.warmup)):
+        fn()
+    ts = []
+    for _ in range(max(5, min(args.steps, 50))):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return _gbs(nbytes, statistics.mean(ts), peaks)
+
+
 def run_fp8_paths(torch, pkv, wl, flush, args):
     """Chunk of 2,048 queries at the end of the 20,000-token e4m3 context, both fp8 prefill paths:
     kv_fp8_dequant_dense + bf16 prefill on the scratch, against paged_prefill_attn_fp8 (per-tile
@@ -449,23 +487,26 @@ def run_verify_batch(torch, pkv, dev, flush, args):
     bt, _, _ = device_meta(p)
     peaks = load_peaks()
 
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
     def measure(q, seq_lens, T, hq):
         sld = torch.from_numpy(np.asarray(seq_lens, dtype=np.int32)).to(dev)
-        S = pkv.splits_needed(int(max(seq_lens)), SPLIT)
+        split = pick_split(seq_lens, n_sms)
+        S = pkv.splits_needed(int(max(seq_lens)), split)
         po = torch.empty((S, q.shape[0], hq, D), dtype=torch.float32, device=dev)
         pl = torch.empty((S, q.shape[0], hq), dtype=torch.float32, device=dev)
         out = torch.empty_like(q)
         for _ in range(max(3, args.warmup)):
-            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, SPLIT, po, pl)
-            pkv.spec_verify_combine(po, pl, sld, T, SPLIT, out)
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, split, po, pl)
+            pkv.spec_verify_combine(po, pl, sld, T, split, out)
         times, tp, tc = [], [], []
         for _ in range(max(5, args.steps)):
             flush.zero_()
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             e[0].record()
-            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, SPLIT, po, pl)
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sld, T, p.softmax_scale, split, po, pl)
             e[1].record()
-            pkv.spec_verify_combine(po, pl, sld, T, SPLIT, out)
+            pkv.spec_verify_combine(po, pl, sld, T, split, out)
             e[2].record()
             e[2].synchronize()
             times.append(e[0].elapsed_time(e[2]))
@@ -478,7 +519,7 @@ def run_verify_batch(torch, pkv, dev, flush, args):
         return {"requests": p.num_reqs, "T": T, "q_heads": hq, "sum_seq_len": int(np.sum(seq_lens)),
                 "algorithmic_bytes": int(nbytes), "ms": round(ms, 4), "gbs": round(g, 1),
                 "frac_hbm": round(g / peaks["hbm_gbs"], 4), "partial_ms": round(statistics.mean(tp), 4),
-                "partial_gbs": round(gp, 1), "combine_ms": round(statistics.mean(tc), 4), "split_tokens": SPLIT}
+                "partial_gbs": round(gp, 1), "combine_ms": round(statistics.mean(tc), 4), "split_tokens": split}
 
     res = measure(device_q(p), p.seq_lens, T_VERIFY, HQ)
     # decode: the first token of each request's verify window, alone
@@ -603,14 +644,15 @@ def run_ncu_case(args):
         ks, vs = device_scale_pool(p, "k"), device_scale_pool(p, "v")
         bt, sl, _ = device_meta(p)
         q = device_q(p)
-        S = pkv.splits_needed(int(p.seq_lens.max()), SPLIT)
+        split = pick_split(p.seq_lens, torch.cuda.get_device_properties(dev).multi_processor_count)
+        S = pkv.splits_needed(int(p.seq_lens.max()), split)
         po = torch.empty((S, q.shape[0], HQ, D), dtype=torch.float32, device=dev)
         pl = torch.empty((S, q.shape[0], HQ), dtype=torch.float32, device=dev)
         out = torch.empty_like(q)
 
         def fn():
-            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sl, T_VERIFY, p.softmax_scale, SPLIT, po, pl)
-            pkv.spec_verify_combine(po, pl, sl, T_VERIFY, SPLIT, out)
+            pkv.spec_verify_attn_partial(q, k, v, ks, vs, bt, sl, T_VERIFY, p.softmax_scale, split, po, pl)
+            pkv.spec_verify_combine(po, pl, sl, T_VERIFY, split, out)
     else:
         nb = 64
         kv_dtype = "e4m3" if case == "fp8_dequant" else "bf16"

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
-      if (lane == 0 && j >= 2) mbar_wait(&freeb[st], ((j >> 1) - 1) & 1, abort);
+      if (lane == 0 && j >= 2) mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort);
       __syncwarp();
       if (*abort) break;
       const int key0 = k_begin + j * kBN;
@@ -293,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
       const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
+        if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
         const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
         for (int hh = 0; hh < 2; ++hh) {  // each half of head_dim as soon as its V half is widened
-          if (!mbar_wait(&bar.v_ready[hh], i & 1, abort)) return false;
+          if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort)) return false;
           tc_fence_after();
           for (int ks = 0; ks < 8; ++ks)
             umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
@@ -307,10 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
-      bool ok = mbar_wait(&bar.q_ready, 0, abort);
+      bool ok = mbar_wait_suspend(&bar.q_ready, 0, abort);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&bar.k_ready[st], (j >> 1) & 1, abort)) break;
+        if (!mbar_wait_suspend(&bar.k_ready[st], (j >> 1) & 1, abort)) break;
         tc_fence_after();
         for (int ks = 0; ks < 16; ++ks)
           umma_f16_ts(tmem + col_s(st), tmem + col_k(st) + ks * 8,
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    bool dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
+    bool dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.q_full, 0, abort));
     if (!dead) {  // row k & 31, chunk k >> 5; padding rows (past the CTA's columns) become zeros
       const int row = k & 31, c = k >> 5;
       const bool live_row = row < nq;
@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
       const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
-      bool got = mbar_wait(&bar.kst_full[st], (j >> 1) & 1, abort);
-      if (got && j >= 2) got = mbar_wait(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
+      bool got = mbar_wait_suspend(&bar.kst_full[st], (j >> 1) & 1, abort);
+      if (got && j >= 2) got = mbar_wait_suspend(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
-      bool got = j == 0 || mbar_wait(&bar.v_free[hv], (j - 1) & 1, abort);
-      if (got) got = mbar_wait(&bar.vst_full[st], (j >> 1) & 1, abort);
+      bool got = j == 0 || mbar_wait_suspend(&bar.v_free[hv], (j - 1) & 1, abort);
+      if (got) got = mbar_wait_suspend(&bar.vst_full[st], (j >> 1) & 1, abort);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
       const uint8_t* src = vstage + kStageCodes + hv * kChunk8 + k * 128;
@@ -426,31 +426,45 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float k_descale = kFp8 ? __ldg(p.k_descale) : 0.0f;
     // block id of this thread's key in tile jj (-1: past the split or a bad table entry)
+    // Position of this thread's key in the pool, advanced tile by tile without divisions:
+    // (col, slot) of key k_begin + t * 128 + k, for the tile t whose block id is looked up next.
+    const int q128 = kBN / p.block_size, r128 = kBN % p.block_size;
+    int col_t = (k_begin + k) / p.block_size, slot_t = (k_begin + k) % p.block_size;
+    auto advance = [&]() {
+      col_t += q128;
+      slot_t += r128;
+      if (slot_t >= p.block_size) {
+        slot_t -= p.block_size;
+        ++col_t;
+      }
+    };
+    // block id of the key in tile jj (at the current (col_t, slot_t)); -1 past the split or bad
     auto key_block = [&](int jj) -> int {
-      const int key = k_begin + jj * kBN + k;
-      if (jj >= n_tiles || key >= k_end) return -1;
-      const int col = key / p.block_size;
-      if (col >= p.max_blocks) return -1;
-      const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
+      if (k_begin + jj * kBN + k >= k_end || col_t >= p.max_blocks) return -1;
+      const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col_t);
       return (blk < 0 || (int64_t)blk >= p.num_blocks) ? -1 : blk;
     };
-    // the key's K and V scales in tile jj (0 for a dead key: its K and V rows are zero)
-    auto key_scales = [&](int jj, int blk, float& ks, float& vs) {
+    // the key's K and V scales in a tile with block id blk and slot slot (0 for a dead key: its K
+    // and V rows are zero)
+    auto key_scales = [&](int blk, int slot, float& ks, float& vs) {
       ks = vs = 0.0f;
       if (blk >= 0) {
-        const int64_t off = (int64_t)blk * p.scale_stride_blk +
-                            (int64_t)((k_begin + jj * kBN + k) % p.block_size) * p.scale_stride_tok + kvh;
+        const int64_t off = (int64_t)blk * p.scale_stride_blk + (int64_t)slot * p.scale_stride_tok + kvh;
         ks = __ldg(p.k_scale + off);
         vs = __ldg(p.v_scale + off);
       }
     };
-    // scales of tiles j and j+1, block id of tile j+2 (e4m3: per-tensor scales on scores and output)
+    // scales of tiles j and j+1, block id and slot of tile j+2 (e4m3: per-tensor scales on scores
+    // and output)
     float ks_cur = 0.0f, vs_cur = 1.0f, ks_1 = 0.0f, vs_1 = 1.0f;
-    int blk_2 = -1;
+    int blk_2 = -1, slot_2 = 0;
     if (!kFp8) {
-      key_scales(0, key_block(0), ks_cur, vs_cur);
-      key_scales(1, key_block(1), ks_1, vs_1);
+      key_scales(key_block(0), slot_t, ks_cur, vs_cur);
+      advance();
+      key_scales(key_block(1), slot_t, ks_1, vs_1);
+      advance();
       blk_2 = key_block(2);
+      slot_2 = slot_t;
     }
     float l_part[16];
 #pragma unroll
@@ -465,10 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       // tile j+2's scales and tile j+3's block id are fetched while this tile is scored
       float ks_2 = 0.0f, vs_2 = 1.0f;
       if (!kFp8) {
-        key_scales(j + 2, blk_2, ks_2, vs_2);
+        key_scales(blk_2, slot_2, ks_2, vs_2);
+        advance();
         blk_2 = key_block(j + 3);
+        slot_2 = slot_t;
       }
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full[st], (j >> 1) & 1, abort));
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.s_full[st], (j >> 1) & 1, abort));
       float s[16];
       {
         uint32_t v[16];
@@ -517,9 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const bool any_rescale = __any_sync(0xffffffffu, rescale);  // the same in all four warps
       // P^T buffer j%2 was last read by PV_{j-2}; O^T may be rescaled only once PV_{j-1} is done
       if (!dead && j >= 2)
-        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
+        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
       if (!dead && any_rescale && j >= 1)
-        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
+        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
       // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
       // the running column sums and the fp16 P^T stores run as independent batches
       float e[16];
@@ -567,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       vs_1 = vs_2;
     }
     // epilogue: column sums, O^T / l, log-sum-exp (each group for its 16 columns)
-    bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
+    bool fin = !dead && !*abort && mbar_wait_suspend(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
