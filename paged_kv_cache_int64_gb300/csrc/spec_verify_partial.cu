@@ -29,14 +29,15 @@
 //              subtraction of 1152 gives b exactly - the int8->fp16 method of Kim et al. 2022,
 //              "Who Says Elephants Can't Run"); e4m3 -> fp16 by the hardware conversion (exact;
 //              the per-tensor scales multiply the scores and the output).
-//   warps 4-7, 16-19 softmax, two warpgroups of 16 query columns each: thread k owns key k's 16
-//              scores of its group (TMEM lane k of S^T) and reads the key's K and V scales from the
-//              scale pools itself, a tile ahead; scores scaled by the K scale; column maxima by a
-//              shuffle reduce-scatter per warp and shared memory across the group's four warps,
-//              after which lane l keeps column (l & 15)'s running max (moved only when it grows by
-//              more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale in fp16 into one of
-//              two buffers, so the softmax waits for the PV two tiles back (and for the last one
-//              only to rescale O^T); at the end, column sums, normalised partial O and its LSE.
+//   warps 4-7, 16-19, 24-27, 28-31 softmax, four warpgroups of 8 query columns each: thread k owns
+//              key k's 8 scores of its group (TMEM lane k of S^T) and reads the key's K and V
+//              scales from the scale pools itself, two tiles ahead; scores scaled by the K scale;
+//              column maxima by a shuffle reduce-scatter per warp and shared memory across the
+//              group's four warps, after which lane l keeps column (l & 7)'s running max (moved
+//              only when it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale
+//              in fp16 into one of two buffers, so the softmax waits for the PV two tiles back (and
+//              for the last one only to rescale O^T); at the end, column sums, normalised partial O
+//              and its LSE.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -50,7 +51,8 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
 constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 768;
+constexpr int kThreads = 1024;
+constexpr int kGC = 8;                // query columns per softmax warpgroup (4 groups)
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
@@ -87,7 +89,7 @@ struct alignas(16) Barriers {
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
-  float red[2][2][4][16];  // [tile parity][softmax group][warp][column]: maxima, then the final sums
+  float red[2][kNQ / kGC][4][kGC];  // [tile parity][softmax group][warp][column]: maxima, then the final sums
   float inv_l[kNQ];      // epilogue: 1 / column sum
 };
 
@@ -154,6 +156,27 @@ __device__ __forceinline__ void widen16(uint4 in, uint32_t (&o)[8]) {
 // Reduce-scatter of 16 columns: on entry every lane holds 16 column values; on exit every lane holds
 // the warp maximum (kMax) or sum of column (lane & 15). 16 shuffles.
 template <bool kMax>
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float keep = upper ? v[q + o] : v[q];
+      const float send = upper ? v[q] : v[q + o];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[q] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (int o = 8; o <= 16; o <<= 1) {
+    const float other = __shfl_xor_sync(0xffffffffu, x, o);
+    x = kMax ? fmaxf(x, other) : x + other;
+  }
+  return x;
+}
+template <bool kMax>
 __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 #pragma unroll
   for (int o = 8; o >= 1; o >>= 1) {
@@ -215,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_init(&bar.v_ready[h], 128);
       mbar_init(&bar.v_free[h], 1);
     }
-    mbar_init(&bar.p_full[0], 256);
-    mbar_init(&bar.p_full[1], 256);
+    mbar_init(&bar.p_full[0], (kNQ / kGC) * 128);  // every softmax thread of the four groups
+    mbar_init(&bar.p_full[1], (kNQ / kGC) * 128);
     mbar_init(&bar.pv_done[0], 1);
     mbar_init(&bar.pv_done[1], 1);
     bar.abort = 0;
@@ -377,13 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_arrive(&bar.k_ready[st]);
       mbar_arrive(&bar.kst_free[st]);
     }
-  } else if ((warp >= 12 && warp < 16) || warp >= 20) {
+  } else if ((warp >= 12 && warp < 16) || (warp >= 20 && warp < 24)) {
     // ---------------------------------------------------------------------------- V converter
     // two warpgroups, one per half of head_dim (warps 12-15: 0-127, warps 20-23: 128-255), each with
     // its own ready / free barriers, so half 0 of V_{j+1} is widened while PV_j still reads half 1.
     // Thread k owns key row k: its half V row -> fp16 into the MN-major V tile (zeros outside the
     // split or in a bad block: the codes are zeroed before widening, which maps 0 to 0).
-    const int hv = warp >= 20 ? 1 : 0;
+    const int hv = warp >= 20 ? 1 : 0;  // warps 20-23: the second half
     const int k = (warp & 3) * 32 + lane;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
@@ -411,16 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------------------- softmax
-    // two warpgroups (warps 4-7: query columns 0-15, warps 16-19: columns 16-31); thread k holds
-    // key k's 16 scores of its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter
-    // leaves column (lane & 15)'s warp maximum in the lane, shared memory combines the four warps;
-    // lane l then keeps column (l & 15)'s running max (the same in all four warps) and hands it to
-    // the other lanes by shuffles. The K scale folds into the scores, the V scale into P^T; each
+    // four warpgroups of kGC = 8 query columns (warps 4-7, 16-19, 24-27, 28-31); thread k holds key
+    // k's 8 scores of its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter leaves
+    // column (lane & 7)'s warp maximum in the lane, shared memory combines the four warps; lane l
+    // then keeps column (l & 7)'s running max (the same in all four warps) and hands it to the
+    // other lanes by shuffles. The K scale folds into the scores, the V scale into P^T; each
     // thread reads its key's two scales from the cache itself, two tiles ahead (the block id three
     // tiles ahead), so no stage buffer waits for the softmax and the HBM latency is covered.
-    const int grp = warp >= 16 ? 1 : 0;
-    const int c0 = 16 * grp;       // the group's first query column
-    const int cl = lane & 15;      // this lane keeps the running max of column c0 + cl
+    const int grp = warp < 8 ? 0 : warp < 20 ? 1 : warp < 28 ? 2 : 3;
+    const int c0 = kGC * grp;      // the group's first query column
+    const int cl = lane & (kGC - 1);  // this lane keeps the running max of column c0 + cl
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -466,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       blk_2 = key_block(2);
       slot_2 = slot_t;
     }
-    float l_part[16];
+    float l_part[kGC];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) l_part[q] = 0.0f;
+    for (int q = 0; q < kGC; ++q) l_part[q] = 0.0f;
     float m_col = -INFINITY;
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
@@ -485,23 +508,23 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         slot_2 = slot_t;
       }
       if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.s_full[st], (j >> 1) & 1, abort));
-      float s[16];
+      float s[kGC];
       {
-        uint32_t v[16];
+        uint32_t v[kGC];
         const float ks = kFp8 ? k_descale : ks_cur;
         if (!dead) {
           tc_fence_after();
-          tmem_ld_32x32b_x16(tmem + lane_off + col_s(st) + c0, v);
+          tmem_ld_32x32b_x8(tmem + lane_off + col_s(st) + c0, v);
           tmem_wait_ld();
         }
         const float f = p.scale_log2 * ks;
         if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
+          for (int q = 0; q < kGC; ++q)
             s[q] = (!dead && in_range && c0 + q < nq) ? __uint_as_float(v[q]) * f : -INFINITY;
         } else {  // causal limit of column c (token t_base + c / group): key <= prefix + that token
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
+          for (int q = 0; q < kGC; ++q) {
             const int c = c0 + q;
             const bool vis = !dead && in_range && c < nq && key <= prefix + t_base + c / p.group;
             s[q] = vis ? __uint_as_float(v[q]) * f : -INFINITY;
@@ -509,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         }
       }
       {
-        float t[16];
+        float t[kGC];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) t[q] = s[q];
-        const float mine = reduce_scatter16<true>(t, lane);
-        if (lane < 16) bar.red[st][grp][quarter][lane] = mine;
+        for (int q = 0; q < kGC; ++q) t[q] = s[q];
+        const float mine = reduce_scatter8<true>(t, lane);
+        if (lane < kGC) bar.red[st][grp][quarter][lane] = mine;
       }
       named_bar_sync(1 + grp, 128);
       // column c0 + cl: tile maximum, running maximum and rescale factor
@@ -538,24 +561,24 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
       // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
       // the running column sums and the fp16 P^T stores run as independent batches
-      float e[16];
+      float e[kGC];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
+      for (int q = 0; q < kGC; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) e[q] = ex2_approx(s[q] - e[q]);
+      for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - e[q]);
       if (any_rescale) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
+        for (int q = 0; q < kGC; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
       } else {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) l_part[q] += e[q];
+        for (int q = 0; q < kGC; ++q) l_part[q] += e[q];
       }
-      if (!dead) {  // P^T column for key k (rows c0..c0+15 of buffer j % 2): p * v_scale, fp16
+      if (!dead) {  // P^T column for key k (rows c0..c0+7 of buffer j % 2): p * v_scale, fp16
         const float vs = vs_cur;
         uint8_t* pt = sP + (j & 1) * 2 * kPChunk + (k >> 6) * kPChunk + c0 * 128 + (k & 7) * 2;
         const uint32_t kc = (uint32_t)(k & 63) >> 3;
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
+        for (int q = 0; q < kGC; ++q)
           *reinterpret_cast<__half*>(pt + q * 128 + ((kc ^ (uint32_t)(q & 7)) * 16)) = __float2half_rn(e[q] * vs);
       }
       if (!dead) {
@@ -563,13 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         if (any_rescale) {  // O^T lane k (head_dim index) times column c0 + q's factor
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
+            uint32_t v[kGC];
+            tmem_ld_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < kGC; ++q)
               v[q] = __float_as_uint(__uint_as_float(v[q]) * __shfl_sync(0xffffffffu, alpha, q));
-            tmem_st_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
+            tmem_st_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
           }
           tmem_wait_st();
         }
@@ -587,11 +610,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
-      const float sum = reduce_scatter16<false>(l_part, lane);
-      if (lane < 16) bar.red[0][grp][quarter][lane] = sum;
+      const float sum = reduce_scatter8<false>(l_part, lane);
+      if (lane < kGC) bar.red[0][grp][quarter][lane] = sum;
     }
     named_bar_sync(1 + grp, 128);
-    if (quarter == 0 && lane < 16) {  // lane q: column c0 + q's sum, 1 / l and log-sum-exp
+    if (quarter == 0 && lane < kGC) {  // lane q: column c0 + q's sum, 1 / l and log-sum-exp
       const int c = c0 + lane;
       const float l = bar.red[0][grp][0][lane] + bar.red[0][grp][1][lane] + bar.red[0][grp][2][lane] +
                       bar.red[0][grp][3][lane];
@@ -608,12 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       tc_fence_after();
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + kColO + hh * 32 + c0, v);
+        uint32_t v[kGC];
+        tmem_ld_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
         tmem_wait_ld();
         const int d = hh * 128 + k;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kGC; ++q) {
           const int c = c0 + q;
           if (c >= nq) break;
           const int t = t_base + c / p.group, h2 = c % p.group;
