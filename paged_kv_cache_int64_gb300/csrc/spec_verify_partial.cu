@@ -15,10 +15,11 @@
 //              (warp 0) and of V (warp 3) through 4-D maps over the paged pool (block id as a
 //              coordinate), each into its own two-stage ring: 2 copies for a tile inside one
 //              block, per-segment copies (gcd(block_size, 128) keys) across blocks.
-//   warp 1     MMA issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
-//              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory),
-//              then O^T += V^T P^T (two M=128 halves of head_dim, N=32, K=128 keys; V MN-major fp16
-//              and P^T fp16 in shared memory).
+//   warp 1     QK issuer: S^T = K Q^T (tcgen05.mma kind::f16, M=128 keys, N=32, K=256; K read
+//              from tensor memory, Q fp16 in shared memory; S^T double-buffered in tensor memory).
+//   warp 2     (after allocating tensor memory) PV issuer: O^T += V^T P^T (two M=128 halves of
+//              head_dim, N=32, K=128 keys; V MN-major fp16 and P^T fp16 in shared memory). Two
+//              issuing threads, because a tile's 32 small MMAs take longer to issue than to run.
 //   warps 8-11 K converter: thread k owns key row k and widens it into the tile's tensor-memory K
 //              buffer (two buffers, so tile j+1 is widened while tile j is scored), then releases
 //              the K stage.
@@ -82,6 +83,7 @@ struct alignas(16) Barriers {
   uint64_t v_ready[2];                // half h (head_dim 128h..128h+127) of V_j widened into shared memory
   uint64_t v_free[2];                 // half h of the V tile read by PV_j
   uint64_t s_full[2];                 // S^T_j in TMEM buffer j%2
+  uint64_t s_free[2];                 // S^T_j read by every softmax thread: QK_{j+2} may overwrite it
   uint64_t p_full[2];                 // P^T_j (buffer j%2) written, O^T rescaled; per tile parity,
                                       // since the softmax may run a tile ahead of the MMA's wait
   uint64_t pv_done[2];                // PV_j complete (V tile and P^T buffer j%2 free, O^T current),
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_init(&bar.k_ready[s], 128);
       mbar_init(&bar.k_free[s], 1);
       mbar_init(&bar.s_full[s], 1);
+      mbar_init(&bar.s_free[s], (kNQ / kGC) * 128);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&bar.v_ready[h], 128);
@@ -310,29 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------------------- QK issuer
+    // S^T_j = K_j Q^T into TMEM buffer j%2, once K_j is in TMEM and every softmax thread has read
+    // S^T_{j-2} out of that buffer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_f16(128, kNQ, false, false, false);
-      constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
-      const uint32_t q_base = smem_u32(sQ), v_base = smem_u32(sV16), p_base = smem_u32(sP);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
-        const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
-        for (int hh = 0; hh < 2; ++hh) {  // each half of head_dim as soon as its V half is widened
-          if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort)) return false;
-          tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
-                        smem_desc(pb + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
-                        (i > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&bar.v_free[hh]);
-        }
-        umma_commit(&bar.pv_done[i & 1]);
-        return true;
-      };
+      const uint32_t q_base = smem_u32(sQ);
       bool ok = mbar_wait_suspend(&bar.q_ready, 0, abort);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
+        if (j >= 2 && !mbar_wait_suspend(&bar.s_free[st], ((j - 2) >> 1) & 1, abort)) break;
         if (!mbar_wait_suspend(&bar.k_ready[st], (j >> 1) & 1, abort)) break;
         tc_fence_after();
         for (int ks = 0; ks < 16; ++ks)
@@ -340,9 +330,35 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
                       smem_desc(q_base + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
         umma_commit(&bar.s_full[st]);
         umma_commit(&bar.k_free[st]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
-      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------------------- PV issuer
+    // O^T += V_j^T P^T_j, each head_dim half as soon as its V half is widened; a second issuing
+    // thread, so the 16 QK and 16 PV MMAs of a tile are issued side by side
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
+      const uint32_t v_base = smem_u32(sV16), p_base = smem_u32(sP);
+      for (int i = 0; i < n_tiles; ++i) {
+        if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort)) break;
+        const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
+        bool ok = true;
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
+                        smem_desc(pb + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
+                        (i > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&bar.v_free[hh]);
+        }
+        if (!ok) break;
+        umma_commit(&bar.pv_done[i & 1]);
+      }
     }
     __syncwarp();
   } else if (warp >= 8 && warp < 12) {
@@ -516,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           tc_fence_after();
           tmem_ld_32x32b_x8(tmem + lane_off + col_s(st) + c0, v);
           tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar.s_free[st]);  // QK_{j+2} may now overwrite this S^T buffer
         }
         const float f = p.scale_log2 * ks;
         if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
