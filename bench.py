@@ -522,6 +522,7 @@ def run_verify_batch(torch, pkv, dev, flush, args):
                 "partial_gbs": round(gp, 1), "combine_ms": round(statistics.mean(tc), 4), "split_tokens": split}
 
     res = measure(device_q(p), p.seq_lens, T_VERIFY, HQ)
+    res["partial_dram_bytes"] = load_traffic("verify_partial")  # ncu capture of this batch's partial launch
     # decode: the first token of each request's verify window, alone
     dec_lens = p.seq_lens - (T_VERIFY - 1)
     res["decode_t1"] = measure(u16_to_bf16(W.bf16_normal(7, (p.num_reqs, HQ, D))).to(dev), dec_lens, 1, HQ)
