@@ -674,8 +674,11 @@ def run_ncu_case(args):
         kd = torch.empty((1, L, HKV, D), dtype=torch.bfloat16, device=dev)
         vd = torch.empty_like(kd)
         sc = torch.tensor([0.5], dtype=torch.float32, device=dev)
+        ws = torch.empty(pkv.paged_prefill_workspace_bytes(), dtype=torch.uint8, device=dev)
         fns = {
             "prefill_bf16": lambda: pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, CHUNK, p.softmax_scale, out),
+            "prefill_bf16_persistent": lambda: pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, CHUNK, p.softmax_scale,
+                                                                      out, workspace=ws),
             "prefill_int8": lambda: pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, CHUNK, p.softmax_scale, out,
                                                            qk_mode=pkv.PKV_QK_INT8, k8_scale=k8s, k16=k16),
             "int8_quant": lambda: pkv.kv_int8_stats_quant(k, bt, pb, sl, CHUNK, k8, k8s, k16=k16),
@@ -697,7 +700,8 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=0, help="query tokens per prefill pass (0: one per core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-batch", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill_bf16", "prefill_int8", "int8_quant", "fp8_dequant", "verify"],
+    ap.add_argument("--ncu-case", choices=["prefill_bf16", "prefill_bf16_persistent", "prefill_int8", "int8_quant",
+                                           "fp8_dequant", "verify"],
                     help="run one kernel on a small case for profiler capture instead of the bench")
     args = ap.parse_args()
     if args.ncu_case:

@@ -81,7 +81,7 @@ typedef enum pkv_kv_dtype {
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version of this header (incremented on any signature change). */
-#define PKV_ABI_VERSION 4
+#define PKV_ABI_VERSION 5
 PKV_API int32_t pkv_abi_version(void);
 
 /*
@@ -152,6 +152,14 @@ PKV_API pkv_status pkv_kv_fp8_dequant_dense(const uint8_t* k_fp8, const uint8_t*
  * writes on request) is given it is read instead of k8 (same result, faster); k8 may then be NULL.
  * PKV_QK_BF16 ignores k8, k8_scale, k16 and max_ctx.
  * max_q_len: host upper bound on any request's q_len. total_q: host, = query_start_loc[num_reqs].
+ * workspace (nullable, caller-owned device memory, 16-byte aligned, workspace_bytes long): NULL
+ *   launches one CTA per (128-row query tile, head, request). Given, the call launches a
+ *   persistent grid of P = min(SM count, workspace_bytes / pkv_paged_prefill_workspace_bytes(1),
+ *   1024) CTAs: the query tiles in full waves of P, then the tiles of the last partial wave cut
+ *   into up to 4 equal key ranges so that every CTA has work, plus a merge kernel for the cut
+ *   tiles. Uncut tiles give the same bytes as the NULL launch; the rows of cut tiles are merged in
+ *   fp32 and rounded to bf16 once. Size it with pkv_paged_prefill_workspace_bytes(SM count); its
+ *   contents are scratch, overwritten per call.
  * Requirements: head_dim == 256; block_size a multiple of 8; q, caches and strides 16-byte
  * aligned; num_q_heads a multiple of num_kv_heads.
  */
@@ -163,8 +171,15 @@ PKV_API pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache, co
                                   int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t block_size, float softmax_scale,
                                   int32_t qk_mode, const int8_t* k8, const float* k8_scale,
-                                  const void* k16, int64_t max_ctx, void* out, int32_t* dev_err,
-                                  void* stream);
+                                  const void* k16, int64_t max_ctx, void* out, void* workspace,
+                                  int64_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * paged_prefill_workspace_bytes - bytes of the persistent prefill workspace for num_ctas CTAs
+ * (four slots per CTA of 128 x 256 fp32 partial outputs and 128 fp32 log-sum-exps: 526,336 bytes
+ * per CTA); 0 for num_ctas <= 0. Pass the device's SM count for a full persistent grid.
+ */
+PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t num_ctas);
 
 /*
  * spec_verify_attn_partial - speculative-decode verify attention over an int8 per-token-head
@@ -284,7 +299,8 @@ PKV_API pkv_status pkv_kv_cache_write(const void* k_new, const void* v_new, int6
  * k_fp8 / v_fp8: uint8 e4m3 pools [num_blocks][block_size][num_kv_heads][head_dim] with element
  * strides (16-byte aligned); k_scale / v_scale: device pointers to one fp32 each. Keys past
  * seq_len or in a block whose id is out of range read as zero (PKV_ERR_DEVICE_BOUNDS for the
- * latter). Requirements as pkv_paged_prefill_attn (head_dim == 256).
+ * latter). workspace / workspace_bytes: as pkv_paged_prefill_attn (NULL: one CTA per query tile;
+ * given: the persistent grid). Requirements as pkv_paged_prefill_attn (head_dim == 256).
  */
 PKV_API pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
                                               const float* k_scale, const float* v_scale, int64_t num_blocks,
@@ -294,7 +310,8 @@ PKV_API pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp
                                               int32_t num_reqs, int32_t total_q, int32_t max_q_len,
                                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                               int32_t block_size, float softmax_scale, void* out,
-                                              int32_t* dev_err, void* stream);
+                                              void* workspace, int64_t workspace_bytes, int32_t* dev_err,
+                                              void* stream);
 
 /*
  * spec_verify_attn_noalloc - pkv_spec_verify_attn_partial followed by pkv_spec_verify_combine, with

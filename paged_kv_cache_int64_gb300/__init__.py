@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA", "PKV_ERR_DEVICE_BOUNDS",
     "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PKV_KV_BF16", "PKV_KV_INT8", "PKV_KV_FP8", "PkvError", "lib",
-    "library_path", "kv_cache_write", "kv_int8_stats_quant", "paged_prefill_attn_fp8", "kv_fp8_dequant_dense", "paged_prefill_attn", "spec_verify_workspace_bytes",
+    "library_path", "kv_cache_write", "kv_int8_stats_quant", "paged_prefill_attn_fp8", "kv_fp8_dequant_dense", "paged_prefill_attn", "paged_prefill_workspace_bytes", "spec_verify_workspace_bytes",
     "spec_verify_attn_partial", "spec_verify_attn_partial_fp8", "spec_verify_combine", "EXPORTED_SYMBOLS",
 ]
 
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
     "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
     "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write", "pkv_paged_prefill_attn_fp8",
+    "pkv_paged_prefill_workspace_bytes",
 )
 
 library_path = _build.LIB
@@ -56,7 +57,9 @@ def _load():
     L.pkv_kv_fp8_dequant_dense.argtypes = [vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, i32, i32, i32, i32, i32,
                                            vp, vp, vp, vp, vp, vp]
     L.pkv_paged_prefill_attn.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32, i32, i32,
-                                         i32, i32, i32, f32, i32, vp, vp, vp, i64, vp, vp, vp]
+                                         i32, i32, i32, f32, i32, vp, vp, vp, i64, vp, vp, i64, vp, vp]
+    L.pkv_paged_prefill_workspace_bytes.argtypes = [i32]
+    L.pkv_paged_prefill_workspace_bytes.restype = sz
     L.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.pkv_spec_verify_workspace_bytes.restype = sz
     L.pkv_spec_verify_attn_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
@@ -72,7 +75,7 @@ def _load():
     L.pkv_kv_cache_write.argtypes = [vp, vp, i64, vp, i64, i32, vp, vp, i32, i32, i32, vp, vp, i64, i64, i64, i64,
                                      vp, vp, i64, i64, vp, vp, i32, i32, i32, vp, vp]
     L.pkv_paged_prefill_attn_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32,
-                                             i32, i32, i32, i32, i32, f32, vp, vp, vp]
+                                             i32, i32, i32, i32, i32, f32, vp, vp, i64, vp, vp]
     for name in ("pkv_paged_prefill_attn_fp8", "pkv_kv_cache_write", "pkv_kv_int8_stats_quant", "pkv_kv_fp8_dequant_dense", "pkv_paged_prefill_attn",
                  "pkv_spec_verify_attn_partial", "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8"):
         getattr(L, name).restype = i32
@@ -102,6 +105,13 @@ def _cache_strides(cache: torch.Tensor):
     assert cache.dim() == 4 and cache.stride(3) == 1, "cache must be [nb][bs][hkv][D] with contiguous D"
     nb, bs, hkv, d = cache.shape
     return nb, bs, hkv, d, cache.stride(0), cache.stride(1), cache.stride(2)
+
+
+def _ws_bytes(ws):
+    if ws is None:
+        return 0
+    assert ws.is_cuda and ws.is_contiguous(), "workspace must be a contiguous CUDA tensor"
+    return ws.numel() * ws.element_size()
 
 
 def _i32(t):
@@ -169,10 +179,12 @@ def kv_fp8_dequant_dense(k_fp8, v_fp8, block_table, seq_lens, k_scale, v_scale, 
 
 
 def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_q_len, softmax_scale,
-                       out, qk_mode=PKV_QK_BF16, k8=None, k8_scale=None, dev_err=None, stream=None, k16=None):
+                       out, qk_mode=PKV_QK_BF16, k8=None, k8_scale=None, dev_err=None, stream=None, k16=None,
+                       workspace=None):
     """Chunked causal prefill attention. q/out bf16 [total_q][Hq][D]; caches bf16 [nb][bs][hkv][D]
     (k_cache may be None in int8 mode, which reads k8 (or its fp16 copy k16) and k8_scale from
-    kv_int8_stats_quant)."""
+    kv_int8_stats_quant). workspace: None (one CTA per query tile) or a CUDA byte tensor of
+    paged_prefill_workspace_bytes() bytes (persistent grid: full waves, last wave cut into key ranges)."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(v_cache)
     if k_cache is not None:
         assert k_cache.stride() == v_cache.stride() and k_cache.shape == v_cache.shape
@@ -184,11 +196,12 @@ def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_l
                                       block_table.stride(0), block_table.shape[1], _ptr(_i32(seq_lens)),
                                       _ptr(_i32(query_start_loc)), R, q.shape[0], int(max_q_len), q.shape[1],
                                       hkv, d, bs, float(softmax_scale), int(qk_mode), _ptr(k8), _ptr(k8_scale),
-                                      _ptr(k16), max_ctx, _ptr(out), _ptr(dev_err), _stream(stream)))
+                                      _ptr(k16), max_ctx, _ptr(out), _ptr(workspace), _ws_bytes(workspace),
+                                      _ptr(dev_err), _stream(stream)))
 
 
 def paged_prefill_attn_fp8(q, k_fp8, v_fp8, k_scale, v_scale, block_table, seq_lens, query_start_loc, max_q_len,
-                           softmax_scale, out, dev_err=None, stream=None):
+                           softmax_scale, out, dev_err=None, stream=None, workspace=None):
     """Chunked causal prefill attention read straight from per-tensor e4m3 paged K/V (uint8
     [nb][bs][hkv][D]) with device scalar scales; each tile is dequantized in shared memory."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_fp8)
@@ -201,7 +214,15 @@ def paged_prefill_attn_fp8(q, k_fp8, v_fp8, k_scale, v_scale, block_table, seq_l
                                           sh, _ptr(block_table), block_table.stride(0), block_table.shape[1],
                                           _ptr(_i32(seq_lens)), _ptr(_i32(query_start_loc)), R, q.shape[0],
                                           int(max_q_len), q.shape[1], hkv, d, bs, float(softmax_scale), _ptr(out),
-                                          _ptr(dev_err), _stream(stream)))
+                                          _ptr(workspace), _ws_bytes(workspace), _ptr(dev_err), _stream(stream)))
+
+
+def paged_prefill_workspace_bytes(num_ctas=None) -> int:
+    """bytes of the persistent prefill workspace for num_ctas CTAs (default: the current device's SM
+    count, the persistent grid's size)."""
+    if num_ctas is None:
+        num_ctas = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(lib.pkv_paged_prefill_workspace_bytes(int(num_ctas)))
 
 
 def spec_verify_workspace_bytes(num_tokens, num_q_heads, head_dim, max_splits) -> int:

@@ -32,8 +32,24 @@
 // Rows of the last tile past seq_len (and of any out-of-range block) are zero-filled in shared
 // memory before the MMAs read them, so stale or NaN pool bytes never reach P.V. Every wait is
 // bounded: on expiry the CTA records PKV_ERR_TIMEOUT, drains and exits.
+//
+// Launches. Classic (no workspace): one CTA per (m-tile, head, request); the CTAs of one chunk all
+// but tie in work, so 256 of them on 152 SMs leave the second wave 68% full. Persistent (a
+// workspace given): one CTA per SM walks a static schedule of segments - whole units (request,
+// m-tile, head) in full waves, then the units of the last partial wave cut into k equal key ranges
+// so that their pieces fill every SM (SegIter). Both keep the CTAs sweeping the same keys at the
+// same time, which is what lets 152 CTAs share every K/V tile through L2 (a stream-K split into
+// equal contiguous shares starts each CTA at a different key offset, and measured slower for that
+// reason). A piece writes the fp32 O / l of its keys and the rows' log-sum-exp to the workspace;
+// prefill_combine_kernel merges the pieces into the bf16 rows. Every role walks the same
+// segments; barrier phases follow the CTA's running tile count, positions and masks the tile index
+// within the unit. Between segments, Q is reloaded once the last QK has read it (q_empty) and the
+// first PV of the next unit overwrites O once the epilogue has read it (o_free).
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "host_common.h"
 #include "sm103.cuh"
@@ -61,8 +77,10 @@ constexpr int kOffV = kOffK + kTileBytes;
 constexpr int kTilesEnd = kOffV + kTileBytes;
 
 struct Barriers {
-  uint64_t q_full;      // TMA Q landed
+  uint64_t q_full;      // TMA Q landed (phase = segment parity)
   uint64_t q_ready;     // int8: Q quantized in place
+  uint64_t q_empty;     // the segment's last QK has read Q: the next segment's Q may land
+  uint64_t o_free;      // the segment's epilogue has read O (256 softmax arrivals)
   uint64_t k_full[4];   // chunk c of K tile j ready (TMA bytes, or converter arrivals)
   uint64_t k_empty[4];  // chunk c of K tile j consumed by the QK MMAs
   uint64_t v_full;      // V tile j ready
@@ -78,8 +96,16 @@ struct Barriers {
   int abort;
   float kscale[2][kBN];  // int8: per-key scales of the tile
   float qscale[kBM];     // int8: per-row q scales
-  float rowmax[2][2][kBM];  // per tile parity, per half: row maxima (and the final row sums)
+  float rowmax[2][2][kBM];  // per tile parity, per half: row maxima
+  float lsum[2][kBM];       // per half: the segment's row sums (epilogue)
 };
+
+// workspace of the persistent launch: kMaxSplit slots per CTA (the pieces of the units cut in key
+// ranges, fewer than P units of at most kMaxSplit pieces), each the normalised fp32 O [128 rows][256]
+// followed by the rows' natural-log LSE [128]
+constexpr int kMaxSplit = 4;
+constexpr int64_t kSlotFloats = (int64_t)kBM * kD + kBM;
+constexpr int64_t kCtaWsBytes = kMaxSplit * kSlotFloats * 4;
 
 struct Params {
   CUtensorMap qmap;   // bf16 q: dims {D, Hq, total_q}, box {64, 1, 128}
@@ -111,6 +137,11 @@ struct Params {
   int64_t stride_blk, stride_tok, stride_head;
   const float* k_scale;
   const float* v_scale;
+  // persistent launch: num_ctas CTAs walk the schedule of whole units and key-range pieces
+  int32_t persistent;
+  int32_t num_reqs;
+  int32_t num_ctas;  // the persistent grid
+  float* ws;         // [num_ctas * kMaxSplit][kSlotFloats]
 };
 
 // kMode 0: exact QK (bf16 K from the pool); 1: int8 QK with K widened from the int8 scratch by
@@ -203,6 +234,150 @@ __device__ __forceinline__ void zero_rows(uint8_t* tile, int n_valid, uint32_t b
   }
 }
 
+// A unit of work: 128 query rows (m-tile mt) of query head qh of request r.
+struct Unit {
+  int r, qh, mt, kvh, seq_len, rows_valid, p0, n_tiles, tok0;
+};
+
+// Fills u for (r, mt, qh); false when the m-tile holds no query rows.
+__device__ __forceinline__ bool make_unit(const Params& p, int r, int mt, int qh, Unit& u) {
+  const int q0 = __ldg(p.qsl + r);
+  const int q_len = __ldg(p.qsl + r + 1) - q0;
+  const int seq_len = __ldg(p.seq_lens + r);
+  if (mt * kBM >= q_len || q_len > seq_len) return false;
+  u.r = r;
+  u.qh = qh;
+  u.mt = mt;
+  u.kvh = qh / p.group;
+  u.seq_len = seq_len;
+  u.rows_valid = min(kBM, q_len - mt * kBM);
+  u.p0 = seq_len - q_len + mt * kBM;                      // position of row 0
+  const int kv_end = min(seq_len, u.p0 + u.rows_valid);  // keys [0, kv_end)
+  u.n_tiles = (kv_end + kBN - 1) / kBN;
+  u.tok0 = q0 + mt * kBM;
+  return true;
+}
+
+// key tiles of each unit of (request r, m-tile mt); 0 when the m-tile holds no rows
+__device__ __forceinline__ int unit_tiles(const Params& p, int r, int mt) {
+  Unit u;
+  return make_unit(p, r, mt, 0, u) ? u.n_tiles : 0;
+}
+
+// A segment: key tiles [t0, t1) of one unit, processed by this CTA.
+struct Seg {
+  Unit u;
+  int t0, t1;
+  bool whole;  // all of the unit's tiles: the CTA writes the final output rows
+  int slot;    // otherwise the workspace slot of the piece
+};
+
+// The persistent schedule. Units with rows - groups (m-tile, request) in the order m-tile
+// descending (heaviest first), then request, each group the num_q_heads units of its heads - are
+// numbered u = 0 .. U - 1. With P CTAs, the first F = P floor(U / P) units are whole: CTA c takes
+// units c, c + P, ... (full waves: every CTA sweeps its unit's keys from the first tile, in step
+// with the others, so the K/V tiles they share are read from L2). The R = U - F remaining units
+// (R < P) are each cut into k equal key ranges, k <= kMaxSplit chosen to fill the P CTAs: piece
+// pi = i R + j is range i of unit F + j, and goes to CTA P - 1 - (pi mod P) (the CTAs holding the
+// lightest whole units take the extra piece). Pieces in that order sweep the same key range at the
+// same time, again in step; their fp32 partials land in workspace slot pi.
+struct Schedule {
+  int U, f, R, k;
+};
+
+__device__ int count_groups(const Params& p) {
+  int n = 0;
+  for (int m = p.n_mtiles - 1; m >= 0; --m)
+    for (int r = 0; r < p.num_reqs; ++r) n += unit_tiles(p, r, m) > 0;
+  return n;
+}
+
+// k in [1, kMaxSplit] minimising the time of the cut units' pieces, ceil(R k / P) / k waves of
+// whole-unit time, plus 2% of a wave per extra piece (its epilogue, Q load and merge)
+__host__ __device__ inline int choose_split(int R, int P) {
+  int best = 1;
+  float best_cost = 2.0f;
+  for (int k = 1; k <= kMaxSplit && R > 0; ++k) {
+    const float cost = (float)((R * k + P - 1) / P) / (float)k + 0.02f * (float)(k - 1);
+    if (cost < best_cost - 1e-6f) {
+      best_cost = cost;
+      best = k;
+    }
+  }
+  return best;
+}
+
+__device__ Schedule make_schedule(const Params& p) {
+  Schedule sc;
+  const int P = p.num_ctas;
+  sc.U = count_groups(p) * p.num_q_heads;
+  sc.f = sc.U / P;
+  sc.R = sc.U - sc.f * P;
+  sc.k = choose_split(sc.R, P);
+  return sc;
+}
+
+// unit u of the persistent order
+__device__ void unit_at(const Params& p, int u, Unit& out) {
+  int g = u / p.num_q_heads;
+  const int qh = u - g * p.num_q_heads;
+  for (int m = p.n_mtiles - 1; m >= 0; --m)
+    for (int r = 0; r < p.num_reqs; ++r)
+      if (unit_tiles(p, r, m) > 0 && g-- == 0) {
+        make_unit(p, r, m, qh, out);
+        return;
+      }
+}
+
+// Walks this CTA's segments; every role walks the same sequence. Classic launch: one segment, the
+// unit of blockIdx (latest m-tiles first), whole. Persistent launch: its whole units, then its pieces.
+struct SegIter {
+  const Params& p;
+  Schedule sc{};
+  int count = 0;   // segments produced
+  int w = 0;       // whole units taken
+  int64_t pi = 0;  // next piece
+  __device__ explicit SegIter(const Params& pp) : p(pp) {
+    if (!p.persistent) return;
+    sc = make_schedule(p);
+    pi = p.num_ctas - 1 - (int)blockIdx.x;
+  }
+  __device__ bool next(Seg& s) {
+    if (!p.persistent) {
+      if (count++ > 0) return false;
+      if (!make_unit(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, s.u)) return false;
+      s.t0 = 0;
+      s.t1 = s.u.n_tiles;
+      s.whole = true;
+      s.slot = 0;
+      return s.u.n_tiles > 0;
+    }
+    const int P = p.num_ctas;
+    if (w < sc.f) {
+      unit_at(p, (int)blockIdx.x + P * w++, s.u);
+      s.t0 = 0;
+      s.t1 = s.u.n_tiles;
+      s.whole = true;
+      s.slot = 0;
+      ++count;
+      return true;
+    }
+    while (pi < (int64_t)sc.R * sc.k) {
+      const int j = (int)(pi % sc.R), i = (int)(pi / sc.R);
+      s.slot = (int)pi;
+      pi += P;
+      unit_at(p, sc.f * P + j, s.u);
+      s.t0 = s.u.n_tiles * i / sc.k;
+      s.t1 = s.u.n_tiles * (i + 1) / sc.k;
+      if (s.t0 == s.t1) continue;  // a unit of fewer than k tiles: this range is empty
+      s.whole = sc.k == 1;
+      ++count;
+      return true;
+    }
+    return false;
+  }
+};
+
 template <int kMode>
 __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     paged_prefill_attn_kernel(const __grid_constant__ Params p) {
@@ -218,23 +393,16 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int r = blockIdx.z;
-  const int qh = blockIdx.y;
-  const int mt = p.n_mtiles - 1 - (int)blockIdx.x;  // latest (heaviest) tiles first
-  const int kvh = qh / p.group;
-  const int q0 = __ldg(p.qsl + r);
-  const int q_len = __ldg(p.qsl + r + 1) - q0;
-  const int seq_len = __ldg(p.seq_lens + r);
-  if (mt * kBM >= q_len || q_len > seq_len) return;  // CTA-uniform
-  const int rows_valid = min(kBM, q_len - mt * kBM);
-  const int p0 = seq_len - q_len + mt * kBM;         // position of row 0
-  const int kv_end = min(seq_len, p0 + rows_valid);  // keys [0, kv_end)
-  const int n_tiles = (kv_end + kBN - 1) / kBN;
-  const int tok0 = q0 + mt * kBM;
+  if (!p.persistent) {  // classic launch: a CTA without rows leaves at once (CTA-uniform)
+    Unit u;
+    if (!make_unit(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, u)) return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
     mbar_init(&bar.q_ready, 128);
+    mbar_init(&bar.q_empty, 1);
+    mbar_init(&bar.o_free, 256);
     for (int c = 0; c < 4; ++c) {
       mbar_init(&bar.k_full[c], (kConv || kFused) ? 128 : 1);
       mbar_init(&bar.k_empty[c], 1);
@@ -259,171 +427,188 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
+  // Barrier phases follow g, the CTA's running tile count over all its segments, and s, its
+  // segment count; positions and masks follow the unit-local tile index j.
 
-  if (warp == 0 && kFused) {
-    // ---------------------------------------------------------------------------- producer (Q)
-    if (lane == 0) {
-      prefetch_tensormap(&p.qmap);
-      mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
-      for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
-    }
-  } else if (warp == 0) {
+  if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
     const int G = p.seg;
     const int nseg = kBN / G;
     const uint32_t seg_bytes = (uint32_t)G * 128u;  // one chunk of one segment
     if (lane == 0) {
       prefetch_tensormap(&p.qmap);
-      prefetch_tensormap(&p.vmap);
-      if (!kInt8) prefetch_tensormap(&p.kmap);
-      if (kMode == 2) prefetch_tensormap(&p.k16map);
-      if (p.big_ok) {
-        prefetch_tensormap(&p.vmap_big);
-        if (!kInt8) prefetch_tensormap(&p.kmap_big);
+      if (!kFused) {
+        prefetch_tensormap(&p.vmap);
+        if (!kInt8) prefetch_tensormap(&p.kmap);
+        if (kMode == 2) prefetch_tensormap(&p.k16map);
+        if (p.big_ok) {
+          prefetch_tensormap(&p.vmap_big);
+          if (!kInt8) prefetch_tensormap(&p.kmap_big);
+        }
       }
-      mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
-      for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, qh, tok0);
     }
-    // block id of segment `lane` of tile j: >= 0, -1 past seq_len, -2 out-of-range entry
-    auto lookup = [&](int j) -> int {
-      const int pos = j * kBN + lane * G;
-      if (lane >= nseg || pos >= seq_len) return -1;
-      const int col = pos / p.block_size;
-      if (col >= p.max_blocks) return -2;
-      const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
-      if (blk < 0 || (int64_t)blk >= p.num_blocks) return -2;
-      return blk;
-    };
-    auto issue_seg = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, int blk, int key0) {
-      const int slot = (key0 + lane * G) % p.block_size;
-      for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes + lane * G * 128, map, mb, c * 64, kvh, slot, blk);
-    };
-    struct TileInfo {
-      int blk;           // this lane's segment block id (>= 0), -1 past seq_len, -2 bad entry
-      uint32_t bad;      // segments with a bad table entry
-      uint32_t nloaded;  // segments with a valid block
-      bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
-      bool big;          // the 128 keys lie in one valid block: 4 copies of 128 rows per tensor
-      int blk0, slot0;   // block and first slot of key 0 of the tile
-    };
-    auto info = [&](int j) -> TileInfo {
-      TileInfo t;
-      t.blk = j < n_tiles ? lookup(j) : -1;
-      t.bad = __ballot_sync(0xffffffffu, t.blk == -2);
-      t.nloaded = __popc(__ballot_sync(0xffffffffu, t.blk >= 0));
-      t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
-      t.blk0 = __shfl_sync(0xffffffffu, t.blk, 0);
-      t.slot0 = (j * kBN) % p.block_size;
-      t.big = p.big_ok && t.bad == 0 && t.blk0 >= 0 && t.slot0 + kBN <= p.block_size;
-      return t;
-    };
-    // a whole tile of one tensor with 4 copies of [128 rows][64 x 16-bit] (lane 0)
-    auto issue_big = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, const TileInfo& t) {
-      if (lane == 0)
-        for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes, map, mb, c * 64, kvh, t.slot0, t.blk0);
-    };
+    SegIter it(p);
+    Seg sg;
+    int g = 0, s = 0;
     uint32_t fix_phase = 0;
-    // K tile j through k_full[c] (bf16) or the K8 stage (int8), chunk by chunk as QK_{j-1} frees it.
-    // K rows past seq_len need no zero-fill (their scores are masked); rows of a bad segment do,
-    // so such a tile goes through the private barrier, is patched, then published.
-    auto load_k = [&](int j, const TileInfo& t) {
-      const int key0 = j * kBN;
-      if (kConv) return;  // the converter warps read the int8 K rows themselves
-      if (kMode == 2) {   // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
-        if (lane == 0) {
-          const int row = (int)((int64_t)r * p.max_ctx + key0);
-          for (int c = 0; c < 4; ++c) {
-            if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
-            mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
-            tma_load_3d(sK + c * kChunkBytes, &p.k16map, &bar.k_full[c], c * 64, kvh, row);
-          }
+    while (!*abort && it.next(sg)) {
+      const Unit& u = sg.u;
+      const int r = u.r, kvh = u.kvh, seq_len = u.seq_len;
+      // Q of this segment's unit, once the previous segment's last QK has read the old one
+      if (lane == 0) {
+        if (s == 0 || mbar_wait(&bar.q_empty, (s - 1) & 1, abort)) {
+          mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
+          for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, u.qh, u.tok0);
         }
-        __syncwarp();
-        return;
       }
-      if (t.bad) {
-        if (lane == 0) {
-          for (int c = 0; c < 4 && j > 0; ++c)
-            if (!mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
-          if (!*abort) mbar_arrive_expect_tx(&bar.fix, 4u * t.nloaded * seg_bytes);
-        }
-        __syncwarp();
-        if (*abort) return;
-        if (t.blk >= 0) issue_seg(sK, &p.kmap, &bar.fix, t.blk, key0);
-        if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
-        ++fix_phase;
-        __syncwarp();
-        if (*abort) return;
-        zero_rows(sK, kBN, t.bad, G, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
+      __syncwarp();
+      if (*abort) break;
+      if (kFused) {  // K and V come from the converter warps
+        g += sg.t1 - sg.t0;
+        ++s;
+        continue;
+      }
+      // block id of segment `lane` of tile j: >= 0, -1 past seq_len, -2 out-of-range entry
+      auto lookup = [&](int j) -> int {
+        const int pos = j * kBN + lane * G;
+        if (lane >= nseg || pos >= seq_len) return -1;
+        const int col = pos / p.block_size;
+        if (col >= p.max_blocks) return -2;
+        const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) return -2;
+        return blk;
+      };
+      auto issue_seg = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, int blk, int key0) {
+        const int slot = (key0 + lane * G) % p.block_size;
+        for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes + lane * G * 128, map, mb, c * 64, kvh, slot, blk);
+      };
+      struct TileInfo {
+        int blk;           // this lane's segment block id (>= 0), -1 past seq_len, -2 bad entry
+        uint32_t bad;      // segments with a bad table entry
+        uint32_t nloaded;  // segments with a valid block
+        bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
+        bool big;          // the 128 keys lie in one valid block: 4 copies of 128 rows per tensor
+        int blk0, slot0;   // block and first slot of key 0 of the tile
+      };
+      auto info = [&](int j) -> TileInfo {
+        TileInfo t;
+        t.blk = j < sg.t1 ? lookup(j) : -1;
+        t.bad = __ballot_sync(0xffffffffu, t.blk == -2);
+        t.nloaded = __popc(__ballot_sync(0xffffffffu, t.blk >= 0));
+        t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
+        t.blk0 = __shfl_sync(0xffffffffu, t.blk, 0);
+        t.slot0 = (j * kBN) % p.block_size;
+        t.big = p.big_ok && t.bad == 0 && t.blk0 >= 0 && t.slot0 + kBN <= p.block_size;
+        return t;
+      };
+      // a whole tile of one tensor with 4 copies of [128 rows][64 x 16-bit] (lane 0)
+      auto issue_big = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* mb, const TileInfo& t) {
         if (lane == 0)
-          for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
-        __syncwarp();
-        return;
-      }
-      if (t.big) {
-        if (lane == 0) {
-          for (int c = 0; c < 4; ++c) {
-            if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) break;
-            mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
-            tma_load_4d(sK + c * kChunkBytes, &p.kmap_big, &bar.k_full[c], c * 64, kvh, t.slot0, t.blk0);
+          for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes, map, mb, c * 64, kvh, t.slot0, t.blk0);
+      };
+      // K tile j (CTA tile gk) chunk by chunk as QK_{gk-1} frees it. K rows past seq_len need no
+      // zero-fill (their scores are masked); rows of a bad segment do, so such a tile goes through
+      // the private barrier, is patched, then published.
+      auto load_k = [&](int j, int gk, const TileInfo& t) {
+        const int key0 = j * kBN;
+        if (kConv) return;  // the converter warps read the int8 K rows themselves
+        if (kMode == 2) {   // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
+          if (lane == 0) {
+            const int row = (int)((int64_t)r * p.max_ctx + key0);
+            for (int c = 0; c < 4; ++c) {
+              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
+              mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+              tma_load_3d(sK + c * kChunkBytes, &p.k16map, &bar.k_full[c], c * 64, kvh, row);
+            }
           }
+          __syncwarp();
+          return;
         }
-        __syncwarp();
-        return;
-      }
-      const int slot = (key0 + lane * G) % p.block_size;
-      for (int c = 0; c < 4; ++c) {
-        if (lane == 0) {
-          if (j == 0 || mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort))
-            mbar_arrive_expect_tx(&bar.k_full[c], t.nloaded * seg_bytes);
+        if (t.bad) {
+          if (lane == 0) {
+            for (int c = 0; c < 4 && gk > 0; ++c)
+              if (!mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
+            if (!*abort) mbar_arrive_expect_tx(&bar.fix, 4u * t.nloaded * seg_bytes);
+          }
+          __syncwarp();
+          if (*abort) return;
+          if (t.blk >= 0) issue_seg(sK, &p.kmap, &bar.fix, t.blk, key0);
+          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+          ++fix_phase;
+          __syncwarp();
+          if (*abort) return;
+          zero_rows(sK, kBN, t.bad, G, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0)
+            for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
+          __syncwarp();
+          return;
         }
-        __syncwarp();
-        if (*abort) return;
-        if (t.blk >= 0)
-          tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
-      }
-    };
-    TileInfo cur = info(0);
-    TileInfo nxt = info(1);
-    load_k(0, cur);
-    for (int j = 0; j < n_tiles && !*abort; ++j) {
-      const int key0 = j * kBN;
-      const int n_valid = min(kBN, seq_len - key0);
-      if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
-      // K of the next tile first: it streams in while QK_j runs (it waits only for QK_j)
-      if (j + 1 < n_tiles) load_k(j + 1, nxt);
-      __syncwarp();
-      if (*abort) break;
-      // V_j once PV_{j-1} has released the V tile
-      if (lane == 0 && j > 0) mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
-      __syncwarp();
-      if (*abort) break;
-      if (!cur.fix) {
-        if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
-        __syncwarp();
-        if (cur.big) issue_big(sV, &p.vmap_big, &bar.v_full, cur);
-        else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
-      } else {
-        // V rows past seq_len or in a bad segment must be zero (P is 0 there, but 0 * NaN is not):
-        // load through the private barrier, zero those rows, then publish.
-        if (lane == 0) mbar_arrive_expect_tx(&bar.fix, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
-        __syncwarp();
-        if (cur.big) issue_big(sV, &p.vmap_big, &bar.fix, cur);
-        else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
-        if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
-        ++fix_phase;
+        if (t.big) {
+          if (lane == 0) {
+            for (int c = 0; c < 4; ++c) {
+              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
+              mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+              tma_load_4d(sK + c * kChunkBytes, &p.kmap_big, &bar.k_full[c], c * 64, kvh, t.slot0, t.blk0);
+            }
+          }
+          __syncwarp();
+          return;
+        }
+        const int slot = (key0 + lane * G) % p.block_size;
+        for (int c = 0; c < 4; ++c) {
+          if (lane == 0) {
+            if (gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort))
+              mbar_arrive_expect_tx(&bar.k_full[c], t.nloaded * seg_bytes);
+          }
+          __syncwarp();
+          if (*abort) return;
+          if (t.blk >= 0)
+            tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
+        }
+      };
+      TileInfo cur = info(sg.t0);
+      TileInfo nxt = info(sg.t0 + 1);
+      load_k(sg.t0, g, cur);
+      for (int j = sg.t0; j < sg.t1 && !*abort; ++j, ++g) {
+        const int key0 = j * kBN;
+        const int n_valid = min(kBN, seq_len - key0);
+        if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
+        // K of the next tile first: it streams in while QK_g runs (it waits only for QK_g)
+        if (j + 1 < sg.t1) load_k(j + 1, g + 1, nxt);
         __syncwarp();
         if (*abort) break;
-        zero_rows(sV, n_valid, cur.bad, G, lane);
-        fence_proxy_async_smem();
+        // V of tile g once PV_{g-1} has released the V tile
+        if (lane == 0 && g > 0) mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar.v_full);
+        if (*abort) break;
+        if (!cur.fix) {
+          if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
+          __syncwarp();
+          if (cur.big) issue_big(sV, &p.vmap_big, &bar.v_full, cur);
+          else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
+        } else {
+          // V rows past seq_len or in a bad segment must be zero (P is 0 there, but 0 * NaN is not):
+          // load through the private barrier, zero those rows, then publish.
+          if (lane == 0) mbar_arrive_expect_tx(&bar.fix, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
+          __syncwarp();
+          if (cur.big) issue_big(sV, &p.vmap_big, &bar.fix, cur);
+          else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
+          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+          ++fix_phase;
+          __syncwarp();
+          if (*abort) break;
+          zero_rows(sV, n_valid, cur.bad, G, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar.v_full);
+        }
+        __syncwarp();
+        cur = nxt;
+        nxt = info(j + 2);
       }
-      __syncwarp();
-      cur = nxt;
-      nxt = info(j + 2);
+      ++s;
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------------------- MMA issuer
@@ -431,41 +616,67 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       constexpr uint32_t id_qk = idesc_f16(128, 128, !kInt8, false, false);
       constexpr uint32_t id_pv = idesc_f16(128, 256, true, false, true);
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
-      bool ok = mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, 0, abort);
-      auto issue_pv = [&](int i) -> bool {
+      // PV of CTA tile i; `first`: the first tile of segment si (O starts from zero once the
+      // previous segment's epilogue has read it)
+      auto issue_pv = [&](int i, bool first, int si) -> bool {
         if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
         if (!mbar_wait(&bar.v_full, i & 1, abort)) return false;
+        if (first && si > 0 && !mbar_wait(&bar.o_free, (si - 1) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t a = tmem + ((i & 1) ? kColP1 : kColP0);
         for (int ks = 0; ks < 8; ++ks)
           umma_f16_ts(tmem + kColO, a + ks * 8, smem_desc(v_base + ks * 2048, 16384, 1024), id_pv,
-                      (i > 0 || ks > 0) ? 1u : 0u);
+                      (!first || ks > 0) ? 1u : 0u);
         umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        // S is single-buffered: QK_j overwrites it once both softmax halves hold S_{j-1} in
-        // registers (PV_{j-2}, queued before QK_j, keeps the tensor pipe busy meanwhile)
-        if (j >= 1 && !mbar_wait(&bar.s_free, (j - 1) & 1, abort)) break;
-        const uint32_t dS = tmem + kColS;
-        for (int c = 0; c < 4; ++c) {
-          if (!mbar_wait(&bar.k_full[c], j & 1, abort)) {
+      SegIter it(p);
+      Seg sg;
+      int g = 0, s = 0;
+      bool ok = true;
+      int pend = -1;            // CTA tile of the PV not yet issued
+      bool pend_first = false;  // ... the first tile of its segment
+      int pend_seg = 0;         // ... in segment pend_seg
+      while (ok && it.next(sg)) {
+        if (!mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, s & 1, abort)) break;
+        for (int j = sg.t0; ok && j < sg.t1; ++j, ++g) {
+          // S is single-buffered: QK_g overwrites it once both softmax halves hold S_{g-1} in
+          // registers (PV_{g-2}, queued before QK_g, keeps the tensor pipe busy meanwhile)
+          if (g >= 1 && !mbar_wait(&bar.s_free, (g - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t off = c * kChunkBytes + kk * 32;
-            umma_f16_ss(dS, smem_desc(q_base + off, 16, 1024), smem_desc(k_base + off, 16, 1024), id_qk,
-                        (c | kk) ? 1u : 0u);
+          const uint32_t dS = tmem + kColS;
+          for (int c = 0; c < 4; ++c) {
+            if (!mbar_wait(&bar.k_full[c], g & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t off = c * kChunkBytes + kk * 32;
+              umma_f16_ss(dS, smem_desc(q_base + off, 16, 1024), smem_desc(k_base + off, 16, 1024), id_qk,
+                          (c | kk) ? 1u : 0u);
+            }
+            umma_commit(&bar.k_empty[c]);
           }
-          umma_commit(&bar.k_empty[c]);
+          if (!ok) break;
+          umma_commit(&bar.s_full);
+          if (j + 1 == sg.t1) umma_commit(&bar.q_empty);  // the segment's last read of Q
+          if (pend >= 0 && !issue_pv(pend, pend_first, pend_seg)) ok = false;
+          pend = g;
+          pend_first = j == sg.t0;
+          pend_seg = s;
         }
-        if (!ok) break;
-        umma_commit(&bar.s_full);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        // int8: the softmax quantizes the next segment's Q only after this segment's epilogue, which
+        // waits for its last PV - so that PV cannot wait for the next segment's first QK
+        if (kInt8 && ok && pend >= 0) {
+          ok = issue_pv(pend, pend_first, pend_seg);
+          pend = -1;
+        }
+        ++s;
       }
-      if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+      if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -477,245 +688,294 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     const int h = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;
-    const int p_i = min(p0 + i, seq_len - 1);
-    const bool row_valid = i < rows_valid;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float sc = p.scale_log2;
     bool dead = false;  // warp-uniform
-    if (kInt8) {
-      dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, 0, abort));
-      if (!dead && h == 0) {
-        bar.qscale[i] = quantize_q_row_inplace(sQ, i);
-        fence_proxy_async_smem();
-        mbar_arrive(&bar.q_ready);
+    SegIter it(p);
+    Seg sg;
+    int g = 0, s = 0;
+    while (it.next(sg)) {
+      const Unit& u = sg.u;
+      const int p_i = min(u.p0 + i, u.seq_len - 1);
+      const bool row_valid = i < u.rows_valid;
+      float sc = p.scale_log2;
+      if (kInt8) {
+        // half 0 quantizes the segment's Q rows in place; half 1 takes the row scales at the named
+        // barrier (it never waits for q_full: with a one-tile segment the next segment's Q may land
+        // before half 1 gets here, and a parity wait would then miss the phase)
+        if (h == 0) {
+          if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, s & 1, abort));
+          if (!dead) {
+            bar.qscale[i] = quantize_q_row_inplace(sQ, i);
+            fence_proxy_async_smem();
+            mbar_arrive(&bar.q_ready);
+          }
+        }
+        named_bar_sync(1, 256);
+        if (!dead) sc = p.scale_log2 * bar.qscale[i];
       }
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_ready, 0, abort));
-      if (!dead) sc = p.scale_log2 * bar.qscale[i];
-    }
-    float m_run = -INFINITY, l_run = 0.0f;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int key0 = j * kBN;
-      const float* ks = bar.kscale[j & 1] + 64 * h;
-      if (kInt8 && h == 0 && !dead) {
-        const int key = key0 + i;
-        float v = 0.0f;
-        if (key < seq_len) v = __ldg(p.k8_scale + ((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh);
-        bar.kscale[j & 1][i] = v;
-      }
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, j & 1, abort));
-      const uint32_t sb = tmem + lane_off + kColS;
-      const uint32_t pb = tmem + lane_off + ((j & 1) ? kColP1 : kColP0);
-      uint32_t sv[64];
-      if (!dead) {
-        tc_fence_after();
-        uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld_32x32b_x32(sb + 64 * h, a);
-        tmem_ld_32x32b_x32(sb + 64 * h + 32, b);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bar.s_free);  // S may now be overwritten by QK_{j+1}
-      } else {
+      float m_run = -INFINITY, l_run = 0.0f;
+      for (int j = sg.t0; j < sg.t1; ++j, ++g) {
+        const int key0 = j * kBN;
+        const float* ks = bar.kscale[g & 1] + 64 * h;
+        if (kInt8 && h == 0 && !dead) {
+          const int key = key0 + i;
+          float v = 0.0f;
+          if (key < u.seq_len) v = __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh);
+          bar.kscale[g & 1][i] = v;
+        }
+        if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, g & 1, abort));
+        const uint32_t sb = tmem + lane_off + kColS;
+        const uint32_t pb = tmem + lane_off + ((g & 1) ? kColP1 : kColP0);
+        uint32_t sv[64];
+        if (!dead) {
+          tc_fence_after();
+          uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
+          uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
+          tmem_ld_32x32b_x32(sb + 64 * h, a);
+          tmem_ld_32x32b_x32(sb + 64 * h + 32, b);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar.s_free);  // S may now be overwritten by QK_{g+1}
+        } else {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = 0u;
-      }
-      const int lim = p_i - key0 - 64 * h;  // this half's columns > lim are masked
-      const bool need_mask = lim < 63;
-      if (kInt8) {  // fold the per-key scales in place: s = S * ks
-        named_bar_sync(1, 256);  // this tile's kscale, written by half 0, is visible
+          for (int e = 0; e < 64; ++e) sv[e] = 0u;
+        }
+        const int lim = p_i - key0 - 64 * h;  // this half's columns > lim are masked
+        const bool need_mask = lim < 63;
+        if (kInt8) {  // fold the per-key scales in place: s = S * ks
+          named_bar_sync(1, 256);  // this tile's kscale, written by half 0, is visible
 #pragma unroll
-        for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
-      }
-      float mx = -INFINITY;
+          for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
+        }
+        float mx = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        float v = __uint_as_float(sv[e]);
-        if (need_mask && e > lim) v = -INFINITY;
-        mx = fmaxf(mx, v);
-      }
-      mx *= sc;  // sc > 0 (or NaN for a NaN q row)
-      // both halves of a row agree on its maximum through shared memory
-      bar.rowmax[j & 1][h][i] = mx;
-      named_bar_sync(1, 256);
-      mx = fmaxf(mx, bar.rowmax[j & 1][h ^ 1][i]);
-      bool rescale = false;
-      float alpha = 1.0f;
-      if (m_run == -INFINITY || mx > m_run + kRescaleThreshold) {
-        const float m_new = fmaxf(m_run, mx);
-        if (m_new != -INFINITY) {
-          rescale = m_run != -INFINITY;
-          alpha = rescale ? ex2_approx(m_run - m_new) : 0.0f;
-          l_run *= alpha;
-          m_run = m_new;
+        for (int e = 0; e < 64; ++e) {
+          float v = __uint_as_float(sv[e]);
+          if (need_mask && e > lim) v = -INFINITY;
+          mx = fmaxf(mx, v);
+        }
+        mx *= sc;  // sc > 0 (or NaN for a NaN q row)
+        // both halves of a row agree on its maximum through shared memory
+        bar.rowmax[g & 1][h][i] = mx;
+        named_bar_sync(1, 256);
+        mx = fmaxf(mx, bar.rowmax[g & 1][h ^ 1][i]);
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (m_run == -INFINITY || mx > m_run + kRescaleThreshold) {
+          const float m_new = fmaxf(m_run, mx);
+          if (m_new != -INFINITY) {
+            rescale = m_run != -INFINITY;
+            alpha = rescale ? ex2_approx(m_run - m_new) : 0.0f;
+            l_run *= alpha;
+            m_run = m_new;
+          }
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+        // P = exp2(s*sc - m) packed to bf16 pairs; the row sum uses the rounded weights that the PV
+        // MMA multiplies, so the result is a convex combination of V rows
+        uint32_t pk[32];
+        float lsum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
+          if (need_mask && 2 * e > lim) s0 = -INFINITY;
+          if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
+          const float e0 = ex2_approx(fmaf(s0, sc, -m_use)), e1 = ex2_approx(fmaf(s1, sc, -m_use));
+          pk[e] = pack_bf16x2(e0, e1);
+          lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+        }
+        l_run += lsum;
+        // P buffer g%2 was last read by PV_{g-2}; O may be rescaled only once PV_{g-1} is done
+        // (never needed on a segment's first tile: the running max starts there)
+        if (!dead && g >= 2)
+          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[g & 1], ((g - 2) >> 1) & 1, abort));
+        const bool need_o = __any_sync(0xffffffffu, rescale);
+        if (!dead && need_o && g >= 1)
+          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort));
+        if (!dead) {
+          tc_fence_after();
+          tmem_st_32x32b_x32(pb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
+          if (need_o) {
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t v[32];
+              const uint32_t oa = tmem + lane_off + kColO + 128 * h + cc * 32;
+              tmem_ld_32x32b_x32(oa, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              tmem_st_32x32b_x32(oa, v);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar.p_full[g & 1]);
         }
       }
-      const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-      // P = exp2(s*sc - m) packed to bf16 pairs; the row sum uses the rounded weights that the PV
-      // MMA multiplies, so the result is a convex combination of V rows
-      uint32_t pk[32];
-      float lsum = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
-        if (need_mask && 2 * e > lim) s0 = -INFINITY;
-        if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
-        const float e0 = ex2_approx(fmaf(s0, sc, -m_use)), e1 = ex2_approx(fmaf(s1, sc, -m_use));
-        pk[e] = pack_bf16x2(e0, e1);
-        lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
-      }
-      l_run += lsum;
-      // P buffer j%2 was last read by PV_{j-2}; O may be rescaled only once PV_{j-1} is done
-      if (!dead && j >= 2)
-        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
-      const bool need_o = __any_sync(0xffffffffu, rescale);
-      if (!dead && need_o && j >= 1)
-        dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
-      if (!dead) {
+      // epilogue: the segment's last PV done, then O / l - bf16 output rows for a whole unit, or
+      // the normalised fp32 partial and its log-sum-exp for a unit cut between CTAs
+      const int gl = g - 1;  // the segment's last CTA tile
+      bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[gl & 1], (gl >> 1) & 1, abort);
+      fin = __all_sync(0xffffffffu, fin);
+      bar.lsum[h][i] = l_run;
+      named_bar_sync(1, 256);
+      const float l_tot = l_run + bar.lsum[h ^ 1][i];
+      if (fin) {
         tc_fence_after();
-        tmem_st_32x32b_x32(pb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
-        if (need_o) {
+        const float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+        if (sg.whole) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(u.tok0 + i) * p.num_q_heads + u.qh) * kD + 128 * h);
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t v[32];
-            const uint32_t oa = tmem + lane_off + kColO + 128 * h + cc * 32;
-            tmem_ld_32x32b_x32(oa, v);
+            tmem_ld_32x32b_x32(tmem + lane_off + kColO + 128 * h + cc * 32, v);
+            tmem_wait_ld();
+            if (row_valid) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv_l, __uint_as_float(v[8 * q + 1]) * inv_l);
+                o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv_l, __uint_as_float(v[8 * q + 3]) * inv_l);
+                o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv_l, __uint_as_float(v[8 * q + 5]) * inv_l);
+                o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv_l, __uint_as_float(v[8 * q + 7]) * inv_l);
+                dst[cc * 4 + q] = o;
+              }
+            }
+          }
+        } else {
+          float* slot = p.ws + (int64_t)sg.slot * kSlotFloats;
+          float4* dst = reinterpret_cast<float4*>(slot + (int64_t)i * kD + 128 * h);
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + lane_off + kColO + 128 * h + cc * 32, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st_32x32b_x32(oa, v);
+            for (int q = 0; q < 8; ++q)
+              dst[cc * 8 + q] = make_float4(__uint_as_float(v[4 * q + 0]) * inv_l, __uint_as_float(v[4 * q + 1]) * inv_l,
+                                            __uint_as_float(v[4 * q + 2]) * inv_l, __uint_as_float(v[4 * q + 3]) * inv_l);
           }
+          // natural-log LSE of the row over this segment's keys: (m + log2 l) ln 2; -inf if none
+          if (h == 0)
+            slot[kBM * kD + i] = l_tot > 0.0f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
         }
-        tmem_wait_st();
+      }
+      if (!dead) {  // O has been read: the next segment's first PV may overwrite it
         tc_fence_before();
-        mbar_arrive(&bar.p_full[j & 1]);
+        mbar_arrive(&bar.o_free);
       }
-    }
-    // epilogue: O / l -> bf16, each half writes its 128 output columns of the row
-    bool fin = !dead && !*abort && n_tiles > 0;
-    if (n_tiles >= 2) fin = fin && mbar_wait(&bar.pv_done[n_tiles & 1], ((n_tiles - 2) >> 1) & 1, abort);
-    fin = fin && mbar_wait(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
-    fin = __all_sync(0xffffffffu, fin);
-    bar.rowmax[n_tiles & 1][h][i] = l_run;  // the slots of the parity no later tile reads
-    named_bar_sync(1, 256);
-    const float l_tot = l_run + bar.rowmax[n_tiles & 1][h ^ 1][i];
-    if (fin) {
-      tc_fence_after();
-      const float inv_l = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)(tok0 + i) * p.num_q_heads + qh) * kD + 128 * h);
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + kColO + 128 * h + cc * 32, v);
-        tmem_wait_ld();
-        if (row_valid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv_l, __uint_as_float(v[8 * q + 1]) * inv_l);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv_l, __uint_as_float(v[8 * q + 3]) * inv_l);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv_l, __uint_as_float(v[8 * q + 5]) * inv_l);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv_l, __uint_as_float(v[8 * q + 7]) * inv_l);
-            dst[cc * 4 + q] = o;
-          }
-        }
-      }
+      ++s;
     }
   } else if (kFused && warp >= 12) {
     // ---------------------------------------------------------------------------- fp8 dequant
     // thread t owns key row t of each tile: its e4m3 K row (256 B) and V row are read straight from
     // the paged pool through the block table (64-bit offsets), dequantized exactly as
     // kv_fp8_dequant_dense does (bf16_rn(fp32(e4m3) * scale)) and written into the swizzled bf16
-    // tiles: K chunk by chunk as QK_{j-1} releases it, V once PV_{j-1} is done. Rows past seq_len
+    // tiles: K chunk by chunk as QK_{g-1} releases it, V once PV_{g-1} is done. Rows past seq_len
     // or in an out-of-range block are zeros. The next row's loads are issued before each wait.
     const int t = (warp - 12) * 32 + lane;
     const float ksc = __ldg(p.k_scale), vsc = __ldg(p.v_scale);
-    auto row_src = [&](const uint8_t* pool, int key) -> const uint4* {
-      if (key >= seq_len) return nullptr;
-      const int col = key / p.block_size;
-      const int blk = col < p.max_blocks ? __ldg(p.block_table + (int64_t)r * p.bt_stride + col) : -1;
-      if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        record_error(p.dev_err, kErrDeviceBounds);
-        return nullptr;
-      }
-      return reinterpret_cast<const uint4*>(pool + (int64_t)blk * p.stride_blk +
-                                            (int64_t)(key % p.block_size) * p.stride_tok +
-                                            (int64_t)kvh * p.stride_head);
-    };
     uint4 raw[16];
     auto load_row = [&](const uint4* src) {
 #pragma unroll
       for (int q = 0; q < 16; ++q) raw[q] = src ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
     };
     // 64 codes of chunk c -> row t of chunk c of a swizzled [4][128][64 x bf16] tile
-    auto store_chunk = [&](uint8_t* tile, int c, float sc) {
+    auto store_chunk = [&](uint8_t* tile, int c, float scv) {
       uint8_t* row = tile + c * kChunkBytes + t * 128;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 hi;
-        const uint4 lo = dequant16_e4m3_bf16(raw[4 * c + q], sc, hi);
+        const uint4 lo = dequant16_e4m3_bf16(raw[4 * c + q], scv, hi);
         *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
         *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
       }
     };
-    load_row(row_src(p.k_fp8, t));
+    SegIter it(p);
+    Seg sg;
+    int g = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    while (ok && it.next(sg)) {
+      const Unit& u = sg.u;
+      auto row_src = [&](const uint8_t* pool, int key) -> const uint4* {
+        if (key >= u.seq_len) return nullptr;
+        const int col = key / p.block_size;
+        const int blk = col < p.max_blocks ? __ldg(p.block_table + (int64_t)u.r * p.bt_stride + col) : -1;
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+          record_error(p.dev_err, kErrDeviceBounds);
+          return nullptr;
+        }
+        return reinterpret_cast<const uint4*>(pool + (int64_t)blk * p.stride_blk +
+                                              (int64_t)(key % p.block_size) * p.stride_tok +
+                                              (int64_t)u.kvh * p.stride_head);
+      };
+      load_row(row_src(p.k_fp8, sg.t0 * kBN + t));
+      for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {  // unrolled: raw[] stays in registers
-        if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) {
+        for (int c = 0; c < 4; ++c) {  // unrolled: raw[] stays in registers
+          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          store_chunk(sK, c, ksc);
+          fence_proxy_async_smem();
+          mbar_arrive(&bar.k_full[c]);
+        }
+        if (!ok) break;
+        load_row(row_src(p.v_fp8, j * kBN + t));
+        if (g > 0 && !mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) {
           ok = false;
           break;
         }
-        store_chunk(sK, c, ksc);
-        fence_proxy_async_smem();
-        mbar_arrive(&bar.k_full[c]);
-      }
-      if (!ok) break;
-      load_row(row_src(p.v_fp8, j * kBN + t));
-      if (j > 0 && !mbar_wait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) break;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) store_chunk(sV, c, vsc);
-      fence_proxy_async_smem();
-      mbar_arrive(&bar.v_full);
-      if (j + 1 < n_tiles) load_row(row_src(p.k_fp8, (j + 1) * kBN + t));
+        for (int c = 0; c < 4; ++c) store_chunk(sV, c, vsc);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.v_full);
+        if (j + 1 < sg.t1) load_row(row_src(p.k_fp8, (j + 1) * kBN + t));
+      }
     }
   } else if (kConv && warp >= 12) {
     // ---------------------------------------------------------------------------- int8 K widening
     // thread t owns key row t of each tile: its 256 int8 codes come straight from the dense scratch
     // (16 x 16-byte loads, issued before waiting for the K tile to be free), are widened to fp16
-    // integers and stored into the swizzled K tile chunk by chunk as QK_{j-1} releases it
+    // integers and stored into the swizzled K tile chunk by chunk as QK_{g-1} releases it
     const int t = (warp - 12) * 32 + lane;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int key = j * kBN + t;
-      uint4 raw[16];
-      if (key < seq_len) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.k8 + (((int64_t)r * p.max_ctx + key) * p.num_kv_heads + kvh) * kD);
+    SegIter it(p);
+    Seg sg;
+    int g = 0;
+    bool ok = true;
+    while (ok && it.next(sg)) {
+      const Unit& u = sg.u;
+      for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
+        const int key = j * kBN + t;
+        uint4 raw[16];
+        if (key < u.seq_len) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.k8 + (((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh) * kD);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) raw[q] = __ldg(src + q);
-      } else {
+          for (int q = 0; q < 16; ++q) raw[q] = __ldg(src + q);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) raw[q] = make_uint4(0, 0, 0, 0);
-      }
-      bool ok = true;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (j > 0 && !mbar_wait(&bar.k_empty[c], (j - 1) & 1, abort)) {
-          ok = false;
-          break;
+          for (int q = 0; q < 16; ++q) raw[q] = make_uint4(0, 0, 0, 0);
         }
-        uint8_t* row = sK + c * kChunkBytes + t * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 16 codes = fp16 elements 64c + 16q .. +15
-          uint4 lo, hi;
-          widen16(raw[4 * c + q], lo, hi);
-          *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
-          *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
+        for (int c = 0; c < 4; ++c) {
+          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* row = sK + c * kChunkBytes + t * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // 16 codes = fp16 elements 64c + 16q .. +15
+            uint4 lo, hi;
+            widen16(raw[4 * c + q], lo, hi);
+            *reinterpret_cast<uint4*>(row + (((2u * q) ^ (t & 7)) * 16)) = lo;
+            *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bar.k_full[c]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&bar.k_full[c]);
       }
-      if (!ok) break;
     }
   }
 
@@ -728,6 +988,82 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   if (threadIdx.x == 0 && bar.abort) record_error(p.dev_err, kErrTimeout);
 }
 
+
+// Merges the pieces of the units that the persistent launch cut into key ranges: block (b, y) takes
+// rows 8y .. 8y + 7 of cut unit F + b. Piece i holds O_i = its keys' softmax-weighted V rows / l_i
+// and lse_i = m_i + ln l_i; the row is sum_i e^(lse_i - M) O_i / sum_i e^(lse_i - M) with
+// M = max_i lse_i (a piece whose keys the row cannot see has lse_i = -inf and weight 0). Warp w
+// takes row 8y + w, lane l columns 8l .. 8l + 7; every load of the row is issued before the first
+// is used (one memory round trip per thread).
+constexpr int kCombineRows = 8;
+
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ Params p) {
+  __shared__ Unit s_u;
+  __shared__ int s_n;                          // pieces; 0: nothing to merge in this block
+  __shared__ const float* s_slot[kMaxSplit];  // each piece's workspace slot
+  if (threadIdx.x == 0) {
+    s_n = 0;
+    const Schedule sc = make_schedule(p);
+    const int b = blockIdx.x;
+    if (sc.k > 1 && b < sc.R) {
+      Unit u;
+      unit_at(p, sc.f * p.num_ctas + b, u);
+      int n = 0;
+      for (int i = 0; i < sc.k; ++i)
+        if (u.n_tiles * i / sc.k < u.n_tiles * (i + 1) / sc.k) s_slot[n++] = p.ws + ((int64_t)i * sc.R + b) * kSlotFloats;
+      s_u = u;
+      s_n = n;
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  const int row = blockIdx.y * kCombineRows + (threadIdx.x >> 5);
+  if (n == 0 || row >= s_u.rows_valid) return;
+  const int lane = threadIdx.x & 31;
+  float lse[kMaxSplit];
+  float4 o[kMaxSplit][2];
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) {
+    if (k < n) {
+      const float* sl = s_slot[k];
+      lse[k] = sl[kBM * kD + row];
+      const float4* src = reinterpret_cast<const float4*>(sl + (int64_t)row * kD) + 2 * lane;
+      o[k][0] = src[0];
+      o[k][1] = src[1];
+    } else {
+      lse[k] = -INFINITY;
+      o[k][0] = o[k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) M = fmaxf(M, lse[k]);
+  float den = 0.0f;
+  float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) {
+    const float w = lse[k] == -INFINITY ? 0.0f : expf(lse[k] - M);
+    den += w;
+    acc[0] = fmaf(w, o[k][0].x, acc[0]);
+    acc[1] = fmaf(w, o[k][0].y, acc[1]);
+    acc[2] = fmaf(w, o[k][0].z, acc[2]);
+    acc[3] = fmaf(w, o[k][0].w, acc[3]);
+    acc[4] = fmaf(w, o[k][1].x, acc[4]);
+    acc[5] = fmaf(w, o[k][1].y, acc[5]);
+    acc[6] = fmaf(w, o[k][1].z, acc[6]);
+    acc[7] = fmaf(w, o[k][1].w, acc[7]);
+  }
+  const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+  uint4 r;
+  r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  r.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  r.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  r.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  reinterpret_cast<uint4*>(p.out + ((int64_t)(s_u.tok0 + row) * p.num_q_heads + s_u.qh) * kD)[lane] = r;
+}
+
+constexpr int kMaxCtas = 1024;  // persistent CTAs at most
+
 int gcd_int(int a, int b) {
   while (b) {
     const int t = a % b;
@@ -735,6 +1071,37 @@ int gcd_int(int a, int b) {
     b = t;
   }
   return a;
+}
+
+// Launches mode kMode: the classic grid, or (workspace given) the persistent grid of
+// P = min(SMs, workspace_bytes / kCtaWsBytes, kMaxCtas) CTAs followed by the combine ((P - 1) x 16
+// blocks: at most P - 1 units are cut, 8 rows a block).
+template <int kMode>
+pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t workspace_bytes, cudaStream_t st,
+                          const char* name) {
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(paged_prefill_attn_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg<kMode>::kSmem);
+    attr = true;
+  }
+  p.num_reqs = num_reqs;
+  if (!workspace) {
+    p.persistent = 0;
+    dim3 grid((unsigned)p.n_mtiles, (unsigned)p.num_q_heads, (unsigned)num_reqs);
+    paged_prefill_attn_kernel<kMode><<<grid, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
+    return check_launch(name);
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t P = std::min<int64_t>({(int64_t)sms, workspace_bytes / kCtaWsBytes, (int64_t)kMaxCtas});
+  p.persistent = 1;
+  p.num_ctas = (int32_t)P;
+  p.ws = static_cast<float*>(workspace);
+  paged_prefill_attn_kernel<kMode><<<(unsigned)P, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
+  if (P > 1) prefill_combine_kernel<<<dim3((unsigned)(P - 1), kBM / kCombineRows), 256, 0, st>>>(p);
+  return check_launch(name);
 }
 
 }  // namespace
@@ -749,8 +1116,8 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
                                              int32_t max_q_len, int32_t num_q_heads, int32_t num_kv_heads,
                                              int32_t head_dim, int32_t block_size, float softmax_scale,
                                              int32_t qk_mode, const int8_t* k8, const float* k8_scale,
-                                             const void* k16, int64_t max_ctx, void* out, int32_t* dev_err,
-                                             void* stream) {
+                                             const void* k16, int64_t max_ctx, void* out, void* workspace,
+                                             int64_t workspace_bytes, int32_t* dev_err, void* stream) {
   using namespace pkv;
   clear_error();
   PKV_UNSUP(head_dim == kD, "paged_prefill_attn: head_dim must be 256 (got %d)", head_dim);
@@ -772,6 +1139,9 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
           "paged_prefill_attn: q, caches, out and strides must be 16-byte aligned");
   PKV_ARG(softmax_scale > 0.0f, "paged_prefill_attn: softmax_scale must be positive");
   PKV_UNSUP(!int8 || (int64_t)num_reqs * max_ctx < (1ll << 31), "paged_prefill_attn: int8 scratch too large");
+  PKV_ARG(!workspace || (aligned16(workspace) && workspace_bytes >= kCtaWsBytes),
+          "paged_prefill_attn: workspace must be 16-byte aligned and hold at least %lld bytes (got %lld)",
+          (long long)kCtaWsBytes, (long long)workspace_bytes);
   if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
 
   Params p{};
@@ -823,7 +1193,6 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   p.out = static_cast<__nv_bfloat16*>(out);
   p.dev_err = dev_err;
 
-  dim3 grid((unsigned)p.n_mtiles, (unsigned)num_q_heads, (unsigned)num_reqs);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int mode = !int8 ? 0 : (k16 ? 2 : 1);
   if (mode == 2) {
@@ -833,18 +1202,9 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
     pkv_status s = encode_tiled(&p.k16map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k16, dims, strides, box, "k16");
     if (s != PKV_OK) return s;
   }
-  auto launch = [&](auto kernel, int threads, int smem_bytes, bool& attr) {
-    if (!attr) {
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-      attr = true;
-    }
-    kernel<<<grid, threads, smem_bytes, st>>>(p);
-  };
-  static bool attr0 = false, attr1 = false, attr2 = false;
-  if (mode == 0) launch(paged_prefill_attn_kernel<0>, Cfg<0>::kThreads, Cfg<0>::kSmem, attr0);
-  else if (mode == 1) launch(paged_prefill_attn_kernel<1>, Cfg<1>::kThreads, Cfg<1>::kSmem, attr1);
-  else launch(paged_prefill_attn_kernel<2>, Cfg<2>::kThreads, Cfg<2>::kSmem, attr2);
-  return check_launch("paged_prefill_attn");
+  if (mode == 0) return launch_prefill<0>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
+  if (mode == 1) return launch_prefill<1>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
+  return launch_prefill<2>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
 }
 
 extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
@@ -855,7 +1215,8 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
                                                  int32_t num_reqs, int32_t total_q, int32_t max_q_len,
                                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                                  int32_t block_size, float softmax_scale, void* out,
-                                                 int32_t* dev_err, void* stream) {
+                                                 void* workspace, int64_t workspace_bytes, int32_t* dev_err,
+                                                 void* stream) {
   using namespace pkv;
   clear_error();
   PKV_UNSUP(head_dim == kD, "paged_prefill_attn_fp8: head_dim must be 256 (got %d)", head_dim);
@@ -871,6 +1232,9 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
               stride_tok % 16 == 0 && stride_head % 16 == 0,
           "paged_prefill_attn_fp8: q, out, pools and pool strides must be 16-byte aligned");
   PKV_ARG(softmax_scale > 0.0f, "paged_prefill_attn_fp8: softmax_scale must be positive");
+  PKV_ARG(!workspace || (aligned16(workspace) && workspace_bytes >= kCtaWsBytes),
+          "paged_prefill_attn_fp8: workspace must be 16-byte aligned and hold at least %lld bytes (got %lld)",
+          (long long)kCtaWsBytes, (long long)workspace_bytes);
 
   Params p{};
   {
@@ -902,12 +1266,10 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
   p.stride_head = stride_head;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(paged_prefill_attn_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<3>::kSmem);
-    attr = true;
-  }
-  dim3 grid((unsigned)p.n_mtiles, (unsigned)num_q_heads, (unsigned)num_reqs);
-  paged_prefill_attn_kernel<3><<<grid, Cfg<3>::kThreads, Cfg<3>::kSmem, static_cast<cudaStream_t>(stream)>>>(p);
-  return check_launch("paged_prefill_attn_fp8");
+  return launch_prefill<3>(p, num_reqs, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                           "paged_prefill_attn_fp8");
+}
+
+extern "C" size_t pkv_paged_prefill_workspace_bytes(int32_t num_ctas) {
+  return num_ctas > 0 ? (size_t)num_ctas * (size_t)pkv::kCtaWsBytes : 0;
 }

@@ -57,7 +57,7 @@ def test_library_targets_sm103a(libpath):
 
 
 def test_abi_version(pkv):
-    assert pkv.lib.pkv_abi_version() == 4
+    assert pkv.lib.pkv_abi_version() == 5
 
 
 def test_workspace_bytes(pkv):
@@ -70,11 +70,11 @@ def test_workspace_bytes(pkv):
 def _prefill_args(**kw):
     a = dict(q=16, k=16, v=16, nb=4, sb=16384, st=1024, sh=256, bt=16, bts=1, mb=1, sl=16, qsl=16, R=1, total_q=1,
              max_q=1, hq=16, hkv=4, d=256, bs=16, scale=0.0625, mode=0, k8=None, k8s=None, k16=None, max_ctx=0,
-             out=16, err=None, stream=None)
+             out=16, ws=None, ws_bytes=0, err=None, stream=None)
     a.update(kw)
     return [a[k] for k in ("q", "k", "v", "nb", "sb", "st", "sh", "bt", "bts", "mb", "sl", "qsl", "R", "total_q",
                            "max_q", "hq", "hkv", "d", "bs", "scale", "mode", "k8", "k8s", "k16", "max_ctx", "out",
-                           "err", "stream")]
+                           "ws", "ws_bytes", "err", "stream")]
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -86,6 +86,8 @@ def _prefill_args(**kw):
     (dict(mode=7), 1),                # unknown qk mode
     (dict(mode=1), 1),                # int8 mode without k8 / k8_scale
     (dict(sb=-5), 1),                 # negative stride
+    (dict(ws=24, ws_bytes=1 << 20), 1),  # misaligned workspace
+    (dict(ws=16, ws_bytes=1000), 1),  # workspace smaller than one CTA's slots
 ])
 def test_prefill_rejects_bad_arguments(pkv, kw, status):
     rc = pkv.lib.pkv_paged_prefill_attn(*_prefill_args(**kw))
@@ -156,7 +158,8 @@ def test_cache_write_empty_batch_launches_nothing(pkv):
 
 def test_fused_fp8_prefill_rejects_bad_arguments(pkv):
     f = pkv.lib.pkv_paged_prefill_attn_fp8
-    base = [16, 16, 16, 16, 16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 1, 1, 16, 4, 256, 16, 0.0625, 16, None, None]
+    base = [16, 16, 16, 16, 16, 4, 16384, 1024, 256, 16, 1, 1, 16, 16, 1, 1, 1, 16, 4, 256, 16, 0.0625, 16, None, 0,
+            None, None]
     bad = list(base); bad[19] = 128   # head_dim != 256
     assert f(*bad) == 2
     bad = list(base); bad[1] = None   # null K pool
@@ -165,5 +168,14 @@ def test_fused_fp8_prefill_rejects_bad_arguments(pkv):
     assert f(*bad) == 1
     bad = list(base); bad[17] = 15    # q heads not a multiple of kv heads
     assert f(*bad) == 2
+    bad = list(base); bad[23] = 16; bad[24] = 4096  # workspace below one CTA's slots
+    assert f(*bad) == 1
     empty = list(base); empty[14] = 0  # no requests: nothing launched
     assert f(*empty) == 0
+
+
+def test_prefill_workspace_bytes(pkv):
+    # four slots per CTA, each 128 x 256 fp32 partial outputs and 128 fp32 log-sum-exps
+    assert pkv.paged_prefill_workspace_bytes(1) == 4 * (128 * 256 + 128) * 4
+    assert pkv.paged_prefill_workspace_bytes(152) == 152 * 526336
+    assert pkv.paged_prefill_workspace_bytes(0) == 0

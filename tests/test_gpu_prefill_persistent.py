@@ -1,0 +1,194 @@
+"""GPU parity of the persistent prefill launch: the same attention as the classic grid, with the
+query tiles of the last partial wave cut into key ranges so that every SM has work.
+
+Every case runs at several grid sizes (a workspace sized for P CTAs gives a grid of P): P = 1 (one
+CTA walks every unit, nothing is cut), small P (many units per CTA, several cut), and the full SM
+count. Bars: query tiles that the schedule does not cut are computed with the classic kernel's
+arithmetic in the same order, so their rows equal the classic launch bit for bit; rows of cut tiles
+are merged from fp32 partials and must meet the classic path's bound against the oracle. The
+workspace starts as NaN, so a read of a slot that no CTA wrote shows up.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-3
+TOL_INT8 = 5e-3
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_int64_gb300 as m
+    return m
+
+
+from _devsetup import bf16_to_u16, dev_err, device_meta, device_pool, device_q  # noqa: E402
+from test_gpu_parity import _close, _edge_tol, _oracle_prefill  # noqa: E402
+
+
+def split_count(R, P, k_max=4):
+    """the number of key ranges each unit of the last partial wave is cut into: k in [1, 4]
+    minimising ceil(R k / P) / k + 0.02 (k - 1)."""
+    best, best_cost = 1, 2.0
+    for k in range(1, k_max + 1):
+        if R == 0:
+            break
+        cost = -(-R * k // P) / k + 0.02 * (k - 1)
+        if cost < best_cost - 1e-6:
+            best, best_cost = k, cost
+    return best
+
+
+def cut_rows(p, P):
+    """Host model of the persistent schedule: a boolean per (token, q head), True where the row's
+    query tile is cut into key ranges. Units with rows, in the order m-tile descending, request,
+    head; the first P floor(U / P) are whole, the remaining R are cut when split_count(R, P) > 1."""
+    n_mt = (max(r.q_len for r in p.requests) + 127) // 128
+    units = []
+    for mt in reversed(range(n_mt)):
+        for r, req in enumerate(p.requests):
+            if mt * 128 >= req.q_len or req.q_len > req.seq_len:
+                continue
+            rows = min(128, req.q_len - mt * 128)
+            for qh in range(p.num_q_heads):
+                units.append((int(p.query_start_loc[r]) + mt * 128, rows, qh))
+    U = len(units)
+    F = P * (U // P)
+    cut = np.zeros((p.total_q, p.num_q_heads), dtype=bool)
+    if split_count(U - F, P) > 1:
+        for tok0, rows, qh in units[F:]:
+            cut[tok0:tok0 + rows, qh] = True
+    return cut
+
+
+def _inputs(pkv, p, mode):
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, sl, qsl = device_meta(p)
+    q = device_q(p)
+    kw = {}
+    if mode:
+        max_ctx = int(p.seq_lens.max())
+        k8 = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads, 256), dtype=torch.int8, device="cuda")
+        ks = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads), dtype=torch.float32, device="cuda")
+        k16 = torch.zeros((p.num_reqs, max_ctx, p.num_kv_heads, 256), dtype=torch.float16, device="cuda")
+        pb = torch.zeros(p.num_reqs, dtype=torch.int32, device="cuda")
+        pkv.kv_int8_stats_quant(k, bt, pb, sl, max_ctx, k8, ks, k16=k16)
+        kw = dict(qk_mode=1, k8_scale=ks, k8=k8 if mode == 1 else None, k16=k16 if mode == 2 else None)
+        k = None
+    return q, k, v, bt, sl, qsl, kw
+
+
+def _prefill(pkv, p, inp, P):
+    q, k, v, bt, sl, qsl, kw = inp
+    out = torch.full_like(q, float("nan"))
+    err = dev_err()
+    ws = None
+    if P:
+        ws = torch.full((pkv.paged_prefill_workspace_bytes(P) // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+    pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, max(r.q_len for r in p.requests), p.softmax_scale, out,
+                           dev_err=err, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device status {err.item()}"
+    return bf16_to_u16(out)
+
+
+CASES = {
+    # several requests, q_len and seq_len off every tile boundary, one-tile units among long ones
+    "ragged": dict(seq_lens=[700, 129, 300, 1], q_lens=[300, 129, 1, 1], num_blocks=80, block_size=16),
+    # the pages' 24 query / 4 KV heads
+    "gqa6": dict(seq_lens=[517, 260], q_lens=[200, 133], num_blocks=64, block_size=16, num_q_heads=24,
+                 num_kv_heads=4),
+    # block 880: tiles straddle blocks in 16-key segments
+    "bs880": dict(seq_lens=[2000, 1000], q_lens=[300, 1000], num_blocks=40, block_size=880),
+    # one decode-like row per head over 3,000 keys: fewer tiles than CTAs, units cut into many pieces
+    "thin": dict(seq_lens=[3000], q_lens=[1], num_blocks=200, block_size=16, num_q_heads=4, num_kv_heads=4),
+}
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("case", list(CASES))
+def test_persistent_prefill_matches_classic_and_oracle(pkv, mode, case):
+    p = W.make_problem(case, seed=60 + list(CASES).index(case), **CASES[case])
+    inp = _inputs(pkv, p, mode)
+    classic = _prefill(pkv, p, inp, 0)
+    ref = _oracle_prefill(p, min(mode, 1))
+    tol = _edge_tol(p, TOL_INT8 if mode else TOL_BF16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for P in (1, 3, 7, sms):
+        got = _prefill(pkv, p, inp, P)
+        cut = cut_rows(p, P)
+        assert P > 1 or not cut.any()
+        whole = ~cut
+        assert np.array_equal(got.reshape(p.total_q, p.num_q_heads, 256)[whole],
+                              classic.reshape(p.total_q, p.num_q_heads, 256)[whole]), f"P={P}"
+        _close(got, ref, tol)
+
+
+def test_persistent_fp8_fused_prefill(pkv):
+    """The fused fp8 path on the persistent grid equals its classic launch on uncut query tiles and
+    the dense-scratch oracle everywhere."""
+    p = W.make_problem("f8p", seed=70, seq_lens=[1500, 300, 129], q_lens=[700, 300, 1], num_blocks=150,
+                       block_size=16, kv_dtype="e4m3")
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    bt, sl, qsl = device_meta(p)
+    q = device_q(p)
+    scale = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    max_q = max(r.q_len for r in p.requests)
+
+    def run(P):
+        out = torch.full_like(q, float("nan"))
+        err = dev_err()
+        ws = None
+        if P:
+            ws = torch.full((pkv.paged_prefill_workspace_bytes(P) // 4,), float("nan"), dtype=torch.float32,
+                            device="cuda")
+        pkv.paged_prefill_attn_fp8(q, k, v, scale, scale, bt, sl, qsl, max_q, p.softmax_scale, out, dev_err=err,
+                                   workspace=ws)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        return bf16_to_u16(out)
+
+    classic = run(0)
+    rk, rv = oracle.kv_fp8_dequant_dense(p.pool_numpy("k"), p.pool_numpy("v"), p.block_table(fill=0), p.seq_lens,
+                                         int(p.seq_lens.max()), 0.5, 0.5)
+    ident = np.arange(p.num_reqs, dtype=np.int32).reshape(p.num_reqs, 1)
+    ref = oracle.paged_prefill_attn(p.q, rk, rv, ident, p.seq_lens, p.query_start_loc, p.num_q_heads,
+                                    p.softmax_scale)
+    for P in (5, torch.cuda.get_device_properties(0).multi_processor_count):
+        got = run(P)
+        whole = ~cut_rows(p, P)
+        assert np.array_equal(got.reshape(p.total_q, p.num_q_heads, 256)[whole],
+                              classic.reshape(p.total_q, p.num_q_heads, 256)[whole])
+        _close(got, ref, _edge_tol(p, TOL_BF16))
+
+
+def test_persistent_bigpool_sampled_rows(pkv):
+    """The bench chunk (20,000-token request on the top blocks of a 2,600-block pool, last 2,048
+    queries) on the full persistent grid: sampled rows against the oracle, in every qk mode."""
+    p = W.bigpool(top=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cut = cut_rows(p, sms)
+    for mode in (0, 2):
+        inp = _inputs(pkv, p, mode)
+        got = _prefill(pkv, p, inp, sms)
+        classic = _prefill(pkv, p, inp, 0)
+        whole = ~cut
+        assert np.array_equal(got.reshape(p.total_q, p.num_q_heads, 256)[whole],
+                              classic.reshape(p.total_q, p.num_q_heads, 256)[whole])
+        # rows of cut and uncut tiles: the first and last rows of the chunk and of an m-tile boundary
+        for t in (0, 127, 128, 1000, 2047):
+            ref = _oracle_prefill(p, min(mode, 1), tok_begin=t, tok_end=t + 1)
+            _close(got[t:t + 1], ref, TOL_INT8 if mode else TOL_BF16)
+        assert cut.any() and whole.any()
+        del inp
+        torch.cuda.empty_cache()
