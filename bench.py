@@ -184,6 +184,9 @@ class Workload:
         self.pl = torch.empty((S, T_VERIFY, HQ), dtype=torch.float32, device=dev)
         self.vout = torch.empty_like(self.vq)
         self.host_q = None
+        # the persistent prefill launch (one CTA per SM: full waves of whole query tiles, the last
+        # partial wave cut into key ranges and merged) needs a workspace; every prefill uses it
+        self.ws = torch.empty(pkv.paged_prefill_workspace_bytes(), dtype=torch.uint8, device=dev)
         del u16_to_bf16
 
     def step(self, ev=None):
@@ -201,23 +204,23 @@ class Workload:
                 ev.append((name, a, b))
 
         rec("prefill_bf16", lambda: pkv.paged_prefill_attn(self.q, self.k, self.v, self.bt, self.sl, self.qsl, CHUNK,
-                                                           s, self.out[0]))
+                                                           s, self.out[0], workspace=self.ws))
         rec("int8_quant", lambda: pkv.kv_int8_stats_quant(self.k, self.bt, self.pos_begin, self.sl, CHUNK, self.k8,
                                                           self.k8s, k16=self.k16))
         rec("prefill_int8", lambda: pkv.paged_prefill_attn(self.q, None, self.v, self.bt, self.sl, self.qsl, CHUNK, s,
                                                            self.out[1], qk_mode=pkv.PKV_QK_INT8, k8_scale=self.k8s,
-                                                           k16=self.k16))
+                                                           k16=self.k16, workspace=self.ws))
         rec("fp8_dequant", lambda: pkv.kv_fp8_dequant_dense(self.kf, self.vf, self.bt, self.sl, self.fscale,
                                                             self.fscale, self.kd, self.vd))
         rec("prefill_fp8_dense", lambda: pkv.paged_prefill_attn(self.q, self.kd, self.vd, self.ident, self.sl,
-                                                                self.qsl, CHUNK, s, self.out[2]))
+                                                                self.qsl, CHUNK, s, self.out[2], workspace=self.ws))
         rec("verify_partial", lambda: pkv.spec_verify_attn_partial(self.vq, self.vk, self.vv, self.vks, self.vvs,
                                                                    self.vbt, self.vsl, T_VERIFY, self.pv.softmax_scale,
                                                                    self.split, self.po, self.pl))
         rec("verify_combine", lambda: pkv.spec_verify_combine(self.po, self.pl, self.vsl, T_VERIFY, self.split,
                                                               self.vout))
 
-    LAUNCHES_PER_STEP = 7
+    LAUNCHES_PER_STEP = 10  # 3 prefills x (persistent kernel + merge), quant, dequant, verify partial + combine
     TOKENS_PER_STEP = 3 * CHUNK + T_VERIFY
 
 
@@ -288,6 +291,7 @@ def run_gpu(args):
     # the two fp8 prefill paths on the step's fp8 chunk: dequantize once into the dense scratch, or
     # dequantize every tile inside the prefill
     fp8_paths = run_fp8_paths(torch, pkv, wl, flush, args)
+    prefill_launches = run_prefill_launches(torch, pkv, wl, flush, args)
     quant_full = run_quant_full_context(torch, pkv, wl, flush, args)
 
     if rank != 0:
@@ -317,7 +321,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
         "config": {"workload": "bigpool_20000_last_chunk_2048: 2,600-block pool, block_size 880, request on blocks "
-                               "2577-2599, 16 q / 4 kv heads, head_dim 256; step = bf16 + int8-QK + fp8-dense "
+                               "2577-2599, 16 q / 4 kv heads, head_dim 256; step = bf16 + int8-QK + fp8-dense (persistent launch) "
                                "prefill of the chunk and an 8-token int8-KV verify",
                    "tokens_per_step": wl.TOKENS_PER_STEP, "l2": "flushed before every step (512 MB write)",
                    "parallelism": f"replicas x{world}"},
@@ -334,6 +338,7 @@ def run_gpu(args):
         },
         "verify_batch": vb,
         "fp8_prefill_paths": fp8_paths,
+        "prefill_launches": prefill_launches,
         "e2e": e2e,
         "gpu_launches": wl.LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks.summary(),
@@ -438,6 +443,37 @@ def run_quant_full_context(torch, pkv, wl, flush, args):
     return _gbs(nbytes, statistics.mean(ts), peaks)
 
 
+def run_prefill_launches(torch, pkv, wl, flush, args):
+    """The step's bf16 and int8-QK prefills launched both ways: one CTA per query tile (no
+    workspace) and the persistent grid the step uses. CUDA events, L2 flushed before each call."""
+    s = wl.p.softmax_scale
+    out = torch.empty_like(wl.q)
+    calls = {
+        "bf16": lambda ws: pkv.paged_prefill_attn(wl.q, wl.k, wl.v, wl.bt, wl.sl, wl.qsl, CHUNK, s, out, workspace=ws),
+        "int8": lambda ws: pkv.paged_prefill_attn(wl.q, None, wl.v, wl.bt, wl.sl, wl.qsl, CHUNK, s, out,
+                                                  qk_mode=pkv.PKV_QK_INT8, k8_scale=wl.k8s, k16=wl.k16, workspace=ws),
+    }
+    flops = algorithmic()["prefill_flops"]
+    res = {}
+    for name, fn in calls.items():
+        for ws in (None, wl.ws):
+            for _ in range(max(3, args.warmup)):
+                fn(ws)
+        t = {"per_query_tile": [], "persistent": []}
+        for _ in range(max(5, min(args.steps, 30))):
+            for kind, ws in (("per_query_tile", None), ("persistent", wl.ws)):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn(ws)
+                b.record()
+                b.synchronize()
+                t[kind].append(a.elapsed_time(b))
+        res[name] = {k: {"ms": round(statistics.mean(v), 4),
+                         "tflops": round(flops / (statistics.mean(v) * 1e-3) / 1e12, 2)} for k, v in t.items()}
+    return res
+
+
 def run_fp8_paths(torch, pkv, wl, flush, args):
     """Chunk of 2,048 queries at the end of the 20,000-token e4m3 context, both fp8 prefill paths:
     kv_fp8_dequant_dense + bf16 prefill on the scratch, against paged_prefill_attn_fp8 (per-tile
@@ -449,10 +485,11 @@ def run_fp8_paths(torch, pkv, wl, flush, args):
         pkv.kv_fp8_dequant_dense(wl.kf, wl.vf, wl.bt, wl.sl, wl.fscale, wl.fscale, wl.kd, wl.vd)
 
     def dense_attn():
-        pkv.paged_prefill_attn(wl.q, wl.kd, wl.vd, wl.ident, wl.sl, wl.qsl, CHUNK, s, out)
+        pkv.paged_prefill_attn(wl.q, wl.kd, wl.vd, wl.ident, wl.sl, wl.qsl, CHUNK, s, out, workspace=wl.ws)
 
     def fused():
-        pkv.paged_prefill_attn_fp8(wl.q, wl.kf, wl.vf, wl.fscale, wl.fscale, wl.bt, wl.sl, wl.qsl, CHUNK, s, out)
+        pkv.paged_prefill_attn_fp8(wl.q, wl.kf, wl.vf, wl.fscale, wl.fscale, wl.bt, wl.sl, wl.qsl, CHUNK, s, out,
+                                   workspace=wl.ws)
 
     for _ in range(max(3, args.warmup)):
         dense(); dense_attn(); fused()
@@ -680,7 +717,8 @@ def run_ncu_case(args):
             "prefill_bf16_persistent": lambda: pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, CHUNK, p.softmax_scale,
                                                                       out, workspace=ws),
             "prefill_int8": lambda: pkv.paged_prefill_attn(q, None, v, bt, sl, qsl, CHUNK, p.softmax_scale, out,
-                                                           qk_mode=pkv.PKV_QK_INT8, k8_scale=k8s, k16=k16),
+                                                           qk_mode=pkv.PKV_QK_INT8, k8_scale=k8s, k16=k16,
+                                                           workspace=ws),
             "int8_quant": lambda: pkv.kv_int8_stats_quant(k, bt, pb, sl, CHUNK, k8, k8s, k16=k16),
             "fp8_dequant": lambda: pkv.kv_fp8_dequant_dense(k, v, bt, sl, sc, sc, kd, vd),
         }

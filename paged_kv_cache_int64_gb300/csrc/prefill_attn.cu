@@ -102,10 +102,13 @@ struct Barriers {
 
 // workspace of the persistent launch: kMaxSplit slots per CTA (the pieces of the units cut in key
 // ranges, fewer than P units of at most kMaxSplit pieces), each the normalised fp32 O [128 rows][256]
-// followed by the rows' natural-log LSE [128]
+// followed by the rows' natural-log LSE [128]. The last slot (never a piece's: pieces number at most
+// (P - 1) kMaxSplit) holds the merge's header: F, R, k, then per cut unit its tok0, head, rows and
+// key tiles, written by the persistent kernel so that the merge need not recompute the schedule.
 constexpr int kMaxSplit = 4;
 constexpr int64_t kSlotFloats = (int64_t)kBM * kD + kBM;
 constexpr int64_t kCtaWsBytes = kMaxSplit * kSlotFloats * 4;
+constexpr int kHdrUnits = 4;  // ints before the first unit entry
 
 struct Params {
   CUtensorMap qmap;   // bf16 q: dims {D, Hq, total_q}, box {64, 1, 128}
@@ -141,6 +144,7 @@ struct Params {
   int32_t persistent;
   int32_t num_reqs;
   int32_t num_ctas;  // the persistent grid
+  int32_t total_q;
   float* ws;         // [num_ctas * kMaxSplit][kSlotFloats]
 };
 
@@ -427,6 +431,13 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
+  if (p.persistent && blockIdx.x == 0 && threadIdx.x == 96) {  // warp 3: the merge header's schedule
+    const Schedule sc = make_schedule(p);
+    int* hdr = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
+    hdr[0] = sc.f * p.num_ctas;
+    hdr[1] = sc.R;
+    hdr[2] = sc.k;
+  }
   // Barrier phases follow g, the CTA's running tile count over all its segments, and s, its
   // segment count; positions and masks follow the unit-local tile index j.
 
@@ -858,6 +869,14 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           // natural-log LSE of the row over this segment's keys: (m + log2 l) ln 2; -inf if none
           if (h == 0)
             slot[kBM * kD + i] = l_tot > 0.0f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : -INFINITY;
+          if (h == 0 && i == 0) {  // the unit's header entry (every piece writes the same values)
+            int* e = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats) + kHdrUnits +
+                     4 * (sg.slot % it.sc.R);
+            e[0] = u.tok0;
+            e[1] = u.qh;
+            e[2] = u.rows_valid;
+            e[3] = u.n_tiles;
+          }
         }
       }
       if (!dead) {  // O has been read: the next segment's first PV may overwrite it
@@ -1001,18 +1020,29 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
   __shared__ Unit s_u;
   __shared__ int s_n;                          // pieces; 0: nothing to merge in this block
   __shared__ const float* s_slot[kMaxSplit];  // each piece's workspace slot
+  // launched as a programmatic dependent: wait for the persistent kernel's writes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     s_n = 0;
-    const Schedule sc = make_schedule(p);
+    const int* hdr = reinterpret_cast<const int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
+    const int R = hdr[1], k = hdr[2];
     const int b = blockIdx.x;
-    if (sc.k > 1 && b < sc.R) {
+    if (k > 1 && k <= kMaxSplit && R < p.num_ctas && b < R) {
+      const int* e = hdr + kHdrUnits + 4 * b;
       Unit u;
-      unit_at(p, sc.f * p.num_ctas + b, u);
-      int n = 0;
-      for (int i = 0; i < sc.k; ++i)
-        if (u.n_tiles * i / sc.k < u.n_tiles * (i + 1) / sc.k) s_slot[n++] = p.ws + ((int64_t)i * sc.R + b) * kSlotFloats;
-      s_u = u;
-      s_n = n;
+      u.tok0 = e[0];
+      u.qh = e[1];
+      u.rows_valid = e[2];
+      u.n_tiles = e[3];
+      // the entry was written by this launch unless it aborted; never write outside out
+      if (u.tok0 >= 0 && u.rows_valid >= 1 && u.rows_valid <= kBM && u.tok0 <= p.total_q - u.rows_valid &&
+          u.qh >= 0 && u.qh < p.num_q_heads && u.n_tiles >= 1) {
+        int n = 0;
+        for (int i = 0; i < k; ++i)
+          if (u.n_tiles * i / k < u.n_tiles * (i + 1) / k) s_slot[n++] = p.ws + ((int64_t)i * R + b) * kSlotFloats;
+        s_u = u;
+        s_n = n;
+      }
     }
   }
   __syncthreads();
@@ -1100,7 +1130,21 @@ pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t 
   p.num_ctas = (int32_t)P;
   p.ws = static_cast<float*>(workspace);
   paged_prefill_attn_kernel<kMode><<<(unsigned)P, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
-  if (P > 1) prefill_combine_kernel<<<dim3((unsigned)(P - 1), kBM / kCombineRows), 256, 0, st>>>(p);
+  if (P > 1) {
+    // programmatic dependent launch: the merge's blocks may be scheduled as the persistent CTAs
+    // exit and wait (griddepcontrol.wait) for the whole grid's writes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(P - 1), kBM / kCombineRows);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, prefill_combine_kernel, p);
+  }
   return check_launch(name);
 }
 
@@ -1190,6 +1234,7 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   p.max_ctx = max_ctx;
   p.num_kv_heads = num_kv_heads;
   p.n_mtiles = (max_q_len + kBM - 1) / kBM;
+  p.total_q = total_q;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.dev_err = dev_err;
 
@@ -1257,6 +1302,7 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.num_kv_heads = num_kv_heads;
   p.n_mtiles = (max_q_len + kBM - 1) / kBM;
+  p.total_q = total_q;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.dev_err = dev_err;
   p.k_fp8 = k_fp8;
