@@ -192,3 +192,67 @@ def test_persistent_bigpool_sampled_rows(pkv):
         assert cut.any() and whole.any()
         del inp
         torch.cuda.empty_cache()
+
+
+def _run_both(pkv, p, bt, P_list):
+    """classic then persistent launches (P CTAs each) on the same inputs: outputs and device status."""
+    k, v = device_pool(p, "k"), device_pool(p, "v")
+    _, sl, qsl = device_meta(p)
+    q = device_q(p)
+    max_q = max(max(r.q_len for r in p.requests), 1)
+    res = []
+    for P in [0] + list(P_list):
+        out = torch.full_like(q, float("nan"))
+        err = dev_err()
+        ws = None
+        if P:
+            ws = torch.full((pkv.paged_prefill_workspace_bytes(P) // 4,), float("nan"), dtype=torch.float32,
+                            device="cuda")
+        pkv.paged_prefill_attn(q, k, v, bt, sl, qsl, max_q, p.softmax_scale, out, dev_err=err, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((P, bf16_to_u16(out), err.item()))
+    return res
+
+
+def test_persistent_out_of_range_block_is_reported_and_zero_filled(pkv):
+    """A table entry one past the pool: both launches report PKV_ERR_DEVICE_BOUNDS, read nothing
+    through it (those keys count as zeros), and agree on every uncut query tile bit for bit."""
+    p = W.make_problem("badp", seed=72, seq_lens=[700, 300], q_lens=[400, 300], num_blocks=80, block_size=16)
+    bt, _, _ = device_meta(p)
+    bt[0, 5] = p.num_blocks  # keys 80..95 of request 0
+    res = _run_both(pkv, p, bt, (7, torch.cuda.get_device_properties(0).multi_processor_count))
+    _, classic, err0 = res[0]
+    assert err0 == pkv.PKV_ERR_DEVICE_BOUNDS
+    assert np.isfinite(W.bf16_bits_to_f32(classic)).all()
+    c = W.bf16_bits_to_f32(classic).astype(np.float64)
+    for P, got, err in res[1:]:
+        assert err == pkv.PKV_ERR_DEVICE_BOUNDS
+        whole = ~cut_rows(p, P)
+        g = got.reshape(p.total_q, p.num_q_heads, 256)
+        assert np.array_equal(g[whole], classic.reshape(p.total_q, p.num_q_heads, 256)[whole])
+        gf = W.bf16_bits_to_f32(got).astype(np.float64)
+        assert np.isfinite(gf).all()
+        assert (np.abs(gf - c) <= 2.0 ** -7 * np.abs(c) + 2e-3).all()
+
+
+def test_persistent_skips_empty_and_inconsistent_requests(pkv):
+    """A request with no queries and one whose q_len exceeds its seq_len (no causal chunk) have no
+    query tiles: both launches leave the second's rows unwritten and compute the others alike."""
+    p = W.make_problem("skip", seed=73, seq_lens=[300, 200, 30, 500], q_lens=[0, 150, 40, 130], num_blocks=80,
+                       block_size=16)
+    bt, _, _ = device_meta(p)
+    res = _run_both(pkv, p, bt, (3, torch.cuda.get_device_properties(0).multi_processor_count))
+    _, classic, err0 = res[0]
+    c = W.bf16_bits_to_f32(classic).astype(np.float64)
+    skipped = np.zeros(p.total_q, dtype=bool)
+    skipped[150:190] = True  # request 2's rows
+    assert np.isnan(c[skipped]).all() and np.isfinite(c[~skipped]).all()
+    for P, got, err in res[1:]:
+        assert err == err0
+        gf = W.bf16_bits_to_f32(got).astype(np.float64)
+        assert np.isnan(gf[skipped]).all() and np.isfinite(gf[~skipped]).all()
+        whole = ~cut_rows(p, P)
+        g = got.reshape(p.total_q, p.num_q_heads, 256)
+        assert np.array_equal(g[whole & ~skipped[:, None]], classic.reshape(p.total_q, p.num_q_heads, 256)[
+            whole & ~skipped[:, None]])
+        assert (np.abs(gf[~skipped] - c[~skipped]) <= 2.0 ** -7 * np.abs(c[~skipped]) + 2e-3).all()
