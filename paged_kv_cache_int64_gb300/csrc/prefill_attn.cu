@@ -145,6 +145,11 @@ struct Params {
   int32_t num_reqs;
   int32_t num_ctas;  // the persistent grid
   int32_t total_q;
+  // key tiles: 0 - tile t holds keys [128 t, 128 t + 128); else (block_size >= 128 and not a multiple
+  // of 128) the tiles of each block in turn, tpb = ceil(block_size / 128) per block, the last one
+  // short, so that no tile straddles two blocks
+  int32_t tpb;
+  float tpb_inv;  // 1 / tpb (fast division of tile indices)
   float* ws;         // [num_ctas * kMaxSplit][kSlotFloats]
 };
 
@@ -243,7 +248,71 @@ struct Unit {
   int r, qh, mt, kvh, seq_len, rows_valid, p0, n_tiles, tok0;
 };
 
+// Key tiles. With p.tpb == 0 tile t is keys [128 t, 128 t + 128). Otherwise tiles follow the blocks:
+// tile t is the (t % tpb)-th 128-key piece of block t / tpb, the block's last piece shorter, so a
+// tile never straddles two blocks and is always one TMA box per chunk (the box's rows past the
+// block end read as zeros and are masked). With block_size 880 this removes the 16-key segment
+// loads that one tile in eight would otherwise need.
+// t = b * tpb + l (tile indices are below 2^24 since keys are below 2^31: the float quotient is
+// within one of the exact one, and one correction step makes it exact)
+__device__ __forceinline__ void tile_divmod(const Params& p, int t, int& b, int& l) {
+  b = (int)((float)t * p.tpb_inv);
+  l = t - b * p.tpb;
+  if (l < 0) {
+    --b;
+    l += p.tpb;
+  } else if (l >= p.tpb) {
+    ++b;
+    l -= p.tpb;
+  }
+}
+// first key and number of keys of tile t
+template <bool kA>
+__device__ __forceinline__ void tile_range(const Params& p, int t, int& key0, int& len) {
+  if constexpr (!kA) {
+    key0 = t * kBN;
+    len = kBN;
+    return;
+  }
+  int b, l;
+  tile_divmod(p, t, b, l);
+  key0 = b * p.block_size + l * kBN;
+  len = min(kBN, p.block_size - l * kBN);
+}
+// Walks consecutive tiles without divisions: the next tile starts where this one ends.
+struct TileCursor {
+  int key0, len;  // first key and number of keys of the tile
+  int l;          // its index within its block (tpb > 0)
+};
+template <bool kA>
+__device__ __forceinline__ TileCursor tile_cursor(const Params& p, int t) {
+  TileCursor c;
+  c.l = 0;
+  if constexpr (kA) {
+    int b;
+    tile_divmod(p, t, b, c.l);
+  }
+  tile_range<kA>(p, t, c.key0, c.len);
+  return c;
+}
+template <bool kA>
+__device__ __forceinline__ void tile_advance(const Params& p, TileCursor& c) {
+  c.key0 += c.len;
+  if constexpr (kA) {
+    if (++c.l == p.tpb) c.l = 0;
+    c.len = min(kBN, p.block_size - c.l * kBN);
+  }
+}
+// tiles covering keys [0, keys)
+template <bool kA>
+__device__ __forceinline__ int tiles_for(const Params& p, int keys) {
+  if constexpr (!kA) return (keys + kBN - 1) / kBN;
+  const int full = keys / p.block_size;
+  return full * p.tpb + (keys - full * p.block_size + kBN - 1) / kBN;
+}
+
 // Fills u for (r, mt, qh); false when the m-tile holds no query rows.
+template <bool kA>
 __device__ __forceinline__ bool make_unit(const Params& p, int r, int mt, int qh, Unit& u) {
   const int q0 = __ldg(p.qsl + r);
   const int q_len = __ldg(p.qsl + r + 1) - q0;
@@ -257,15 +326,16 @@ __device__ __forceinline__ bool make_unit(const Params& p, int r, int mt, int qh
   u.rows_valid = min(kBM, q_len - mt * kBM);
   u.p0 = seq_len - q_len + mt * kBM;                      // position of row 0
   const int kv_end = min(seq_len, u.p0 + u.rows_valid);  // keys [0, kv_end)
-  u.n_tiles = (kv_end + kBN - 1) / kBN;
+  u.n_tiles = tiles_for<kA>(p, kv_end);
   u.tok0 = q0 + mt * kBM;
   return true;
 }
 
 // key tiles of each unit of (request r, m-tile mt); 0 when the m-tile holds no rows
+template <bool kA>
 __device__ __forceinline__ int unit_tiles(const Params& p, int r, int mt) {
   Unit u;
-  return make_unit(p, r, mt, 0, u) ? u.n_tiles : 0;
+  return make_unit<kA>(p, r, mt, 0, u) ? u.n_tiles : 0;
 }
 
 // A segment: key tiles [t0, t1) of one unit, processed by this CTA.
@@ -289,10 +359,11 @@ struct Schedule {
   int U, f, R, k;
 };
 
+template <bool kA>
 __device__ int count_groups(const Params& p) {
   int n = 0;
   for (int m = p.n_mtiles - 1; m >= 0; --m)
-    for (int r = 0; r < p.num_reqs; ++r) n += unit_tiles(p, r, m) > 0;
+    for (int r = 0; r < p.num_reqs; ++r) n += unit_tiles<kA>(p, r, m) > 0;
   return n;
 }
 
@@ -311,10 +382,11 @@ __host__ __device__ inline int choose_split(int R, int P) {
   return best;
 }
 
+template <bool kA>
 __device__ Schedule make_schedule(const Params& p) {
   Schedule sc;
   const int P = p.num_ctas;
-  sc.U = count_groups(p) * p.num_q_heads;
+  sc.U = count_groups<kA>(p) * p.num_q_heads;
   sc.f = sc.U / P;
   sc.R = sc.U - sc.f * P;
   sc.k = choose_split(sc.R, P);
@@ -322,19 +394,21 @@ __device__ Schedule make_schedule(const Params& p) {
 }
 
 // unit u of the persistent order
+template <bool kA>
 __device__ void unit_at(const Params& p, int u, Unit& out) {
   int g = u / p.num_q_heads;
   const int qh = u - g * p.num_q_heads;
   for (int m = p.n_mtiles - 1; m >= 0; --m)
     for (int r = 0; r < p.num_reqs; ++r)
-      if (unit_tiles(p, r, m) > 0 && g-- == 0) {
-        make_unit(p, r, m, qh, out);
+      if (unit_tiles<kA>(p, r, m) > 0 && g-- == 0) {
+        make_unit<kA>(p, r, m, qh, out);
         return;
       }
 }
 
 // Walks this CTA's segments; every role walks the same sequence. Classic launch: one segment, the
 // unit of blockIdx (latest m-tiles first), whole. Persistent launch: its whole units, then its pieces.
+template <bool kA>
 struct SegIter {
   const Params& p;
   Schedule sc{};
@@ -343,13 +417,13 @@ struct SegIter {
   int64_t pi = 0;  // next piece
   __device__ explicit SegIter(const Params& pp) : p(pp) {
     if (!p.persistent) return;
-    sc = make_schedule(p);
+    sc = make_schedule<kA>(p);
     pi = p.num_ctas - 1 - (int)blockIdx.x;
   }
   __device__ bool next(Seg& s) {
     if (!p.persistent) {
       if (count++ > 0) return false;
-      if (!make_unit(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, s.u)) return false;
+      if (!make_unit<kA>(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, s.u)) return false;
       s.t0 = 0;
       s.t1 = s.u.n_tiles;
       s.whole = true;
@@ -358,7 +432,7 @@ struct SegIter {
     }
     const int P = p.num_ctas;
     if (w < sc.f) {
-      unit_at(p, (int)blockIdx.x + P * w++, s.u);
+      unit_at<kA>(p, (int)blockIdx.x + P * w++, s.u);
       s.t0 = 0;
       s.t1 = s.u.n_tiles;
       s.whole = true;
@@ -370,7 +444,7 @@ struct SegIter {
       const int j = (int)(pi % sc.R), i = (int)(pi / sc.R);
       s.slot = (int)pi;
       pi += P;
-      unit_at(p, sc.f * P + j, s.u);
+      unit_at<kA>(p, sc.f * P + j, s.u);
       s.t0 = s.u.n_tiles * i / sc.k;
       s.t1 = s.u.n_tiles * (i + 1) / sc.k;
       if (s.t0 == s.t1) continue;  // a unit of fewer than k tiles: this range is empty
@@ -382,7 +456,9 @@ struct SegIter {
   }
 };
 
-template <int kMode>
+// kA: key tiles follow the blocks (block_size >= 128, not a multiple of 128, several blocks per
+// request); otherwise plain 128-key tiles
+template <int kMode, bool kA>
 __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     paged_prefill_attn_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -399,7 +475,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   if (!p.persistent) {  // classic launch: a CTA without rows leaves at once (CTA-uniform)
     Unit u;
-    if (!make_unit(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, u)) return;
+    if (!make_unit<kA>(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, u)) return;
   }
 
   if (threadIdx.x == 0) {
@@ -432,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
   if (p.persistent && blockIdx.x == 0 && threadIdx.x == 96) {  // warp 3: the merge header's schedule
-    const Schedule sc = make_schedule(p);
+    const Schedule sc = make_schedule<kA>(p);
     int* hdr = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
     hdr[0] = sc.f * p.num_ctas;
     hdr[1] = sc.R;
@@ -458,7 +534,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
       }
     }
-    SegIter it(p);
+    SegIter<kA> it(p);
     Seg sg;
     int g = 0, s = 0;
     uint32_t fix_phase = 0;
@@ -480,9 +556,9 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         continue;
       }
       // block id of segment `lane` of tile j: >= 0, -1 past seq_len, -2 out-of-range entry
-      auto lookup = [&](int j) -> int {
-        const int pos = j * kBN + lane * G;
-        if (lane >= nseg || pos >= seq_len) return -1;
+      auto lookup = [&](int key0, int len) -> int {
+        const int pos = key0 + lane * G;
+        if (lane >= nseg || lane * G >= len || pos >= seq_len) return -1;
         const int col = pos / p.block_size;
         if (col >= p.max_blocks) return -2;
         const int blk = __ldg(p.block_table + (int64_t)r * p.bt_stride + col);
@@ -500,16 +576,23 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
         bool big;          // the 128 keys lie in one valid block: 4 copies of 128 rows per tensor
         int blk0, slot0;   // block and first slot of key 0 of the tile
+        int key0, len;     // the tile's keys
       };
-      auto info = [&](int j) -> TileInfo {
+      // the tile at cursor c (in_seg: one of the segment's tiles)
+      auto info = [&](const TileCursor& c, bool in_seg) -> TileInfo {
         TileInfo t;
-        t.blk = j < sg.t1 ? lookup(j) : -1;
+        const int key0 = c.key0, len = c.len;
+        t.key0 = key0;
+        t.len = len;
+        t.blk = in_seg ? lookup(key0, len) : -1;
         t.bad = __ballot_sync(0xffffffffu, t.blk == -2);
         t.nloaded = __popc(__ballot_sync(0xffffffffu, t.blk >= 0));
-        t.fix = t.bad != 0 || seq_len - j * kBN < kBN;
+        t.fix = t.bad != 0 || seq_len - key0 < len;
         t.blk0 = __shfl_sync(0xffffffffu, t.blk, 0);
-        t.slot0 = (j * kBN) % p.block_size;
-        t.big = p.big_ok && t.bad == 0 && t.blk0 >= 0 && t.slot0 + kBN <= p.block_size;
+        t.slot0 = key0 % p.block_size;
+        // one block holds the tile's keys: 4 copies of a 128-row box per tensor (rows past the
+        // block's end, in a short tile, read as zeros)
+        t.big = p.big_ok && t.bad == 0 && t.blk0 >= 0 && t.slot0 + len <= p.block_size;
         return t;
       };
       // a whole tile of one tensor with 4 copies of [128 rows][64 x 16-bit] (lane 0)
@@ -520,8 +603,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       // K tile j (CTA tile gk) chunk by chunk as QK_{gk-1} frees it. K rows past seq_len need no
       // zero-fill (their scores are masked); rows of a bad segment do, so such a tile goes through
       // the private barrier, is patched, then published.
-      auto load_k = [&](int j, int gk, const TileInfo& t) {
-        const int key0 = j * kBN;
+      auto load_k = [&](int gk, const TileInfo& t) {
+        const int key0 = t.key0;
         if (kConv) return;  // the converter warps read the int8 K rows themselves
         if (kMode == 2) {   // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
           if (lane == 0) {
@@ -579,15 +662,17 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
             tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
         }
       };
-      TileInfo cur = info(sg.t0);
-      TileInfo nxt = info(sg.t0 + 1);
-      load_k(sg.t0, g, cur);
+      TileCursor nc = tile_cursor<kA>(p, sg.t0);  // the tile `nxt` describes
+      TileInfo cur = info(nc, true);
+      tile_advance<kA>(p, nc);
+      TileInfo nxt = info(nc, sg.t0 + 1 < sg.t1);
+      load_k(g, cur);
       for (int j = sg.t0; j < sg.t1 && !*abort; ++j, ++g) {
-        const int key0 = j * kBN;
-        const int n_valid = min(kBN, seq_len - key0);
+        const int key0 = cur.key0;
+        const int n_valid = min(cur.len, seq_len - key0);
         if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
         // K of the next tile first: it streams in while QK_g runs (it waits only for QK_g)
-        if (j + 1 < sg.t1) load_k(j + 1, g + 1, nxt);
+        if (j + 1 < sg.t1) load_k(g + 1, nxt);
         __syncwarp();
         if (*abort) break;
         // V of tile g once PV_{g-1} has released the V tile
@@ -617,7 +702,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
         __syncwarp();
         cur = nxt;
-        nxt = info(j + 2);
+        tile_advance<kA>(p, nc);
+        nxt = info(nc, j + 2 < sg.t1);
       }
       ++s;
     }
@@ -641,7 +727,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
-      SegIter it(p);
+      SegIter<kA> it(p);
       Seg sg;
       int g = 0, s = 0;
       bool ok = true;
@@ -701,7 +787,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     const int i = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool dead = false;  // warp-uniform
-    SegIter it(p);
+    SegIter<kA> it(p);
     Seg sg;
     int g = 0, s = 0;
     while (it.next(sg)) {
@@ -725,13 +811,15 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         if (!dead) sc = p.scale_log2 * bar.qscale[i];
       }
       float m_run = -INFINITY, l_run = 0.0f;
-      for (int j = sg.t0; j < sg.t1; ++j, ++g) {
-        const int key0 = j * kBN;
+      TileCursor tc = tile_cursor<kA>(p, sg.t0);
+      for (int j = sg.t0; j < sg.t1; ++j, ++g, tile_advance<kA>(p, tc)) {
+        const int key0 = tc.key0, len = tc.len;
         const float* ks = bar.kscale[g & 1] + 64 * h;
         if (kInt8 && h == 0 && !dead) {
           const int key = key0 + i;
           float v = 0.0f;
-          if (key < u.seq_len) v = __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh);
+          if (i < len && key < u.seq_len)
+            v = __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh);
           bar.kscale[g & 1][i] = v;
         }
         if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, g & 1, abort));
@@ -751,7 +839,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 64; ++e) sv[e] = 0u;
         }
-        const int lim = p_i - key0 - 64 * h;  // this half's columns > lim are masked
+        // this half's columns > lim are masked: keys after the row's position or past a short tile
+        const int lim = min(p_i, key0 + len - 1) - key0 - 64 * h;
         const bool need_mask = lim < 63;
         if (kInt8) {  // fold the per-key scales in place: s = S * ks
           named_bar_sync(1, 256);  // this tile's kscale, written by half 0, is visible
@@ -910,14 +999,17 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         *reinterpret_cast<uint4*>(row + (((2u * q + 1) ^ (t & 7)) * 16)) = hi;
       }
     };
-    SegIter it(p);
+    SegIter<kA> it(p);
     Seg sg;
     int g = 0;
     bool ok = true;
     while (ok && it.next(sg)) {
       const Unit& u = sg.u;
-      auto row_src = [&](const uint8_t* pool, int key) -> const uint4* {
-        if (key >= u.seq_len) return nullptr;
+      // row t of the tile at cursor c (nullptr: zeros - past a short tile, past seq_len, or a bad
+      // block)
+      auto row_src = [&](const uint8_t* pool, const TileCursor& c) -> const uint4* {
+        const int key = c.key0 + t;
+        if (t >= c.len || key >= u.seq_len) return nullptr;
         const int col = key / p.block_size;
         const int blk = col < p.max_blocks ? __ldg(p.block_table + (int64_t)u.r * p.bt_stride + col) : -1;
         if (blk < 0 || (int64_t)blk >= p.num_blocks) {
@@ -928,7 +1020,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
                                               (int64_t)(key % p.block_size) * p.stride_tok +
                                               (int64_t)u.kvh * p.stride_head);
       };
-      load_row(row_src(p.k_fp8, sg.t0 * kBN + t));
+      TileCursor tc = tile_cursor<kA>(p, sg.t0);
+      load_row(row_src(p.k_fp8, tc));
       for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // unrolled: raw[] stays in registers
@@ -941,7 +1034,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           mbar_arrive(&bar.k_full[c]);
         }
         if (!ok) break;
-        load_row(row_src(p.v_fp8, j * kBN + t));
+        load_row(row_src(p.v_fp8, tc));
         if (g > 0 && !mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) {
           ok = false;
           break;
@@ -950,7 +1043,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         for (int c = 0; c < 4; ++c) store_chunk(sV, c, vsc);
         fence_proxy_async_smem();
         mbar_arrive(&bar.v_full);
-        if (j + 1 < sg.t1) load_row(row_src(p.k_fp8, (j + 1) * kBN + t));
+        tile_advance<kA>(p, tc);
+        if (j + 1 < sg.t1) load_row(row_src(p.k_fp8, tc));
       }
     }
   } else if (kConv && warp >= 12) {
@@ -959,16 +1053,17 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     // (16 x 16-byte loads, issued before waiting for the K tile to be free), are widened to fp16
     // integers and stored into the swizzled K tile chunk by chunk as QK_{g-1} releases it
     const int t = (warp - 12) * 32 + lane;
-    SegIter it(p);
+    SegIter<kA> it(p);
     Seg sg;
     int g = 0;
     bool ok = true;
     while (ok && it.next(sg)) {
       const Unit& u = sg.u;
-      for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
-        const int key = j * kBN + t;
+      TileCursor tc = tile_cursor<kA>(p, sg.t0);
+      for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g, tile_advance<kA>(p, tc)) {
+        const int key = tc.key0 + t;
         uint4 raw[16];
-        if (key < u.seq_len) {
+        if (t < tc.len && key < u.seq_len) {
           const uint4* src = reinterpret_cast<const uint4*>(
               p.k8 + (((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh) * kD);
 #pragma unroll
@@ -1106,12 +1201,12 @@ int gcd_int(int a, int b) {
 // Launches mode kMode: the classic grid, or (workspace given) the persistent grid of
 // P = min(SMs, workspace_bytes / kCtaWsBytes, kMaxCtas) CTAs followed by the combine ((P - 1) x 16
 // blocks: at most P - 1 units are cut, 8 rows a block).
-template <int kMode>
+template <int kMode, bool kA>
 pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t workspace_bytes, cudaStream_t st,
                           const char* name) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(paged_prefill_attn_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(paged_prefill_attn_kernel<kMode, kA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg<kMode>::kSmem);
     attr = true;
   }
@@ -1119,7 +1214,7 @@ pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t 
   if (!workspace) {
     p.persistent = 0;
     dim3 grid((unsigned)p.n_mtiles, (unsigned)p.num_q_heads, (unsigned)num_reqs);
-    paged_prefill_attn_kernel<kMode><<<grid, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
+    paged_prefill_attn_kernel<kMode, kA><<<grid, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
     return check_launch(name);
   }
   int dev = 0, sms = 0;
@@ -1129,7 +1224,7 @@ pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t 
   p.persistent = 1;
   p.num_ctas = (int32_t)P;
   p.ws = static_cast<float*>(workspace);
-  paged_prefill_attn_kernel<kMode><<<(unsigned)P, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
+  paged_prefill_attn_kernel<kMode, kA><<<(unsigned)P, Cfg<kMode>::kThreads, Cfg<kMode>::kSmem, st>>>(p);
   if (P > 1) {
     // programmatic dependent launch: the merge's blocks may be scheduled as the persistent CTAs
     // exit and wait (griddepcontrol.wait) for the whole grid's writes
@@ -1235,6 +1330,9 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
   p.num_kv_heads = num_kv_heads;
   p.n_mtiles = (max_q_len + kBM - 1) / kBM;
   p.total_q = total_q;
+  // block-aligned tiles where a 128-key tile could straddle two blocks of a request
+  p.tpb = (block_size >= kBN && block_size % kBN != 0 && max_blocks > 1) ? (block_size + kBN - 1) / kBN : 0;
+  p.tpb_inv = p.tpb ? 1.0f / (float)p.tpb : 0.0f;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.dev_err = dev_err;
 
@@ -1247,9 +1345,15 @@ extern "C" pkv_status pkv_paged_prefill_attn(const void* q, const void* k_cache,
     pkv_status s = encode_tiled(&p.k16map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, k16, dims, strides, box, "k16");
     if (s != PKV_OK) return s;
   }
-  if (mode == 0) return launch_prefill<0>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
-  if (mode == 1) return launch_prefill<1>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
-  return launch_prefill<2>(p, num_reqs, workspace, workspace_bytes, st, "paged_prefill_attn");
+  const char* nm = "paged_prefill_attn";
+  if (p.tpb) {
+    if (mode == 0) return launch_prefill<0, true>(p, num_reqs, workspace, workspace_bytes, st, nm);
+    if (mode == 1) return launch_prefill<1, true>(p, num_reqs, workspace, workspace_bytes, st, nm);
+    return launch_prefill<2, true>(p, num_reqs, workspace, workspace_bytes, st, nm);
+  }
+  if (mode == 0) return launch_prefill<0, false>(p, num_reqs, workspace, workspace_bytes, st, nm);
+  if (mode == 1) return launch_prefill<1, false>(p, num_reqs, workspace, workspace_bytes, st, nm);
+  return launch_prefill<2, false>(p, num_reqs, workspace, workspace_bytes, st, nm);
 }
 
 extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp8, const uint8_t* v_fp8,
@@ -1303,6 +1407,9 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
   p.num_kv_heads = num_kv_heads;
   p.n_mtiles = (max_q_len + kBM - 1) / kBM;
   p.total_q = total_q;
+  // plain 128-key tiles: the converter warps read K/V rows one by one, so tiles that straddle
+  // blocks cost nothing extra, and the tiles (so the arithmetic) are those of the dense-scratch path
+  p.tpb = 0;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.dev_err = dev_err;
   p.k_fp8 = k_fp8;
@@ -1312,7 +1419,7 @@ extern "C" pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k
   p.stride_head = stride_head;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
-  return launch_prefill<3>(p, num_reqs, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+  return launch_prefill<3, false>(p, num_reqs, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
                            "paged_prefill_attn_fp8");
 }
 

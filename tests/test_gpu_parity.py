@@ -163,7 +163,7 @@ def test_prefill_tiny_config_bf16(pkv):
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])  # 2: int8 QK reading the fp16 copy of the codes
-@pytest.mark.parametrize("case", ["ragged", "gqa6", "from_scratch", "bs880"])
+@pytest.mark.parametrize("case", ["ragged", "gqa6", "from_scratch", "bs880", "bs200"])
 def test_prefill_ragged_cases(pkv, mode, case):
     if case == "ragged":     # several requests, q_len and seq_len off every tile boundary
         p = W.make_problem("r", seed=5, seq_lens=[700, 129, 300, 1], q_lens=[300, 129, 1, 1], num_blocks=80,
@@ -173,8 +173,10 @@ def test_prefill_ragged_cases(pkv, mode, case):
                            num_q_heads=24, num_kv_heads=4)
     elif case == "from_scratch":  # a first chunk: q_len == seq_len, queries from position 0
         p = W.make_problem("s", seed=7, seq_lens=[333], q_lens=[333], num_blocks=32, block_size=16)
-    else:                    # block 880, tiles straddle blocks in 16-key segments
+    elif case == "bs880":    # block 880: key tiles follow the blocks (6 of 128 keys and one of 112)
         p = W.make_problem("b", seed=8, seq_lens=[2000, 1000], q_lens=[300, 1000], num_blocks=40, block_size=880)
+    else:                    # block 200: tiles of 128 and 72 keys; the last tile of a request ragged too
+        p = W.make_problem("c", seed=9, seq_lens=[1111, 333], q_lens=[400, 333], num_blocks=16, block_size=200)
     got, _ = _run_prefill(pkv, p, min(mode, 1), use_k16=mode == 2)
     ref = _oracle_prefill(p, min(mode, 1))
     _close(got, ref, _edge_tol(p, TOL_INT8 if mode else TOL_BF16))

@@ -108,8 +108,10 @@ CASES = {
     # the pages' 24 query / 4 KV heads
     "gqa6": dict(seq_lens=[517, 260], q_lens=[200, 133], num_blocks=64, block_size=16, num_q_heads=24,
                  num_kv_heads=4),
-    # block 880: tiles straddle blocks in 16-key segments
+    # block 880: key tiles follow the blocks (6 of 128 keys and one of 112 per block)
     "bs880": dict(seq_lens=[2000, 1000], q_lens=[300, 1000], num_blocks=40, block_size=880),
+    # block 200: tiles of 128 and 72 keys
+    "bs200": dict(seq_lens=[1111, 333], q_lens=[400, 333], num_blocks=16, block_size=200),
     # one decode-like row per head over 3,000 keys: fewer tiles than CTAs, units cut into many pieces
     "thin": dict(seq_lens=[3000], q_lens=[1], num_blocks=200, block_size=16, num_q_heads=4, num_kv_heads=4),
 }
