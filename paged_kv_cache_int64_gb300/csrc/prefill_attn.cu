@@ -812,15 +812,26 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       }
       float m_run = -INFINITY, l_run = 0.0f;
       TileCursor tc = tile_cursor<kA>(p, sg.t0);
+      // int8: the scale of key i of the tile at cursor c (0 past a short tile or seq_len); half 0
+      // loads the next tile's while this one is scored, so the load's latency stays off the path
+      auto key_scale = [&](const TileCursor& c) -> float {
+        const int key = c.key0 + i;
+        return (i < c.len && key < u.seq_len)
+                   ? __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh)
+                   : 0.0f;
+      };
+      float ks_next = 0.0f;
+      if (kInt8 && h == 0 && !dead) ks_next = key_scale(tc);
       for (int j = sg.t0; j < sg.t1; ++j, ++g, tile_advance<kA>(p, tc)) {
         const int key0 = tc.key0, len = tc.len;
         const float* ks = bar.kscale[g & 1] + 64 * h;
         if (kInt8 && h == 0 && !dead) {
-          const int key = key0 + i;
-          float v = 0.0f;
-          if (i < len && key < u.seq_len)
-            v = __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh);
-          bar.kscale[g & 1][i] = v;
+          bar.kscale[g & 1][i] = ks_next;
+          if (j + 1 < sg.t1) {
+            TileCursor nc = tc;
+            tile_advance<kA>(p, nc);
+            ks_next = key_scale(nc);
+          }
         }
         if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, g & 1, abort));
         const uint32_t sb = tmem + lane_off + kColS;
