@@ -7,12 +7,14 @@
 // block table with the block id widened to int64 before the stride product.
 //
 // sm_103a design (one CTA = 128 query rows of one query head of one request):
-//   warp 0      TMA producer: Q once; per 128-key tile, K and V gathered from the paged pool with
+//   warp 0      TMA producer: Q once; per key tile, K and V gathered from the paged pool with
 //               4-D tensor maps [head_dim, kv_heads, block_size, num_blocks] whose block
 //               coordinate is the block id (the TMA unit forms the 64-bit address): a tile inside
-//               one block is 4 copies of 128 rows per tensor; a tile across blocks is split into
-//               segments of gcd(block_size, 128) keys, one lane per segment reading the table; the
-//               next tile's block ids are read early.
+//               one block is 4 copies of 128 rows per tensor; with blocks under 128 keys a tile is
+//               split into segments of gcd(block_size, 128) keys, one lane per segment reading the
+//               table; the next tile's block ids are read early. Key tiles are 128 keys, or (kA:
+//               block_size >= 128 and not a multiple of 128) follow the blocks, the last tile of a
+//               block short, so that no tile straddles two blocks (tile_range, TileCursor).
 //   warp 1      MMA issuer (one thread): S = Q K^T (tcgen05.mma kind::f16, M=128 N=128 K=256,
 //               both operands in shared memory, f32 accumulator in tensor memory), then
 //               O += P V (M=128 N=256 K=128) with P read from tensor memory and V MN-major.
@@ -27,7 +29,7 @@
 //               epilogue normalises O and stores bf16.
 //   warps 12-15 int8-QK only: read the int8 K rows (dense scratch of kv_int8_stats_quant) and
 //               widen them to fp16 integers in the K tile; half 0 of the softmax quantizes the Q
-//               rows in place first. Q8.K8 runs as an f16 MMA: every product and partial sum is an
+//               rows in place first and loads each tile's per-key K scales a tile ahead. Q8.K8 runs as an f16 MMA: every product and partial sum is an
 //               integer below 2^24, so the f32 accumulator holds the exact integer dot product.
 // Rows of the last tile past seq_len (and of any out-of-range block) are zero-filled in shared
 // memory before the MMAs read them, so stale or NaN pool bytes never reach P.V. Every wait is
