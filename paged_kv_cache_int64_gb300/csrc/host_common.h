@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
+
+#include <atomic>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -25,6 +27,18 @@ pkv_status encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, c
                         const char* what, bool swizzle128 = true);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Runs fn once per (flag, current device): for kernel attributes the driver keeps per device, such
+// as the dynamic shared-memory opt-in. Devices 64 and up run fn on every call.
+template <typename F>
+inline void once_per_device(std::atomic<uint64_t>& done, F&& fn) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_relaxed) & bit)) return;
+  fn();
+  if (bit) done.fetch_or(bit, std::memory_order_relaxed);
+}
 
 // SM count of the current device (cached per device).
 int num_sms();

@@ -1217,12 +1217,11 @@ int gcd_int(int a, int b) {
 template <int kMode, bool kA>
 pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t workspace_bytes, cudaStream_t st,
                           const char* name) {
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<uint64_t> attr_done{0};
+  once_per_device(attr_done, [] {
     cudaFuncSetAttribute(paged_prefill_attn_kernel<kMode, kA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg<kMode>::kSmem);
-    attr = true;
-  }
+  });
   p.num_reqs = num_reqs;
   if (!workspace) {
     p.persistent = 0;

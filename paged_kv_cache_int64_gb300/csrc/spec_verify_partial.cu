@@ -789,11 +789,10 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   p.rows = (int64_t)num_reqs * T * num_q_heads;
   p.dev_err = dev_err;
   constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<uint64_t> attr_done{0};
+  once_per_device(attr_done, [] {
     cudaFuncSetAttribute(spec_verify_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    attr = true;
-  }
+  });
   dim3 grid((unsigned)(max_splits * n_tg), (unsigned)num_kv_heads, (unsigned)num_reqs);
   spec_verify_partial_kernel<kFp8><<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
   return check_launch(name);
