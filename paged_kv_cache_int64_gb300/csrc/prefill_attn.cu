@@ -557,7 +557,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         ++s;
         continue;
       }
-      // block id of segment `lane` of tile j: >= 0, -1 past seq_len, -2 out-of-range entry
+      // block id of segment `lane` of the tile with keys [key0, key0 + len): >= 0, -1 past the tile
+      // or seq_len, -2 out-of-range entry
       auto lookup = [&](int key0, int len) -> int {
         const int pos = key0 + lane * G;
         if (lane >= nseg || lane * G >= len || pos >= seq_len) return -1;
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         uint32_t bad;      // segments with a bad table entry
         uint32_t nloaded;  // segments with a valid block
         bool fix;          // rows to zero-fill: a tail past seq_len or a bad segment
-        bool big;          // the 128 keys lie in one valid block: 4 copies of 128 rows per tensor
+        bool big;          // the tile's keys lie in one valid block: 4 copies of 128 rows per tensor
         int blk0, slot0;   // block and first slot of key 0 of the tile
         int key0, len;     // the tile's keys
       };
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         if (lane == 0)
           for (int c = 0; c < 4; ++c) tma_load_4d(tile + c * kChunkBytes, map, mb, c * 64, kvh, t.slot0, t.blk0);
       };
-      // K tile j (CTA tile gk) chunk by chunk as QK_{gk-1} frees it. K rows past seq_len need no
+      // K of the tile t (CTA tile gk) chunk by chunk as QK_{gk-1} frees it. K rows past seq_len need no
       // zero-fill (their scores are masked); rows of a bad segment do, so such a tile goes through
       // the private barrier, is patched, then published.
       auto load_k = [&](int gk, const TileInfo& t) {
