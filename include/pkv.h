@@ -28,8 +28,11 @@
  *     at position p attends keys 0..p (causal).
  *   - head_dim must be 256 (the pages' geometry); other values return PKV_ERR_UNSUPPORTED.
  *   - Ownership: the caller allocates every buffer (caches, tables, scratch, partials, outputs).
- *     The library allocates no device memory and keeps no state beyond a thread-local error
- *     message. All pointers except `stream` are device pointers unless stated otherwise.
+ *     The library never allocates device memory (no cudaMalloc). Its state: a thread-local error
+ *     message, per-device records of kernel attributes already set, and the fixed scratch array of
+ *     pkv_spec_verify_attn_noalloc (part of the library's device image, with its address cached
+ *     per device; see that call for its sharing rules). All pointers except `stream` are device
+ *     pointers unless stated otherwise.
  *   - Streams: every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and returns without synchronising. Results are ready when the stream is.
  *   - Errors: arguments are validated on the host before anything is launched; a failed check
@@ -81,8 +84,21 @@ typedef enum pkv_kv_dtype {
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version of this header (incremented on any signature change). */
-#define PKV_ABI_VERSION 5
+#define PKV_ABI_VERSION 6
 PKV_API int32_t pkv_abi_version(void);
+
+/*
+ * testing_set_wait_limit_ns - a testing hook with no counterpart on the pages: the next attention
+ * kernel launched by the calling host thread (pkv_paged_prefill_attn, pkv_paged_prefill_attn_fp8,
+ * pkv_spec_verify_attn_partial, pkv_spec_verify_attn_partial_fp8) bounds each of its internal
+ * waits by ns nanoseconds instead of the default one second; later launches use the default
+ * again. ns = 0 keeps the default. With a bound far below the time a copy or an MMA takes, the
+ * launch's CTAs give up at their first wait that is not already satisfied: each records
+ * PKV_ERR_TIMEOUT in dev_err, waits (with its own bound) for the copies and MMAs it has in flight,
+ * frees its tensor memory and exits, so the context stays usable; the outputs of that launch are
+ * undefined. This is how the give-up path is tested without a hung kernel.
+ */
+PKV_API void pkv_testing_set_wait_limit_ns(uint64_t ns);
 
 /*
  * kv_int8_stats_quant - per-token-head symmetric int8 quantization of the bf16 K cache
@@ -324,7 +340,8 @@ PKV_API pkv_status pkv_paged_prefill_attn_fp8(const void* q, const uint8_t* k_fp
  * PKV_ERR_INVALID_ARG with a message - use fewer splits (larger split_tokens) or the workspace call.
  * The array is reserved on every GPU that loads the library until the process exits. Its device
  * address is looked up on the first call made on each device (with that device current), so make
- * that first call before any stream capture. All calls on a device share the array and overwrite
+ * that first call before any stream capture; the address is then kept for the life of the process,
+ * so do not cudaDeviceReset a device after calling this on it. All calls on a device share the array and overwrite
  * it; calls that overlap on the GPU race on it. Each call writes every partial it reads.
  * Arguments, layouts and requirements are those of pkv_spec_verify_attn_partial, with out bf16
  * [num_reqs*T][num_q_heads][head_dim] as in pkv_spec_verify_combine.

@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
     "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
     "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write", "pkv_paged_prefill_attn_fp8",
-    "pkv_paged_prefill_workspace_bytes",
+    "pkv_paged_prefill_workspace_bytes", "pkv_testing_set_wait_limit_ns",
 )
 
 library_path = _build.LIB
@@ -52,6 +52,8 @@ def _load():
     i32, i64, f32, vp, sz = C.c_int32, C.c_int64, C.c_float, C.c_void_p, C.c_size_t
     L.pkv_last_error.restype = C.c_char_p
     L.pkv_abi_version.restype = i32
+    L.pkv_testing_set_wait_limit_ns.argtypes = [C.c_uint64]
+    L.pkv_testing_set_wait_limit_ns.restype = None
     L.pkv_kv_int8_stats_quant.argtypes = [vp, i64, i64, i64, i64, vp, i64, i32, vp, vp, i32, i32, i32, i32, i32,
                                           vp, vp, vp, i64, vp, vp]
     L.pkv_kv_fp8_dequant_dense.argtypes = [vp, vp, i64, i64, i64, i64, vp, i64, i32, vp, i32, i32, i32, i32, i32,
@@ -155,6 +157,7 @@ def kv_int8_stats_quant(k_cache, block_table, pos_begin, pos_end, max_tokens, k8
     k8_scale [R][max_ctx][hkv] fp32 for positions [pos_begin[r], pos_end[r]); k16 (optional, fp16, same
     shape as k8) also receives the codes as fp16 values."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_cache)
+    assert k_cache.dtype == torch.bfloat16, "kv_int8_stats_quant reads a bf16 K cache"
     _i32(block_table)
     R = block_table.shape[0]
     assert k8.dtype == torch.int8 and k8.is_contiguous() and k8_scale.dtype == torch.float32
@@ -169,6 +172,7 @@ def kv_fp8_dequant_dense(k_fp8, v_fp8, block_table, seq_lens, k_scale, v_scale, 
     """e4m3 paged K/V (uint8 [nb][bs][hkv][D]) -> dense bf16 [R][max_seq][hkv][D] for pos < seq_lens[r]."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_fp8)
     assert v_fp8.stride() == k_fp8.stride() and v_fp8.shape == k_fp8.shape
+    assert k_fp8.dtype == torch.uint8 and v_fp8.dtype == torch.uint8, "e4m3 caches are uint8 tensors"
     _i32(block_table)
     R = block_table.shape[0]
     assert k_dense.is_contiguous() and v_dense.is_contiguous() and k_dense.dtype == torch.bfloat16
@@ -186,6 +190,8 @@ def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start_l
     kv_int8_stats_quant). workspace: None (one CTA per query tile) or a CUDA byte tensor of
     paged_prefill_workspace_bytes() bytes (persistent grid: full waves, last wave cut into key ranges)."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(v_cache)
+    assert v_cache.dtype == torch.bfloat16 and (k_cache is None or k_cache.dtype == torch.bfloat16), \
+        "paged_prefill_attn reads bf16 caches (e4m3 caches: paged_prefill_attn_fp8)"
     if k_cache is not None:
         assert k_cache.stride() == v_cache.stride() and k_cache.shape == v_cache.shape
     assert q.is_contiguous() and out.is_contiguous() and q.dtype == torch.bfloat16 and out.dtype == torch.bfloat16
@@ -234,6 +240,7 @@ def spec_verify_attn_partial(q, k_cache, v_cache, k_scale, v_scale, block_table,
     """Split-KV verify partials over an int8 cache ([nb][bs][hkv][D]) with fp32 per-token-head
     scales ([nb][bs][hkv]); part_o [S][R*T][Hq][D], part_lse [S][R*T][Hq] fp32."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_cache)
+    assert k_cache.dtype == torch.int8 and v_cache.dtype == torch.int8, "int8 caches"
     assert v_cache.stride() == k_cache.stride() and k_scale.stride() == v_scale.stride()
     assert k_scale.dim() == 3 and k_scale.stride(2) == 1
     _i32(block_table)
@@ -253,6 +260,7 @@ def spec_verify_attn_partial_fp8(q, k_fp8, v_fp8, k_descale, v_descale, block_ta
     v_descale: device fp32 scalars."""
     nb, bs, hkv, d, sb, st, sh = _cache_strides(k_fp8)
     assert v_fp8.stride() == k_fp8.stride()
+    assert k_fp8.dtype == torch.uint8 and v_fp8.dtype == torch.uint8, "e4m3 caches are uint8 tensors"
     _i32(block_table)
     R = block_table.shape[0]
     _check(lib.pkv_spec_verify_attn_partial_fp8(_ptr(q), _ptr(k_fp8), _ptr(v_fp8), _ptr(k_descale),

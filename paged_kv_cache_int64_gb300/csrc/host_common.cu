@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "host_common.h"
+#include "sm103.cuh"
 
 namespace pkv {
 
@@ -80,7 +81,16 @@ int num_sms() {
   return n;
 }
 
+static thread_local uint64_t g_next_wait_limit_ns = 0;  // 0: the default
+
+uint64_t take_wait_limit_ns() {
+  const uint64_t v = g_next_wait_limit_ns;
+  g_next_wait_limit_ns = 0;
+  return v ? v : kWaitLimitNs;
+}
+
 }  // namespace pkv
 
 extern "C" const char* pkv_last_error(void) { return pkv::g_last_error; }
+extern "C" void pkv_testing_set_wait_limit_ns(uint64_t ns) { pkv::g_next_wait_limit_ns = ns; }
 extern "C" int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }

@@ -43,6 +43,10 @@ inline void once_per_device(std::atomic<uint64_t>& done, F&& fn) {
 // SM count of the current device (cached per device).
 int num_sms();
 
+// The bound on each wait of the next attention kernel that the calling thread launches: the
+// default (one second) unless pkv_testing_set_wait_limit_ns set another for that one launch.
+uint64_t take_wait_limit_ns();
+
 }  // namespace pkv
 
 #define PKV_REQUIRE(cond, status, ...)   \

@@ -71,6 +71,13 @@ constexpr uint32_t kColS = 256;   // S: 128 fp32 columns (one buffer)
 constexpr uint32_t kColP0 = 384;  // P: two buffers of 64 columns (128 bf16 keys packed in pairs)
 constexpr uint32_t kColP1 = 448;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Units whose first query row sees at most kLoKeys keys take P as two bf16 parts, P = hi + lo with
+// lo = bf16(P - hi), and O += hi V + lo V (16 PV MMAs instead of 8). A bf16 weight alone carries a
+// relative error up to 2^-9; over many keys these errors average out in the output, over a few they
+// do not (rows with a handful of visible keys would miss the output bar by up to 2x). With the
+// remainder the weights are exact to ~2^-17. Only the first query tiles of a prompt's first chunk
+// qualify, so the cost stays there.
+constexpr int kLoKeys = 1024;
 
 // dynamic shared memory layout (1024-byte aligned base)
 constexpr int kOffQ = 0;
@@ -94,6 +101,9 @@ struct Barriers {
   // for, which a parity wait cannot tell apart from the phase itself
   uint64_t p_full[2];   // P_j in TMEM and O rescaled (256 softmax arrivals), tile parity j & 1
   uint64_t pv_done[2];  // PV_j complete (V free, O current), tile parity j & 1
+  uint64_t drain;       // after a wait gave up: every MMA issued so far is complete
+  uint32_t armed[7];    // phases the producer started (TMA or its own arrival): q_full, k_full[0..3],
+                        // v_full, fix - the drain waits for the last one of each
   uint32_t tmem_base;
   int abort;
   float kscale[2][kBN];  // int8: per-key scales of the tile
@@ -153,6 +163,7 @@ struct Params {
   int32_t tpb;
   float tpb_inv;  // 1 / tpb (fast division of tile indices)
   float* ws;         // [num_ctas * kMaxSplit][kSlotFloats]
+  uint64_t wait_limit_ns;  // bound on each wait (kWaitLimitNs unless a test shortens it)
 };
 
 // kMode 0: exact QK (bf16 K from the pool); 1: int8 QK with K widened from the int8 scratch by
@@ -167,6 +178,14 @@ struct Cfg {
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// The same exp2 instruction as ex2_approx (so the same result bit for bit), marked volatile so that
+// the compiler recomputes it instead of keeping 64 earlier results alive across a wait.
+__device__ __forceinline__ float ex2_again(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Quantize this thread's Q row (row i of the swizzled bf16 Q tile) in place to fp16 integers and
@@ -248,6 +267,7 @@ __device__ __forceinline__ void zero_rows(uint8_t* tile, int n_valid, uint32_t b
 // A unit of work: 128 query rows (m-tile mt) of query head qh of request r.
 struct Unit {
   int r, qh, mt, kvh, seq_len, rows_valid, p0, n_tiles, tok0;
+  bool lo;  // P as two bf16 parts (p0 < kLoKeys)
 };
 
 // Key tiles. With p.tpb == 0 tile t is keys [128 t, 128 t + 128). Otherwise tiles follow the blocks:
@@ -330,6 +350,7 @@ __device__ __forceinline__ bool make_unit(const Params& p, int r, int mt, int qh
   const int kv_end = min(seq_len, u.p0 + u.rows_valid);  // keys [0, kv_end)
   u.n_tiles = tiles_for<kA>(p, kv_end);
   u.tok0 = q0 + mt * kBM;
+  u.lo = u.p0 < kLoKeys;
   return true;
 }
 
@@ -491,6 +512,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     }
     mbar_init(&bar.v_full, kFused ? 128 : 1);
     mbar_init(&bar.fix, 1);
+    mbar_init(&bar.drain, 1);
+    for (int b = 0; b < 7; ++b) bar.armed[b] = 0;
     mbar_init(&bar.s_full, 1);
     mbar_init(&bar.s_free, 256);
     for (int b = 0; b < 2; ++b) {
@@ -509,6 +532,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
+  const uint64_t wl = p.wait_limit_ns;
   if (p.persistent && blockIdx.x == 0 && threadIdx.x == 96) {  // warp 3: the merge header's schedule
     const Schedule sc = make_schedule<kA>(p);
     int* hdr = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
@@ -540,18 +564,17 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     Seg sg;
     int g = 0, s = 0;
     uint32_t fix_phase = 0;
-    while (!*abort && it.next(sg)) {
+    while (!warp_aborted(abort) && it.next(sg)) {
       const Unit& u = sg.u;
       const int r = u.r, kvh = u.kvh, seq_len = u.seq_len;
       // Q of this segment's unit, once the previous segment's last QK has read the old one
       if (lane == 0) {
-        if (s == 0 || mbar_wait(&bar.q_empty, (s - 1) & 1, abort)) {
-          mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
+        if (s == 0 || mbar_wait(&bar.q_empty, (s - 1) & 1, abort, wl)) {
+          mbar_arm_tx(&bar.q_full, kTileBytes, &bar.armed[0]);
           for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, u.qh, u.tok0);
         }
       }
-      __syncwarp();
-      if (*abort) break;
+      if (warp_aborted(abort)) break;
       if (kFused) {  // K and V come from the converter warps
         g += sg.t1 - sg.t0;
         ++s;
@@ -613,8 +636,8 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           if (lane == 0) {
             const int row = (int)((int64_t)r * p.max_ctx + key0);
             for (int c = 0; c < 4; ++c) {
-              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
-              mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl)) break;
+              mbar_arm_tx(&bar.k_full[c], (uint32_t)kChunkBytes, &bar.armed[1 + c]);
               tma_load_3d(sK + c * kChunkBytes, &p.k16map, &bar.k_full[c], c * 64, kvh, row);
             }
           }
@@ -622,31 +645,37 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           return;
         }
         if (t.bad) {
+          // the copies follow their arming whatever happens meanwhile (the drain waits for them)
+          bool armed = false;
           if (lane == 0) {
-            for (int c = 0; c < 4 && gk > 0; ++c)
-              if (!mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
-            if (!*abort) mbar_arrive_expect_tx(&bar.fix, 4u * t.nloaded * seg_bytes);
+            bool ok = true;
+            for (int c = 0; c < 4 && gk > 0 && ok; ++c) ok = mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
+            if (ok && !*abort) {
+              mbar_arm_tx(&bar.fix, 4u * t.nloaded * seg_bytes, &bar.armed[6]);
+              armed = true;
+            }
           }
-          __syncwarp();
-          if (*abort) return;
+          if (!__shfl_sync(0xffffffffu, armed, 0)) return;
           if (t.blk >= 0) issue_seg(sK, &p.kmap, &bar.fix, t.blk, key0);
-          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
           ++fix_phase;
-          __syncwarp();
-          if (*abort) return;
+          if (warp_aborted(abort)) return;
           zero_rows(sK, kBN, t.bad, G, lane);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0)
-            for (int c = 0; c < 4; ++c) mbar_arrive(&bar.k_full[c]);
+            for (int c = 0; c < 4; ++c) {
+              mbar_arrive(&bar.k_full[c]);
+              ++bar.armed[1 + c];  // as for V: counted for the drain's parity
+            }
           __syncwarp();
           return;
         }
         if (t.big) {
           if (lane == 0) {
             for (int c = 0; c < 4; ++c) {
-              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort)) break;
-              mbar_arrive_expect_tx(&bar.k_full[c], (uint32_t)kChunkBytes);
+              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl)) break;
+              mbar_arm_tx(&bar.k_full[c], (uint32_t)kChunkBytes, &bar.armed[1 + c]);
               tma_load_4d(sK + c * kChunkBytes, &p.kmap_big, &bar.k_full[c], c * 64, kvh, t.slot0, t.blk0);
             }
           }
@@ -655,12 +684,12 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
         const int slot = (key0 + lane * G) % p.block_size;
         for (int c = 0; c < 4; ++c) {
-          if (lane == 0) {
-            if (gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort))
-              mbar_arrive_expect_tx(&bar.k_full[c], t.nloaded * seg_bytes);
+          bool armed = false;
+          if (lane == 0 && (gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl))) {
+            mbar_arm_tx(&bar.k_full[c], t.nloaded * seg_bytes, &bar.armed[1 + c]);
+            armed = true;
           }
-          __syncwarp();
-          if (*abort) return;
+          if (!__shfl_sync(0xffffffffu, armed, 0)) return;  // the copies follow their arming
           if (t.blk >= 0)
             tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
         }
@@ -670,38 +699,38 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       tile_advance<kA>(p, nc);
       TileInfo nxt = info(nc, sg.t0 + 1 < sg.t1);
       load_k(g, cur);
-      for (int j = sg.t0; j < sg.t1 && !*abort; ++j, ++g) {
+      for (int j = sg.t0; j < sg.t1 && !warp_aborted(abort); ++j, ++g) {
         const int key0 = cur.key0;
         const int n_valid = min(cur.len, seq_len - key0);
         if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
         // K of the next tile first: it streams in while QK_g runs (it waits only for QK_g)
         if (j + 1 < sg.t1) load_k(g + 1, nxt);
-        __syncwarp();
-        if (*abort) break;
+        if (warp_aborted(abort)) break;
         // V of tile g once PV_{g-1} has released the V tile
-        if (lane == 0 && g > 0) mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort);
-        __syncwarp();
-        if (*abort) break;
+        if (lane == 0 && g > 0) mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl);
+        if (warp_aborted(abort)) break;
         if (!cur.fix) {
-          if (lane == 0) mbar_arrive_expect_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
+          if (lane == 0) mbar_arm_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes, &bar.armed[5]);
           __syncwarp();
           if (cur.big) issue_big(sV, &p.vmap_big, &bar.v_full, cur);
           else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.v_full, cur.blk, key0);
         } else {
           // V rows past seq_len or in a bad segment must be zero (P is 0 there, but 0 * NaN is not):
           // load through the private barrier, zero those rows, then publish.
-          if (lane == 0) mbar_arrive_expect_tx(&bar.fix, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes);
+          if (lane == 0) mbar_arm_tx(&bar.fix, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes, &bar.armed[6]);
           __syncwarp();
           if (cur.big) issue_big(sV, &p.vmap_big, &bar.fix, cur);
           else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
-          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort);
+          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
           ++fix_phase;
-          __syncwarp();
-          if (*abort) break;
+          if (warp_aborted(abort)) break;
           zero_rows(sV, n_valid, cur.bad, G, lane);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar.v_full);
+          if (lane == 0) {
+            mbar_arrive(&bar.v_full);
+            ++bar.armed[5];  // a phase the producer completed itself: counted for the drain's parity
+          }
         }
         __syncwarp();
         cur = nxt;
@@ -717,16 +746,20 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       constexpr uint32_t id_pv = idesc_f16(128, 256, true, false, true);
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV);
       // PV of CTA tile i; `first`: the first tile of segment si (O starts from zero once the
-      // previous segment's epilogue has read it)
-      auto issue_pv = [&](int i, bool first, int si) -> bool {
-        if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort)) return false;
-        if (!mbar_wait(&bar.v_full, i & 1, abort)) return false;
-        if (first && si > 0 && !mbar_wait(&bar.o_free, (si - 1) & 1, abort)) return false;
+      // previous segment's epilogue has read it); `lo`: P is in two parts, hi in the first P buffer
+      // and the remainder in the second, both multiplied into O
+      auto issue_pv = [&](int i, bool first, int si, bool lo) -> bool {
+        if (!mbar_wait(&bar.p_full[i & 1], (i >> 1) & 1, abort, wl)) return false;
+        if (!mbar_wait(&bar.v_full, i & 1, abort, wl)) return false;
+        if (first && si > 0 && !mbar_wait(&bar.o_free, (si - 1) & 1, abort, wl)) return false;
         tc_fence_after();
-        const uint32_t a = tmem + ((i & 1) ? kColP1 : kColP0);
+        const uint32_t a = tmem + ((lo || !(i & 1)) ? kColP0 : kColP1);
         for (int ks = 0; ks < 8; ++ks)
           umma_f16_ts(tmem + kColO, a + ks * 8, smem_desc(v_base + ks * 2048, 16384, 1024), id_pv,
                       (!first || ks > 0) ? 1u : 0u);
+        if (lo)
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ts(tmem + kColO, tmem + kColP1 + ks * 8, smem_desc(v_base + ks * 2048, 16384, 1024), id_pv, 1u);
         umma_commit(&bar.pv_done[i & 1]);
         return true;
       };
@@ -737,18 +770,19 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       int pend = -1;            // CTA tile of the PV not yet issued
       bool pend_first = false;  // ... the first tile of its segment
       int pend_seg = 0;         // ... in segment pend_seg
+      bool pend_lo = false;     // ... of a unit with two-part P
       while (ok && it.next(sg)) {
-        if (!mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, s & 1, abort)) break;
+        if (!mbar_wait(kInt8 ? &bar.q_ready : &bar.q_full, s & 1, abort, wl)) break;
         for (int j = sg.t0; ok && j < sg.t1; ++j, ++g) {
           // S is single-buffered: QK_g overwrites it once both softmax halves hold S_{g-1} in
           // registers (PV_{g-2}, queued before QK_g, keeps the tensor pipe busy meanwhile)
-          if (g >= 1 && !mbar_wait(&bar.s_free, (g - 1) & 1, abort)) {
+          if (g >= 1 && !mbar_wait(&bar.s_free, (g - 1) & 1, abort, wl)) {
             ok = false;
             break;
           }
           const uint32_t dS = tmem + kColS;
           for (int c = 0; c < 4; ++c) {
-            if (!mbar_wait(&bar.k_full[c], g & 1, abort)) {
+            if (!mbar_wait(&bar.k_full[c], g & 1, abort, wl)) {
               ok = false;
               break;
             }
@@ -763,20 +797,21 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           if (!ok) break;
           umma_commit(&bar.s_full);
           if (j + 1 == sg.t1) umma_commit(&bar.q_empty);  // the segment's last read of Q
-          if (pend >= 0 && !issue_pv(pend, pend_first, pend_seg)) ok = false;
+          if (pend >= 0 && !issue_pv(pend, pend_first, pend_seg, pend_lo)) ok = false;
           pend = g;
           pend_first = j == sg.t0;
           pend_seg = s;
+          pend_lo = sg.u.lo;
         }
         // int8: the softmax quantizes the next segment's Q only after this segment's epilogue, which
         // waits for its last PV - so that PV cannot wait for the next segment's first QK
         if (kInt8 && ok && pend >= 0) {
-          ok = issue_pv(pend, pend_first, pend_seg);
+          ok = issue_pv(pend, pend_first, pend_seg, pend_lo);
           pend = -1;
         }
         ++s;
       }
-      if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg);
+      if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg, pend_lo);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -803,7 +838,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         // barrier (it never waits for q_full: with a one-tile segment the next segment's Q may land
         // before half 1 gets here, and a parity wait would then miss the phase)
         if (h == 0) {
-          if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, s & 1, abort));
+          if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.q_full, s & 1, abort, wl));
           if (!dead) {
             bar.qscale[i] = quantize_q_row_inplace(sQ, i);
             fence_proxy_async_smem();
@@ -836,7 +871,14 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
             ks_next = key_scale(nc);
           }
         }
-        if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, g & 1, abort));
+        if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(&bar.s_full, g & 1, abort, wl));
+        // A two-part P takes both P buffers, which PV_{g-1} reads: such a unit waits for PV_{g-1}
+        // (and so for every earlier PV) before it reads S, so that the two parts are stored as soon
+        // as they are computed. The units before and after meet it only through its epilogue,
+        // which waits for its last PV, so this wait never reaches across units.
+        const bool lo = u.lo;
+        if (lo && !dead && g >= 1)
+          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl));
         const uint32_t sb = tmem + lane_off + kColS;
         const uint32_t pb = tmem + lane_off + ((g & 1) ? kColP1 : kColP0);
         uint32_t sv[64];
@@ -886,29 +928,57 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
         const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
         // P = exp2(s*sc - m) packed to bf16 pairs; the row sum uses the rounded weights that the PV
-        // MMA multiplies, so the result is a convex combination of V rows
+        // MMA multiplies, so the result is a convex combination of V rows. remainder: the second part
+        // bf16(P - hi) of a two-part P, from hi in pk (the exp2 recomputed, bit for bit)
+        // pairs e0 .. e0 + n - 1 (keys 2e, 2e + 1 of this half) into pk[0 .. n)
+        auto pack_p = [&](uint32_t* pk, int e0, int n, bool remainder) -> float {
+          float sum = 0.0f;
+#pragma unroll
+          for (int k = 0; k < n; ++k) {
+            const int e = e0 + k;
+            float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
+            if (need_mask && 2 * e > lim) s0 = -INFINITY;
+            if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
+            if (remainder) {
+              const float x0 = ex2_again(fmaf(s0, sc, -m_use)), x1 = ex2_again(fmaf(s1, sc, -m_use));
+              pk[k] = pack_bf16x2(x0 - __uint_as_float(pk[k] << 16), x1 - __uint_as_float(pk[k] & 0xffff0000u));
+            } else {
+              const float x0 = ex2_approx(fmaf(s0, sc, -m_use)), x1 = ex2_approx(fmaf(s1, sc, -m_use));
+              pk[k] = pack_bf16x2(x0, x1);
+            }
+            sum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
+          }
+          return sum;
+        };
         uint32_t pk[32];
         float lsum = 0.0f;
+        if (lo) {
+          // every PV is done (waited above): both parts go to tensor memory as they are computed,
+          // 16 words at a time so that the scores of the other half can die meanwhile
+          if (!dead) {
+            tc_fence_after();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
-          if (need_mask && 2 * e > lim) s0 = -INFINITY;
-          if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
-          const float e0 = ex2_approx(fmaf(s0, sc, -m_use)), e1 = ex2_approx(fmaf(s1, sc, -m_use));
-          pk[e] = pack_bf16x2(e0, e1);
-          lsum += __uint_as_float(pk[e] << 16) + __uint_as_float(pk[e] & 0xffff0000u);
+            for (int part = 0; part < 4; ++part) {
+              uint32_t (&q)[8] = *reinterpret_cast<uint32_t(*)[8]>(&pk[8 * part]);
+              lsum += pack_p(q, 8 * part, 8, false);
+              tmem_st_32x32b_x8(tmem + lane_off + kColP0 + 32 * h + 8 * part, q);  // hi
+              lsum += pack_p(q, 8 * part, 8, true);
+              tmem_st_32x32b_x8(tmem + lane_off + kColP1 + 32 * h + 8 * part, q);  // remainder
+            }
+          }
+        } else {
+          lsum = pack_p(pk, 0, 32, false);
         }
-        l_run += lsum;
         // P buffer g%2 was last read by PV_{g-2}; O may be rescaled only once PV_{g-1} is done
         // (never needed on a segment's first tile: the running max starts there)
-        if (!dead && g >= 2)
-          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[g & 1], ((g - 2) >> 1) & 1, abort));
+        if (!dead && g >= 2 && !lo)
+          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[g & 1], ((g - 2) >> 1) & 1, abort, wl));
         const bool need_o = __any_sync(0xffffffffu, rescale);
-        if (!dead && need_o && g >= 1)
-          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort));
+        if (!dead && need_o && g >= 1 && !lo)
+          dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl));
         if (!dead) {
           tc_fence_after();
-          tmem_st_32x32b_x32(pb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
+          if (!lo) tmem_st_32x32b_x32(pb + 32 * h, pk);  // P columns 32h..32h+31 = keys 64h..64h+63
           if (need_o) {
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
@@ -925,11 +995,12 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           tc_fence_before();
           mbar_arrive(&bar.p_full[g & 1]);
         }
+        l_run += lsum;
       }
       // epilogue: the segment's last PV done, then O / l - bf16 output rows for a whole unit, or
       // the normalised fp32 partial and its log-sum-exp for a unit cut between CTAs
       const int gl = g - 1;  // the segment's last CTA tile
-      bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[gl & 1], (gl >> 1) & 1, abort);
+      bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[gl & 1], (gl >> 1) & 1, abort, wl);
       fin = __all_sync(0xffffffffu, fin);
       bar.lsum[h][i] = l_run;
       named_bar_sync(1, 256);
@@ -1039,7 +1110,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       for (int j = sg.t0; j < sg.t1 && ok; ++j, ++g) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // unrolled: raw[] stays in registers
-          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort)) {
+          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort, wl)) {
             ok = false;
             break;
           }
@@ -1049,7 +1120,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
         if (!ok) break;
         load_row(row_src(p.v_fp8, tc));
-        if (g > 0 && !mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) {
+        if (g > 0 && !mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl)) {
           ok = false;
           break;
         }
@@ -1088,7 +1159,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort)) {
+          if (g > 0 && !mbar_wait(&bar.k_empty[c], (g - 1) & 1, abort, wl)) {
             ok = false;
             break;
           }
@@ -1108,12 +1179,30 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // every role has left its loop; the flag's final value, the same for every thread (a thread that
+  // set it reads it set, so the OR over the CTA sees it)
+  const bool gave_up = __syncthreads_or(*abort != 0);
+  if (gave_up) {
+    // some wait gave up: before the tensor memory is freed and the CTA exits, wait for what this
+    // CTA still has in flight - the TMA copies of every phase it armed and every MMA it issued
+    if (warp == 0 && lane == 0) {
+      drain_armed(&bar.q_full, bar.armed[0]);
+      for (int c = 0; c < 4; ++c) drain_armed(&bar.k_full[c], bar.armed[1 + c]);
+      drain_armed(&bar.v_full, bar.armed[5]);
+      drain_armed(&bar.fix, bar.armed[6]);
+    }
+    if (warp == 1 && lane == 0) {
+      umma_commit(&bar.drain);  // arrives once every MMA this thread issued is complete
+      mbar_wait_drain(&bar.drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0 && bar.abort) record_error(p.dev_err, kErrTimeout);
+  if (threadIdx.x == 0 && gave_up) record_error(p.dev_err, kErrTimeout);
 }
 
 
@@ -1224,6 +1313,7 @@ pkv_status launch_prefill(Params& p, int32_t num_reqs, void* workspace, int64_t 
                          Cfg<kMode>::kSmem);
   });
   p.num_reqs = num_reqs;
+  p.wait_limit_ns = take_wait_limit_ns();
   if (!workspace) {
     p.persistent = 0;
     dim3 grid((unsigned)p.n_mtiles, (unsigned)p.num_q_heads, (unsigned)num_reqs);

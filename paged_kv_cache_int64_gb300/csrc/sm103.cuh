@@ -16,8 +16,12 @@ namespace pkv {
 constexpr int kErrDeviceBounds = 4;  // a block id or position outside its declared range
 constexpr int kErrTimeout = 5;       // a bounded wait gave up
 
-// Upper bound on any single wait inside a kernel. A healthy wait ends in microseconds.
+// Upper bound on any single wait inside a kernel. A healthy wait ends in microseconds. A launch
+// may pass a shorter limit (a test of the give-up path); every wait takes the limit as an argument.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Upper bound on each wait of the drain that a CTA runs after some wait gave up: for the TMA copies
+// it issued and the MMAs it launched, which complete in microseconds once issued.
+constexpr uint64_t kDrainLimitNs = 100ull * 1000ull * 1000ull;  // 100 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -77,9 +81,9 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after kWaitLimitNs, or as soon
-// as another thread of the CTA has given up (*abort != 0); returns false then and sets *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Wait for the phase with the given parity to complete. Gives up after limit_ns, or as soon as
+// another thread of the CTA has given up (*abort != 0); returns false then and sets *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -87,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
@@ -96,7 +100,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // mbar_wait for warps that wait long and whose wake-up latency matters less than the issue slots
 // their polling would take from the computing warps (the verify kernel's roles).
-__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -104,11 +109,39 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_suspend(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
   }
+}
+
+// The CTA's abort flag as one value for the whole warp (a vote). A warp must never branch on its
+// lanes' own reads of the flag: another warp may set it between those reads, the lanes then take
+// different paths, and the ones left behind wait forever at the warp's next shuffle or __syncwarp
+// for lanes that have gone on to the CTA's final barrier.
+__device__ __forceinline__ bool warp_aborted(volatile int* abort) { return __any_sync(0xffffffffu, *abort != 0); }
+
+// The drain's wait: the same test, bounded by kDrainLimitNs, blind to the abort flag (it runs
+// after the CTA has given up).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
+  return true;
+}
+
+// Arms a TMA phase of `bar` for `bytes` and counts it in *armed (the count of phases started on
+// the barrier, including any the producer completes by a plain arrival, which it counts itself),
+// so that a CTA that gives up can wait for the last phase started - the copies it issued - before
+// it exits. Such a barrier has at most one started phase not yet complete: a phase is started only
+// after its consumer has released the previous one, which it does after that phase completed.
+__device__ __forceinline__ void mbar_arm_tx(uint64_t* bar, uint32_t bytes, uint32_t* armed) {
+  mbar_arrive_expect_tx(bar, bytes);
+  ++*armed;
+}
+__device__ __forceinline__ void drain_armed(uint64_t* bar, uint32_t armed) {
+  if (armed) mbar_wait_drain(bar, (armed - 1) & 1);
 }
 
 // ------------------------------------------------------------------------------------------

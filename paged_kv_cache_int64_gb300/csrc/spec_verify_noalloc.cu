@@ -12,10 +12,12 @@
 // the process exits. Host code cannot use its name as a device address (on the host it is only a
 // stand-in), so the address is looked up once per device with cudaGetSymbolAddress, with that
 // device current, on the first call made on it. That first call should therefore come before any
-// stream capture. Every call on a device shares the one array and overwrites what the last call
-// left there; calls that overlap on the GPU (different streams, no ordering between them) race on
-// it. Each call writes every partial it reads (splits past a request's keys are neither written
-// nor read), so nothing has to start at zero.
+// stream capture. The address stays cached for the life of the process: after a cudaDeviceReset
+// of a device that has made such a call the array may sit elsewhere, so such a device must not be
+// reset while the library is in use. Every call on a device shares the one array and overwrites
+// what the last call left there; calls that overlap on the GPU (different streams, no ordering
+// between them) race on it. Each call writes every partial it reads (splits past a request's keys
+// are neither written nor read), so nothing has to start at zero.
 #include <mutex>
 
 #include "host_common.h"
@@ -70,14 +72,24 @@ extern "C" pkv_status pkv_spec_verify_attn_noalloc(const void* q, const int8_t* 
   if (num_reqs == 0) return PKV_OK;
   PKV_ARG(num_reqs > 0 && T > 0 && num_q_heads > 0 && head_dim > 0 && max_splits > 0,
           "spec_verify_attn_noalloc: bad size argument");
-  // partial outputs first, then the log-sum-exps, each 256-byte aligned inside the array
-  const size_t rows = (size_t)num_reqs * (size_t)T * (size_t)num_q_heads * (size_t)max_splits;
-  const size_t o_floats = (rows * (size_t)head_dim + 63) & ~(size_t)63;
-  const size_t need = o_floats + rows;
-  PKV_ARG(need <= kScratchFloats,
-          "spec_verify_attn_noalloc: partials need %zu bytes (num_reqs*T*num_q_heads*max_splits*(head_dim+1)*4), "
-          "more than the fixed %zu-byte scratch; use fewer splits (larger split_tokens) or the workspace call",
-          need * sizeof(float), kScratchFloats * sizeof(float));
+  // partial outputs first, then the log-sum-exps, each 256-byte aligned inside the array. The row
+  // count is built one factor at a time and checked against the capacity before each product, so
+  // no product can wrap around and slip a huge request past the check.
+  size_t rows = 1;
+  bool fits = true;
+  for (const int32_t f : {num_reqs, T, num_q_heads, max_splits}) {
+    if (rows > kScratchFloats / (size_t)f) {
+      fits = false;
+      break;
+    }
+    rows *= (size_t)f;
+  }
+  fits = fits && rows <= kScratchFloats / ((size_t)head_dim + 1);
+  const size_t o_floats = fits ? (rows * (size_t)head_dim + 63) & ~(size_t)63 : 0;
+  PKV_ARG(fits && o_floats + rows <= kScratchFloats,
+          "spec_verify_attn_noalloc: the partials (num_reqs*T*num_q_heads*max_splits*(head_dim+1)*4 bytes) do not "
+          "fit the fixed %zu-byte scratch; use fewer splits (larger split_tokens) or the workspace call",
+          kScratchFloats * sizeof(float));
   float* scratch = nullptr;
   pkv_status s = scratch_for_current_device(&scratch);
   if (s != PKV_OK) return s;

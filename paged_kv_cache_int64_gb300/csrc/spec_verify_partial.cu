@@ -88,6 +88,8 @@ struct alignas(16) Barriers {
                                       // since the softmax may run a tile ahead of the MMA's wait
   uint64_t pv_done[2];                // PV_j complete (V tile and P^T buffer j%2 free, O^T current),
                                       // one barrier per tile parity (the softmax waits two tiles back)
+  uint64_t drain;                     // after a wait gave up: both issuers' MMAs are complete
+  uint32_t armed[5];                  // TMA phases armed: q_full, kst_full[0..1], vst_full[0..1]
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
@@ -118,6 +120,7 @@ struct Params {
   const float* k_scale;    // int8 cache: per-token-head scales [nb][bs][Hkv], read by the softmax
   const float* v_scale;
   int64_t scale_stride_blk, scale_stride_tok;
+  uint64_t wait_limit_ns;  // bound on each wait (kWaitLimitNs unless a test shortens it)
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -245,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     mbar_init(&bar.p_full[1], (kNQ / kGC) * 128);
     mbar_init(&bar.pv_done[0], 1);
     mbar_init(&bar.pv_done[1], 1);
+    mbar_init(&bar.drain, 2);  // the QK and the PV issuer
+    for (int b = 0; b < 5; ++b) bar.armed[b] = 0;
     bar.abort = 0;
     fence_mbar_init();
   }
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
   volatile int* abort = &bar.abort;
+  const uint64_t wl = p.wait_limit_ns;
   const int G = p.seg;
 
   if (warp == 0 || warp == 3) {
@@ -267,21 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const bool is_k = warp == 0;
     const int nseg = kBN / G;
     if (is_k && lane == 0) {
-      mbar_arrive_expect_tx(&bar.q_full, 4u * 128u * (uint32_t)(p.tpc * p.group));  // the whole box
+      mbar_arm_tx(&bar.q_full, 4u * 128u * (uint32_t)(p.tpc * p.group), &bar.armed[0]);  // the whole box
       for (int c = 0; c < 4; ++c)
         tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T + t_base);
     }
     uint64_t* full = is_k ? bar.kst_full : bar.vst_full;
     uint64_t* freeb = is_k ? bar.kst_free : bar.vst_free;
     uint32_t* badw = is_k ? bar.kbad : bar.vbad;
+    uint32_t* armed = bar.armed + (is_k ? 1 : 3);
     const CUtensorMap* codes = is_k ? &p.k8map : &p.v8map;
     const CUtensorMap* codes_big = is_k ? &p.k8map_big : &p.v8map_big;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
-      if (lane == 0 && j >= 2) mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort);
-      __syncwarp();
-      if (*abort) break;
+      if (lane == 0 && j >= 2) mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort, wl);
+      if (warp_aborted(abort)) break;
       const int key0 = k_begin + j * kBN;
       int blk = -1;
       if (lane < nseg && key0 + lane * G < k_end) {
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         if (bad) record_error(p.dev_err, kErrDeviceBounds);
         badw[st] = bad;
         const uint32_t rows = big ? (uint32_t)kBN : nloaded * (uint32_t)G;
-        mbar_arrive_expect_tx(&full[st], rows * 2u * 128u);
+        mbar_arm_tx(&full[st], rows * 2u * 128u, &armed[st]);  // the copies below always follow
         if (big)
           for (int c = 0; c < 2; ++c)
             tma_load_4d(stage + kStageCodes + c * kChunk8, codes_big, &full[st], c * 128, kvh, slot0, blk0);
@@ -319,11 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_f16(128, kNQ, false, false, false);
       const uint32_t q_base = smem_u32(sQ);
-      bool ok = mbar_wait_suspend(&bar.q_ready, 0, abort);
+      bool ok = mbar_wait_suspend(&bar.q_ready, 0, abort, wl);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait_suspend(&bar.s_free[st], ((j - 2) >> 1) & 1, abort)) break;
-        if (!mbar_wait_suspend(&bar.k_ready[st], (j >> 1) & 1, abort)) break;
+        if (j >= 2 && !mbar_wait_suspend(&bar.s_free[st], ((j - 2) >> 1) & 1, abort, wl)) break;
+        if (!mbar_wait_suspend(&bar.k_ready[st], (j >> 1) & 1, abort, wl)) break;
         tc_fence_after();
         for (int ks = 0; ks < 16; ++ks)
           umma_f16_ts(tmem + col_s(st), tmem + col_k(st) + ks * 8,
@@ -341,11 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
       const uint32_t v_base = smem_u32(sV16), p_base = smem_u32(sP);
       for (int i = 0; i < n_tiles; ++i) {
-        if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort)) break;
+        if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort, wl)) break;
         const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
         bool ok = true;
         for (int hh = 0; hh < 2 && ok; ++hh) {
-          if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort)) {
+          if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort, wl)) {
             ok = false;
             break;
           }
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    bool dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.q_full, 0, abort));
+    bool dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.q_full, 0, abort, wl));
     if (!dead) {  // row k & 31, chunk k >> 5; padding rows (past the CTA's columns) become zeros
       const int row = k & 31, c = k >> 5;
       const bool live_row = row < nq;
@@ -391,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
       const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
-      bool got = mbar_wait_suspend(&bar.kst_full[st], (j >> 1) & 1, abort);
-      if (got && j >= 2) got = mbar_wait_suspend(&bar.k_free[st], ((j >> 1) - 1) & 1, abort);
+      bool got = mbar_wait_suspend(&bar.kst_full[st], (j >> 1) & 1, abort, wl);
+      if (got && j >= 2) got = mbar_wait_suspend(&bar.k_free[st], ((j >> 1) - 1) & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
@@ -427,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
-      bool got = j == 0 || mbar_wait_suspend(&bar.v_free[hv], (j - 1) & 1, abort);
-      if (got) got = mbar_wait_suspend(&bar.vst_full[st], (j >> 1) & 1, abort);
+      bool got = j == 0 || mbar_wait_suspend(&bar.v_free[hv], (j - 1) & 1, abort, wl);
+      if (got) got = mbar_wait_suspend(&bar.vst_full[st], (j >> 1) & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
       const uint8_t* src = vstage + kStageCodes + hv * kChunk8 + k * 128;
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         blk_2 = key_block(j + 3);
         slot_2 = slot_t;
       }
-      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.s_full[st], (j >> 1) & 1, abort));
+      if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.s_full[st], (j >> 1) & 1, abort, wl));
       float s[kGC];
       {
         uint32_t v[kGC];
@@ -574,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const bool any_rescale = __any_sync(0xffffffffu, rescale);  // the same in all four warps
       // P^T buffer j%2 was last read by PV_{j-2}; O^T may be rescaled only once PV_{j-1} is done
       if (!dead && j >= 2)
-        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort));
+        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort, wl));
       if (!dead && any_rescale && j >= 1)
-        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort));
+        dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, wl));
       // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
       // the running column sums and the fp16 P^T stores run as independent batches
       float e[kGC];
@@ -624,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       vs_1 = vs_2;
     }
     // epilogue: column sums, O^T / l, log-sum-exp (each group for its 16 columns)
-    bool fin = !dead && !*abort && mbar_wait_suspend(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort);
+    bool fin = !dead && !*abort && mbar_wait_suspend(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort, wl);
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
@@ -666,12 +672,30 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
   }
 
   tc_fence_before();
-  __syncthreads();
+  // every role has left its loop; the flag's final value, the same for every thread (a thread that
+  // set it reads it set, so the OR over the CTA sees it)
+  const bool gave_up = __syncthreads_or(*abort != 0);
+  if (gave_up) {
+    // some wait gave up: before the tensor memory is freed and the CTA exits, wait for what this
+    // CTA still has in flight - the TMA copies of every phase it armed and every MMA it issued
+    if ((warp == 0 || warp == 3) && lane == 0) {
+      if (warp == 0) drain_armed(&bar.q_full, bar.armed[0]);
+      const int b = warp == 0 ? 1 : 3;
+      drain_armed(warp == 0 ? &bar.kst_full[0] : &bar.vst_full[0], bar.armed[b]);
+      drain_armed(warp == 0 ? &bar.kst_full[1] : &bar.vst_full[1], bar.armed[b + 1]);
+    }
+    if ((warp == 1 || warp == 2) && lane == 0) {
+      umma_commit(&bar.drain);  // arrives once every MMA this thread issued is complete
+      mbar_wait_drain(&bar.drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0 && bar.abort) record_error(p.dev_err, kErrTimeout);
+  if (threadIdx.x == 0 && gave_up) record_error(p.dev_err, kErrTimeout);
 }
 
 int gcd_int(int a, int b) {
@@ -788,6 +812,7 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   p.part_lse = part_lse;
   p.rows = (int64_t)num_reqs * T * num_q_heads;
   p.dev_err = dev_err;
+  p.wait_limit_ns = take_wait_limit_ns();
   constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
   static std::atomic<uint64_t> attr_done{0};
   once_per_device(attr_done, [] {

@@ -57,7 +57,7 @@ def test_library_targets_sm103a(libpath):
 
 
 def test_abi_version(pkv):
-    assert pkv.lib.pkv_abi_version() == 5
+    assert pkv.lib.pkv_abi_version() == 6
 
 
 def test_workspace_bytes(pkv):
@@ -179,3 +179,15 @@ def test_prefill_workspace_bytes(pkv):
     assert pkv.paged_prefill_workspace_bytes(1) == 4 * (128 * 256 + 128) * 4
     assert pkv.paged_prefill_workspace_bytes(152) == 152 * 526336
     assert pkv.paged_prefill_workspace_bytes(0) == 0
+
+
+def test_noalloc_rejects_sizes_whose_product_wraps(pkv):
+    """The allocation-free verify checks its partials' size one factor at a time: factors whose
+    product wraps a 64-bit size around to a small number are rejected before anything launches."""
+    f = pkv.lib.pkv_spec_verify_attn_noalloc
+    big = (1 << 31) - 1
+    for num_reqs, T, hq, splits in ((big, big, big, big), (big, 1, 1, 1), (1, 1, 1, big), (65536, 65536, 65536, 65536)):
+        rc = f(16, 16, 16, 16, 16, 4, 16384, 1024, 256, 64, 4, 16, 1, 1, 16, num_reqs, T, hq, 4, 256, 16, 0.0625,
+               128, splits, 16, None, None)
+        assert rc == pkv.PKV_ERR_INVALID_ARG
+        assert "scratch" in pkv.lib.pkv_last_error().decode()

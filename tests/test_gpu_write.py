@@ -10,6 +10,7 @@ import torch
 import oracle
 import workloads as W
 from _devsetup import DEV, bf16_to_u16, dev_err, u16_to_bf16
+from _parity import TOL_BF16, close
 
 pytestmark = pytest.mark.gpu
 
@@ -149,31 +150,44 @@ def test_cache_write_bad_entry_is_reported_and_skipped(pkv):
     _assert_same(dev, ref, oracle.KV_INT8)
 
 
-@pytest.mark.parametrize("dt", [oracle.KV_BF16, oracle.KV_INT8])
-def test_cache_write_bigpool_top_placement(pkv, dt):
-    """The last 2,048 rows of the 20,000-token request into the 2,600-block pool, blocks 2,577-2,599:
-    element offsets reach 2.34e9 > 2^31. Only the request's 23 blocks are compared (the rest of the
-    4.69 GB pool is checked for untouched poison on the device)."""
-    p = W.bigpool(top=True, q_len=2048)
-    kn, vn = W.new_rows(p, "k"), W.new_rows(p, "v")
+def _write_bigpool(pkv, p, dt, kn, vn):
+    """Write the chunk's rows into fresh poisoned 2,600-block device pools; returns the caches."""
     shape = (p.num_blocks, p.block_size, p.num_kv_heads, p.head_dim)
     poison = POISON[dt]
     if dt == oracle.KV_BF16:
         kc = torch.full(shape, int(np.uint16(poison).view(np.int16)), dtype=torch.int16, device=DEV).view(torch.bfloat16)
     else:
-        kc = torch.full(shape, poison, dtype=torch.int8, device=DEV)
+        kc = torch.full(shape, poison, dtype=TORCH_DT[dt], device=DEV)
     vc = kc.clone()
     ksc = torch.full(shape[:3], -1.0, dtype=torch.float32, device=DEV)
     vsc = ksc.clone()
+    kscale = torch.tensor([0.5], dtype=torch.float32, device=DEV)
+    vscale = torch.tensor([0.75], dtype=torch.float32, device=DEV)
     err = dev_err()
     bt = torch.from_numpy(p.block_table(fill=-1)).to(DEV)
     sl = torch.from_numpy(p.seq_lens).to(DEV)
     qsl = torch.from_numpy(p.query_start_loc).to(DEV)
     pkv.kv_cache_write(_to_dev_rows(kn), _to_dev_rows(vn), bt, sl, qsl, 2048, kc, vc, kv_dtype=dt,
                        k_scale_cache=ksc if dt == oracle.KV_INT8 else None,
-                       v_scale_cache=vsc if dt == oracle.KV_INT8 else None, dev_err=err)
+                       v_scale_cache=vsc if dt == oracle.KV_INT8 else None,
+                       k_scale=kscale if dt == oracle.KV_FP8 else None, v_scale=vscale if dt == oracle.KV_FP8 else None,
+                       dev_err=err)
     torch.cuda.synchronize()
     assert err.item() == 0
+    return kc, vc, ksc, vsc
+
+
+@pytest.mark.parametrize("dt", [oracle.KV_BF16, oracle.KV_INT8, oracle.KV_FP8])
+def test_cache_write_bigpool_top_placement(pkv, dt):
+    """The last 2,048 rows of the 20,000-token request into the 2,600-block pool, blocks 2,577-2,599:
+    element offsets reach 2.34e9 > 2^31. The written blocks equal the oracle's write byte for byte
+    (the oracle writes a pool holding just those blocks) and the same write at blocks 0-22 bit for
+    bit; nothing outside the request's blocks changes."""
+    p = W.bigpool(top=True, q_len=2048)
+    kn, vn = W.new_rows(p, "k"), W.new_rows(p, "v")
+    shape = (p.num_blocks, p.block_size, p.num_kv_heads, p.head_dim)
+    poison = POISON[dt]
+    kc, vc, ksc, vsc = _write_bigpool(pkv, p, dt, kn, vn)
     blocks = np.asarray(p.requests[0].blocks)
     assert blocks.min() >= 2577
     # oracle on a pool holding just those blocks (same slots, block ids remapped to 0..22)
@@ -182,15 +196,25 @@ def test_cache_write_bigpool_top_placement(pkv, dt):
     hk = np.full(hs, poison, dtype=NP_DT[dt])
     hsc = np.full(hs[:3], -1.0, dtype=np.float32)
     rk, rv, rks, rvs, rc = oracle.kv_cache_write(dt, kn, vn, small_bt, p.seq_lens, p.query_start_loc, hk, hk.copy(),
-                                                 hsc, hsc.copy())
+                                                 hsc, hsc.copy(), k_scale=0.5, v_scale=0.75)
     assert rc == 0
     bidx = torch.from_numpy(blocks).to(DEV)
-    _assert_same((kc[bidx], vc[bidx], ksc[bidx], vsc[bidx]), (rk, rv, rks, rvs), dt)
+    top = (kc[bidx], vc[bidx], ksc[bidx], vsc[bidx])
+    _assert_same(top, (rk, rv, rks, rvs), dt)
     # nothing outside the request's blocks was touched: every changed element lies in those blocks
     for c in (kc, vc):
         raw = c.view(torch.int16) if dt == oracle.KV_BF16 else c
         want = int(np.uint16(poison).view(np.int16)) if dt == oracle.KV_BF16 else poison
         assert int((raw != want).sum()) == int((raw[bidx] != want).sum())
+    top = tuple(t.clone() for t in top)
+    del kc, vc, ksc, vsc
+    torch.cuda.empty_cache()
+    # the same rows at the bottom of the pool: the written blocks are identical bit for bit
+    pb = W.bigpool(top=False, q_len=2048)
+    kc, vc, ksc, vsc = _write_bigpool(pkv, pb, dt, kn, vn)
+    bb = torch.from_numpy(np.asarray(pb.requests[0].blocks)).to(DEV)
+    for a, b in zip(top, (kc[bb], vc[bb], ksc[bb], vsc[bb])):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
 
 
 def test_written_int8_cache_feeds_verify(pkv):
@@ -220,5 +244,4 @@ def test_written_int8_cache_feeds_verify(pkv):
     assert err.item() == 0
     rk, rv, rks, rvs = ref
     want = oracle.spec_verify_attn(q, rk, rv, rks, rvs, p.block_table(fill=0), p.seq_lens, T, 16, p.softmax_scale)
-    got = W.bf16_bits_to_f32(bf16_to_u16(out))
-    assert float(np.abs(got - want).max()) <= 2e-3
+    close(bf16_to_u16(out), want, TOL_BF16)

@@ -299,7 +299,8 @@ def verify_batch(seed: int = 5, num_reqs: int = 32, T: int = 8, pool_tokens: int
                  distinct: bool = True, block_size: int = 880, lengths=None, with_kv: bool = True) -> Problem:
     """Speculative-verify batch: cached prefixes lognormal (median 16k, sigma 0.8, clipped to
     4,096..81,920), T query tokens each, int8 per-token-head KV, bs 880. `distinct=False` keeps
-    the literal 480k-token pool (546 blocks) and lets tables wrap (shared blocks)."""
+    the literal 480k-token pool (ceil(480,000 / 880) = 546 blocks) and lets tables wrap (shared
+    blocks)."""
     if lengths is None:
         lengths = lognormal_lengths(seed, num_reqs, 16384.0, 0.8, 4096, 81920)
     seq = [int(L) + T for L in lengths]
@@ -307,7 +308,7 @@ def verify_batch(seed: int = 5, num_reqs: int = 32, T: int = 8, pool_tokens: int
     if distinct:
         nb, placement = need, "permuted"
     else:
-        nb, placement = pool_tokens // block_size, "cyclic"
+        nb, placement = -(-pool_tokens // block_size), "cyclic"  # the blocks holding pool_tokens
     return make_problem("verify", seed=seed, seq_lens=seq, q_lens=[T] * len(seq), num_blocks=nb,
                         block_size=block_size, kv_dtype="int8", placement=placement,
                         softmax_scale=1.0 / 16.0, with_kv=with_kv)
