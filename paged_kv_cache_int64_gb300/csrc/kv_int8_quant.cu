@@ -11,9 +11,11 @@
 // widening each K row once here serves the 64 query tiles that read it.
 //
 // One pass, HBM-bound: 512 B read + 256 B + 4 B written per (token, head) row (+ 512 B with the fp16
-// copy). One warp per row,
-// 16 contiguous bytes per lane (coalesced 512-byte row), the absmax reduced with warp shuffles,
-// four rows in flight per warp.
+// copy). A warp takes four consecutive rows at a time, eight lanes per row: lane l holds elements
+// 32 (l % 8) .. +31 of row l / 8 (four 16-byte loads), the row's absmax is three shuffles among its
+// eight lanes, and the lane stores its 32 codes as two 16-byte words (and their fp16 copy as four);
+// the four rows' scales leave in one store instruction (lanes 0, 8, 16, 24: consecutive floats).
+// Two such quads are in flight per warp (eight 16-byte loads per lane before the first use).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -26,7 +28,8 @@ namespace {
 
 constexpr int kD = 256;
 constexpr int kWarps = 8;
-constexpr int kRowsPerIter = 4;
+constexpr int kQuads = 2;                   // quads of rows in flight per warp
+constexpr int kRowsPerWarpIter = 4 * kQuads;
 
 struct QuantArgs {
   const __nv_bfloat16* k_cache;
@@ -64,48 +67,64 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
   const int r = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int sub = lane >> 3;       // the lane's row within a quad
+  const int part = lane & 7;       // its 32-element part of the row
   const int64_t p0 = __ldg(a.pos_begin + r);
   const int64_t p1 = __ldg(a.pos_end + r);
   const int64_t nrows = (p1 - p0) * a.num_kv_heads;
-  const int64_t stride = (int64_t)gridDim.x * kWarps * kRowsPerIter;
-  for (int64_t base = ((int64_t)blockIdx.x * kWarps + warp) * kRowsPerIter; base < nrows; base += stride) {
-    uint4 raw[kRowsPerIter];
+  const int64_t stride = (int64_t)gridDim.x * kWarps * kRowsPerWarpIter;
+  for (int64_t base = ((int64_t)blockIdx.x * kWarps + warp) * kRowsPerWarpIter; base < nrows; base += stride) {
+    uint4 raw[kQuads][4];
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int64_t row = base + u;
-      raw[u] = make_uint4(0, 0, 0, 0);
+    for (int qd = 0; qd < kQuads; ++qd) {
+      const int64_t row = base + 4 * qd + sub;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) raw[qd][c] = make_uint4(0, 0, 0, 0);
       if (row < nrows) {
         const int64_t pos = p0 + row / a.num_kv_heads;
         const int h = (int)(row % a.num_kv_heads);
         const int64_t off = row_offset(a, r, pos, h);
-        if (off >= 0) raw[u] = __ldg(reinterpret_cast<const uint4*>(a.k_cache + off) + lane);
+        if (off >= 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.k_cache + off) + 4 * part;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) raw[qd][c] = __ldg(src + c);
+        }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const int64_t row = base + u;
-      if (row >= nrows) break;  // warp-uniform
-      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
-      float x[8];
+    for (int qd = 0; qd < kQuads; ++qd) {
+      if (base + 4 * qd >= nrows) break;  // warp-uniform
+      const int64_t row = base + 4 * qd + sub;
+      const bool live_row = row < nrows;
+      float x[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 f = __bfloat1622float2(v2[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
+      for (int c = 0; c < 4; ++c) {
+        const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&raw[qd][c]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(v2[i]);
+          x[8 * c + 2 * i] = f.x;
+          x[8 * c + 2 * i + 1] = f.y;
+        }
       }
       float amax = 0.0f;
-      bool nan = false;
+      int nan = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 32; ++i) {
         nan |= (x[i] != x[i]);
         amax = fmaxf(amax, fabsf(x[i]));
       }
+      // the row's eight lanes: lanes 8s .. 8s + 7
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      nan = __any_sync(0xffffffffu, nan);
+      for (int o = 4; o > 0; o >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+      }
       float scale;
-      uint32_t lo = 0, hi = 0;
-      uint4 wide = make_uint4(0, 0, 0, 0);
+      uint32_t b[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 32 codes, 4 per word
+      uint32_t w[16];                             // 32 fp16 codes, 2 per word
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
       if (nan) {
         scale = __int_as_float(0x7fc00000);  // a NaN row: NaN scale, zero codes
       } else if (amax == 0.0f) {
@@ -113,26 +132,28 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
       } else {
         scale = __fdiv_rn(amax, 127.0f);
         const float inv = __fdiv_rn(127.0f, amax);
-        uint32_t b[8];
-        uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 32; ++i) {
           int c = __float2int_rn(__fmul_rn(x[i], inv));
           c = max(-127, min(127, c));
-          b[i] = (uint32_t)(c & 0xff);
-          const uint32_t hbits = __half_as_ushort(__int2half_rn(c));  // exact: |c| <= 127
-          if (i & 1) w[i >> 1] |= hbits << 16; else w[i >> 1] = hbits;
+          b[i >> 2] |= (uint32_t)(c & 0xff) << (8 * (i & 3));
+          w[i >> 1] |= (uint32_t)__half_as_ushort(__int2half_rn(c)) << (16 * (i & 1));  // exact: |c| <= 127
         }
-        wide = make_uint4(w[0], w[1], w[2], w[3]);
-        lo = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-        hi = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
       }
-      const int64_t pos = p0 + row / a.num_kv_heads;
-      const int h = (int)(row % a.num_kv_heads);
-      const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
-      reinterpret_cast<uint2*>(a.k8 + o * kD)[lane] = make_uint2(lo, hi);
-      if (a.k16) reinterpret_cast<uint4*>(a.k16 + o * kD)[lane] = wide;
-      if (lane == 0) a.k8_scale[o] = scale;
+      if (live_row) {
+        const int64_t pos = p0 + row / a.num_kv_heads;
+        const int h = (int)(row % a.num_kv_heads);
+        const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
+        uint4* d8 = reinterpret_cast<uint4*>(a.k8 + o * kD) + 2 * part;
+        d8[0] = make_uint4(b[0], b[1], b[2], b[3]);
+        d8[1] = make_uint4(b[4], b[5], b[6], b[7]);
+        if (a.k16) {
+          uint4* d16 = reinterpret_cast<uint4*>(a.k16 + o * kD) + 4 * part;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) d16[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        if (part == 0) a.k8_scale[o] = scale;
+      }
     }
   }
 }
@@ -166,7 +187,7 @@ extern "C" pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_b
               block_table, bt_stride, max_blocks, pos_begin, pos_end, block_size, num_kv_heads,
               k8, k8_scale, static_cast<__half*>(k16), max_ctx, dev_err};
   const int64_t rows = (int64_t)max_tokens * num_kv_heads;
-  const int64_t per_cta = (int64_t)kWarps * kRowsPerIter;
+  const int64_t per_cta = (int64_t)kWarps * kRowsPerWarpIter;
   int64_t want = (rows + per_cta - 1) / per_cta;
   int64_t cap = (int64_t)num_sms() * 8;  // 8 resident CTAs of 256 threads per SM
   cap = (cap + num_reqs - 1) / num_reqs;

@@ -479,70 +479,18 @@ struct SegIter {
   }
 };
 
-// kA: key tiles follow the blocks (block_size >= 128, not a multiple of 128, several blocks per
-// request); otherwise plain 128-key tiles
-template <int kMode, bool kA>
-__global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
-    paged_prefill_attn_kernel(const __grid_constant__ Params p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// The roles of one CTA (producer, MMA issuer, softmax, converters). kLoCapable: some unit of this CTA
+// takes P in two parts (its first row sees at most kLoKeys keys); the instantiation without it has
+// none of that code, which would otherwise cost the common path about a fifth of its time.
+template <int kMode, bool kA, bool kLoCapable>
+__device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barriers& bar, uint32_t tmem,
+                                          volatile int* abort, uint64_t wl, int warp, int lane) {
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kMode>::kTiles);
   constexpr bool kInt8 = kMode == 1 || kMode == 2;  // int8 QK (quantized Q, per-key K scales, f16 MMA)
   constexpr bool kConv = kMode == 1;                 // K widened by the converter warps
   constexpr bool kFused = kMode == 3;                // K and V dequantized by the converter warps
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  if (!p.persistent) {  // classic launch: a CTA without rows leaves at once (CTA-uniform)
-    Unit u;
-    if (!make_unit<kA>(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, u)) return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bar.q_full, 1);
-    mbar_init(&bar.q_ready, 128);
-    mbar_init(&bar.q_empty, 1);
-    mbar_init(&bar.o_free, 256);
-    for (int c = 0; c < 4; ++c) {
-      mbar_init(&bar.k_full[c], (kConv || kFused) ? 128 : 1);
-      mbar_init(&bar.k_empty[c], 1);
-    }
-    mbar_init(&bar.v_full, kFused ? 128 : 1);
-    mbar_init(&bar.fix, 1);
-    mbar_init(&bar.drain, 1);
-    for (int b = 0; b < 7; ++b) bar.armed[b] = 0;
-    mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.s_free, 256);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar.p_full[b], 256);
-      mbar_init(&bar.pv_done[b], 1);
-    }
-    bar.abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(&bar.tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bar.tmem_base;
-  volatile int* abort = &bar.abort;
-  const uint64_t wl = p.wait_limit_ns;
-  if (p.persistent && blockIdx.x == 0 && threadIdx.x == 96) {  // warp 3: the merge header's schedule
-    const Schedule sc = make_schedule<kA>(p);
-    int* hdr = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
-    hdr[0] = sc.f * p.num_ctas;
-    hdr[1] = sc.R;
-    hdr[2] = sc.k;
-  }
-  // Barrier phases follow g, the CTA's running tile count over all its segments, and s, its
-  // segment count; positions and masks follow the unit-local tile index j.
-
   if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
     const int G = p.seg;
@@ -560,21 +508,27 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         }
       }
     }
+    // Every go / stop decision of this warp is lane 0's wait result broadcast by one shuffle, so
+    // the lanes never part (once any role gives up, every wait returns false promptly).
+    auto uniform = [&](bool ok0) -> bool { return __shfl_sync(0xffffffffu, ok0, 0); };
     SegIter<kA> it(p);
     Seg sg;
     int g = 0, s = 0;
     uint32_t fix_phase = 0;
-    while (!warp_aborted(abort) && it.next(sg)) {
+    bool go = true;
+    while (go && it.next(sg)) {
       const Unit& u = sg.u;
       const int r = u.r, kvh = u.kvh, seq_len = u.seq_len;
       // Q of this segment's unit, once the previous segment's last QK has read the old one
+      bool ok0 = true;
       if (lane == 0) {
-        if (s == 0 || mbar_wait(&bar.q_empty, (s - 1) & 1, abort, wl)) {
+        ok0 = s == 0 || mbar_wait(&bar.q_empty, (s - 1) & 1, abort, wl);
+        if (ok0) {
           mbar_arm_tx(&bar.q_full, kTileBytes, &bar.armed[0]);
           for (int c = 0; c < 4; ++c) tma_load_3d(sQ + c * kChunkBytes, &p.qmap, &bar.q_full, c * 64, u.qh, u.tok0);
         }
       }
-      if (warp_aborted(abort)) break;
+      if (!uniform(ok0)) break;
       if (kFused) {  // K and V come from the converter warps
         g += sg.t1 - sg.t0;
         ++s;
@@ -629,37 +583,35 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       // K of the tile t (CTA tile gk) chunk by chunk as QK_{gk-1} frees it. K rows past seq_len need no
       // zero-fill (their scores are masked); rows of a bad segment do, so such a tile goes through
       // the private barrier, is patched, then published.
-      auto load_k = [&](int gk, const TileInfo& t) {
+      // returns false (the same in every lane) when a wait gave up
+      auto load_k = [&](int gk, const TileInfo& t) -> bool {
         const int key0 = t.key0;
-        if (kConv) return;  // the converter warps read the int8 K rows themselves
-        if (kMode == 2) {   // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
+        if (kConv) return true;  // the converter warps read the int8 K rows themselves
+        if (kMode == 2) {        // fp16 copy of the int8 codes, dense by position: 4 copies of 128 rows
+          bool ok0 = true;
           if (lane == 0) {
             const int row = (int)((int64_t)r * p.max_ctx + key0);
-            for (int c = 0; c < 4; ++c) {
-              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl)) break;
+            for (int c = 0; c < 4 && ok0; ++c) {
+              ok0 = gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
+              if (!ok0) break;
               mbar_arm_tx(&bar.k_full[c], (uint32_t)kChunkBytes, &bar.armed[1 + c]);
               tma_load_3d(sK + c * kChunkBytes, &p.k16map, &bar.k_full[c], c * 64, kvh, row);
             }
           }
-          __syncwarp();
-          return;
+          return uniform(ok0);
         }
         if (t.bad) {
           // the copies follow their arming whatever happens meanwhile (the drain waits for them)
-          bool armed = false;
+          bool ok0 = true;
           if (lane == 0) {
-            bool ok = true;
-            for (int c = 0; c < 4 && gk > 0 && ok; ++c) ok = mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
-            if (ok && !*abort) {
-              mbar_arm_tx(&bar.fix, 4u * t.nloaded * seg_bytes, &bar.armed[6]);
-              armed = true;
-            }
+            for (int c = 0; c < 4 && gk > 0 && ok0; ++c) ok0 = mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
+            if (ok0) mbar_arm_tx(&bar.fix, 4u * t.nloaded * seg_bytes, &bar.armed[6]);
           }
-          if (!__shfl_sync(0xffffffffu, armed, 0)) return;
+          if (!uniform(ok0)) return false;
           if (t.blk >= 0) issue_seg(sK, &p.kmap, &bar.fix, t.blk, key0);
-          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
+          if (lane == 0) ok0 = mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
           ++fix_phase;
-          if (warp_aborted(abort)) return;
+          if (!uniform(ok0)) return false;
           zero_rows(sK, kBN, t.bad, G, lane);
           fence_proxy_async_smem();
           __syncwarp();
@@ -669,46 +621,48 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
               ++bar.armed[1 + c];  // as for V: counted for the drain's parity
             }
           __syncwarp();
-          return;
+          return true;
         }
         if (t.big) {
+          bool ok0 = true;
           if (lane == 0) {
             for (int c = 0; c < 4; ++c) {
-              if (gk > 0 && !mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl)) break;
+              ok0 = gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
+              if (!ok0) break;
               mbar_arm_tx(&bar.k_full[c], (uint32_t)kChunkBytes, &bar.armed[1 + c]);
               tma_load_4d(sK + c * kChunkBytes, &p.kmap_big, &bar.k_full[c], c * 64, kvh, t.slot0, t.blk0);
             }
           }
-          __syncwarp();
-          return;
+          return uniform(ok0);
         }
         const int slot = (key0 + lane * G) % p.block_size;
         for (int c = 0; c < 4; ++c) {
-          bool armed = false;
-          if (lane == 0 && (gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl))) {
-            mbar_arm_tx(&bar.k_full[c], t.nloaded * seg_bytes, &bar.armed[1 + c]);
-            armed = true;
+          bool ok0 = true;
+          if (lane == 0) {
+            ok0 = gk == 0 || mbar_wait(&bar.k_empty[c], (gk - 1) & 1, abort, wl);
+            if (ok0) mbar_arm_tx(&bar.k_full[c], t.nloaded * seg_bytes, &bar.armed[1 + c]);
           }
-          if (!__shfl_sync(0xffffffffu, armed, 0)) return;  // the copies follow their arming
+          if (!uniform(ok0)) return false;  // the copies follow their arming
           if (t.blk >= 0)
             tma_load_4d(sK + c * kChunkBytes + lane * G * 128, &p.kmap, &bar.k_full[c], c * 64, kvh, slot, t.blk);
         }
+        return true;
       };
       TileCursor nc = tile_cursor<kA>(p, sg.t0);  // the tile `nxt` describes
       TileInfo cur = info(nc, true);
       tile_advance<kA>(p, nc);
       TileInfo nxt = info(nc, sg.t0 + 1 < sg.t1);
-      load_k(g, cur);
-      for (int j = sg.t0; j < sg.t1 && !warp_aborted(abort); ++j, ++g) {
+      go = load_k(g, cur);
+      for (int j = sg.t0; go && j < sg.t1; ++j, ++g) {
         const int key0 = cur.key0;
         const int n_valid = min(cur.len, seq_len - key0);
         if (cur.bad && lane == 0) record_error(p.dev_err, kErrDeviceBounds);
         // K of the next tile first: it streams in while QK_g runs (it waits only for QK_g)
-        if (j + 1 < sg.t1) load_k(g + 1, nxt);
-        if (warp_aborted(abort)) break;
+        if (j + 1 < sg.t1 && !(go = load_k(g + 1, nxt))) break;
         // V of tile g once PV_{g-1} has released the V tile
-        if (lane == 0 && g > 0) mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl);
-        if (warp_aborted(abort)) break;
+        bool ok0 = true;
+        if (lane == 0 && g > 0) ok0 = mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl);
+        if (!(go = uniform(ok0))) break;
         if (!cur.fix) {
           if (lane == 0) mbar_arm_tx(&bar.v_full, cur.big ? (uint32_t)kTileBytes : 4u * cur.nloaded * seg_bytes, &bar.armed[5]);
           __syncwarp();
@@ -721,9 +675,9 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           __syncwarp();
           if (cur.big) issue_big(sV, &p.vmap_big, &bar.fix, cur);
           else if (cur.blk >= 0) issue_seg(sV, &p.vmap, &bar.fix, cur.blk, key0);
-          if (lane == 0) mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
+          if (lane == 0) ok0 = mbar_wait(&bar.fix, fix_phase & 1, abort, wl);
           ++fix_phase;
-          if (warp_aborted(abort)) break;
+          if (!(go = uniform(ok0))) break;
           zero_rows(sV, n_valid, cur.bad, G, lane);
           fence_proxy_async_smem();
           __syncwarp();
@@ -801,7 +755,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
           pend = g;
           pend_first = j == sg.t0;
           pend_seg = s;
-          pend_lo = sg.u.lo;
+          pend_lo = kLoCapable && sg.u.lo;
         }
         // int8: the softmax quantizes the next segment's Q only after this segment's epilogue, which
         // waits for its last PV - so that PV cannot wait for the next segment's first QK
@@ -818,8 +772,10 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
     // ---------------------------------------------------------------------------- softmax
     // Two warpgroups share every row: half h = 0 owns score columns 0-63 and O columns 0-127,
     // half h = 1 columns 64-127 and O columns 128-255. Thread (h, i) owns row i = TMEM lane i.
-    // Both halves meet at named barrier 1 (256 threads) a fixed number of times per tile; a
-    // failed wait never skips a barrier - it only marks the warp dead, so the barriers stay paired.
+    // The two threads of a row (warps q and q + 4, TMEM lane quarter q) meet at named barrier 2 + q
+    // (64 threads) once per tile and once per epilogue; int8 also has each half meet at barrier
+    // 6 + h (128 threads) once per tile to share its keys' scales. A failed wait never skips a
+    // barrier - it only marks the warp dead - so the barriers stay paired.
     const int h = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;
@@ -845,26 +801,29 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
             mbar_arrive(&bar.q_ready);
           }
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(2 + quarter, 64);  // the two threads of row i: half 0 wrote its scale
         if (!dead) sc = p.scale_log2 * bar.qscale[i];
       }
       float m_run = -INFINITY, l_run = 0.0f;
       TileCursor tc = tile_cursor<kA>(p, sg.t0);
-      // int8: the scale of key i of the tile at cursor c (0 past a short tile or seq_len); half 0
-      // loads the next tile's while this one is scored, so the load's latency stays off the path
+      // int8: thread i < 64 of half h loads the scale of key 64h + i of the tile at cursor c (0 past
+      // a short tile or seq_len) - the keys of its own half's columns - one tile ahead, so the load's
+      // latency stays off the path and only the half's own threads meet to share them
+      const bool ks_loader = kInt8 && i < 64;
       auto key_scale = [&](const TileCursor& c) -> float {
-        const int key = c.key0 + i;
-        return (i < c.len && key < u.seq_len)
+        const int col = 64 * h + i;
+        const int key = c.key0 + col;
+        return (col < c.len && key < u.seq_len)
                    ? __ldg(p.k8_scale + ((int64_t)u.r * p.max_ctx + key) * p.num_kv_heads + u.kvh)
                    : 0.0f;
       };
       float ks_next = 0.0f;
-      if (kInt8 && h == 0 && !dead) ks_next = key_scale(tc);
+      if (ks_loader && !dead) ks_next = key_scale(tc);
       for (int j = sg.t0; j < sg.t1; ++j, ++g, tile_advance<kA>(p, tc)) {
         const int key0 = tc.key0, len = tc.len;
         const float* ks = bar.kscale[g & 1] + 64 * h;
-        if (kInt8 && h == 0 && !dead) {
-          bar.kscale[g & 1][i] = ks_next;
+        if (ks_loader && !dead) {
+          bar.kscale[g & 1][64 * h + i] = ks_next;
           if (j + 1 < sg.t1) {
             TileCursor nc = tc;
             tile_advance<kA>(p, nc);
@@ -876,7 +835,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         // (and so for every earlier PV) before it reads S, so that the two parts are stored as soon
         // as they are computed. The units before and after meet it only through its epilogue,
         // which waits for its last PV, so this wait never reaches across units.
-        const bool lo = u.lo;
+        const bool lo = kLoCapable && u.lo;
         if (lo && !dead && g >= 1)
           dead = !__all_sync(0xffffffffu, mbar_wait(&bar.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort, wl));
         const uint32_t sb = tmem + lane_off + kColS;
@@ -899,7 +858,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         const int lim = min(p_i, key0 + len - 1) - key0 - 64 * h;
         const bool need_mask = lim < 63;
         if (kInt8) {  // fold the per-key scales in place: s = S * ks
-          named_bar_sync(1, 256);  // this tile's kscale, written by half 0, is visible
+          named_bar_sync(6 + h, 128);  // this tile's scales of the half's keys, written by the half, are visible
 #pragma unroll
           for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
         }
@@ -913,7 +872,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
         mx *= sc;  // sc > 0 (or NaN for a NaN q row)
         // both halves of a row agree on its maximum through shared memory
         bar.rowmax[g & 1][h][i] = mx;
-        named_bar_sync(1, 256);
+        named_bar_sync(2 + quarter, 64);  // the other thread of row i (same TMEM lane quarter)
         mx = fmaxf(mx, bar.rowmax[g & 1][h ^ 1][i]);
         bool rescale = false;
         float alpha = 1.0f;
@@ -1003,7 +962,7 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       bool fin = !dead && !*abort && mbar_wait(&bar.pv_done[gl & 1], (gl >> 1) & 1, abort, wl);
       fin = __all_sync(0xffffffffu, fin);
       bar.lsum[h][i] = l_run;
-      named_bar_sync(1, 256);
+      named_bar_sync(2 + quarter, 64);
       const float l_tot = l_run + bar.lsum[h ^ 1][i];
       if (fin) {
         tc_fence_after();
@@ -1177,6 +1136,85 @@ __global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
       }
     }
   }
+}
+
+// Whether some unit of the launch may take P in two parts: a request with queries whose chunk starts
+// before position kLoKeys (the same answer in every thread; a few loads per request). Launches of a
+// prompt's later chunks answer no and run the instantiation without that code.
+__device__ bool launch_has_lo_units(const Params& p) {
+  const int n = p.persistent ? p.num_reqs : 1;
+  const int r0 = p.persistent ? 0 : (int)blockIdx.z;
+  for (int r = r0; r < r0 + n; ++r) {
+    const int q_len = __ldg(p.qsl + r + 1) - __ldg(p.qsl + r);
+    if (q_len > 0 && __ldg(p.seq_lens + r) - q_len < kLoKeys) return true;
+  }
+  return false;
+}
+
+// kA: key tiles follow the blocks (block_size >= 128, not a multiple of 128, several blocks per
+// request); otherwise plain 128-key tiles
+template <int kMode, bool kA>
+__global__ void __launch_bounds__(Cfg<kMode>::kThreads, 1)
+    paged_prefill_attn_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg<kMode>::kTiles);
+  constexpr bool kConv = kMode == 1;                 // K widened by the converter warps
+  constexpr bool kFused = kMode == 3;                // K and V dequantized by the converter warps
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (!p.persistent) {  // classic launch: a CTA without rows leaves at once (CTA-uniform)
+    Unit u;
+    if (!make_unit<kA>(p, blockIdx.z, p.n_mtiles - 1 - (int)blockIdx.x, blockIdx.y, u)) return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_ready, 128);
+    mbar_init(&bar.q_empty, 1);
+    mbar_init(&bar.o_free, 256);
+    for (int c = 0; c < 4; ++c) {
+      mbar_init(&bar.k_full[c], (kConv || kFused) ? 128 : 1);
+      mbar_init(&bar.k_empty[c], 1);
+    }
+    mbar_init(&bar.v_full, kFused ? 128 : 1);
+    mbar_init(&bar.fix, 1);
+    mbar_init(&bar.drain, 1);
+    for (int b = 0; b < 7; ++b) bar.armed[b] = 0;
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar.p_full[b], 256);
+      mbar_init(&bar.pv_done[b], 1);
+    }
+    bar.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&bar.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  volatile int* abort = &bar.abort;
+  const uint64_t wl = p.wait_limit_ns;
+  if (p.persistent && blockIdx.x == 0 && threadIdx.x == 96) {  // warp 3: the merge header's schedule
+    const Schedule sc = make_schedule<kA>(p);
+    int* hdr = reinterpret_cast<int*>(p.ws + ((int64_t)p.num_ctas * kMaxSplit - 1) * kSlotFloats);
+    hdr[0] = sc.f * p.num_ctas;
+    hdr[1] = sc.R;
+    hdr[2] = sc.k;
+  }
+  // Barrier phases follow g, the CTA's running tile count over all its segments, and s, its
+  // segment count; positions and masks follow the unit-local tile index j.
+
+  if (launch_has_lo_units(p))
+    cta_roles<kMode, kA, true>(p, smem, bar, tmem, abort, wl, warp, lane);
+  else
+    cta_roles<kMode, kA, false>(p, smem, bar, tmem, abort, wl, warp, lane);
 
   tc_fence_before();
   // every role has left its loop; the flag's final value, the same for every thread (a thread that

@@ -116,11 +116,11 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity
   }
 }
 
-// The CTA's abort flag as one value for the whole warp (a vote). A warp must never branch on its
-// lanes' own reads of the flag: another warp may set it between those reads, the lanes then take
-// different paths, and the ones left behind wait forever at the warp's next shuffle or __syncwarp
-// for lanes that have gone on to the CTA's final barrier.
-__device__ __forceinline__ bool warp_aborted(volatile int* abort) { return __any_sync(0xffffffffu, *abort != 0); }
+// A warp must never branch on its lanes' own reads of the CTA's abort flag: another warp may set it
+// between those reads, the lanes then take different paths, and the ones left behind wait forever
+// at the warp's next shuffle or __syncwarp for lanes that have gone on to the CTA's final barrier.
+// Warps that wait in one lane broadcast that lane's result; warps whose lanes all wait agree by a
+// vote (__all_sync) on their results.
 
 // The drain's wait: the same test, bounded by kDrainLimitNs, blind to the abort flag (it runs
 // after the CTA has given up).

@@ -286,8 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
-      if (lane == 0 && j >= 2) mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort, wl);
-      if (warp_aborted(abort)) break;
+      // go / stop is lane 0's wait result, broadcast, so the lanes never part (once any role gives
+      // up, every wait returns false promptly)
+      bool ok0 = true;
+      if (lane == 0 && j >= 2) ok0 = mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort, wl);
+      if (!__shfl_sync(0xffffffffu, ok0, 0)) break;
       const int key0 = k_begin + j * kBN;
       int blk = -1;
       if (lane < nseg && key0 + lane * G < k_end) {
