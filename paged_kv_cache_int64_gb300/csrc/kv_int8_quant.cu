@@ -63,7 +63,7 @@ __device__ __forceinline__ int64_t row_offset(const QuantArgs& a, int r, int64_t
   return blk * a.stride_blk + (pos % a.block_size) * a.stride_tok + (int64_t)h * a.stride_head;
 }
 
-__global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 4) kv_int8_stats_quant_kernel(const QuantArgs a) {
   const int r = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -96,64 +96,58 @@ __global__ void __launch_bounds__(kWarps * 32) kv_int8_stats_quant_kernel(const 
       if (base + 4 * qd >= nrows) break;  // warp-uniform
       const int64_t row = base + 4 * qd + sub;
       const bool live_row = row < nrows;
-      float x[32];
+      // absmax of the lane's 32 elements on their bit patterns: a bf16 magnitude orders as its low
+      // 15 bits, so a packed 16-bit maximum of (bits & 0x7fff) gives it, and a maximum above 0x7f80
+      // (infinity) means a NaN is present
+      uint32_t mx2 = 0u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t w[4] = {raw[qd][c].x, raw[qd][c].y, raw[qd][c].z, raw[qd][c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx2 = __vmaxu2(mx2, w[e] & 0x7fff7fffu);
+      }
+      uint32_t mx = max(mx2 & 0xffffu, mx2 >> 16);
+      // the row's eight lanes: lanes 8s .. 8s + 7
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const bool nan = mx > 0x7f80u;
+      const float amax = __uint_as_float(mx << 16);
+      const bool live = !nan && amax > 0.0f;
+      const float scale = nan ? __int_as_float(0x7fc00000) : (amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f);
+      const float inv = live ? __fdiv_rn(127.0f, amax) : 0.0f;  // a NaN or all-zero row: zero codes
+      if (!live_row) continue;
+      const int64_t pos = p0 + row / a.num_kv_heads;
+      const int h = (int)(row % a.num_kv_heads);
+      const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
+      uint4* d8 = reinterpret_cast<uint4*>(a.k8 + o * kD) + 2 * part;
+      uint4* d16 = a.k16 ? reinterpret_cast<uint4*>(a.k16 + o * kD) + 4 * part : nullptr;
+      // 8 elements per chunk: their codes (two words) and the codes as fp16 (four words), stored as
+      // soon as a 16-byte word is whole
+      uint32_t b_prev[2] = {0u, 0u};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&raw[qd][c]);
+        uint32_t bw[2] = {0u, 0u}, hw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(v2[i]);
-          x[8 * c + 2 * i] = f.x;
-          x[8 * c + 2 * i + 1] = f.y;
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(v2[e]);
+          int c0 = 0, c1 = 0;
+          if (live) {
+            c0 = max(-127, min(127, __float2int_rn(__fmul_rn(f.x, inv))));
+            c1 = max(-127, min(127, __float2int_rn(__fmul_rn(f.y, inv))));
+          }
+          bw[e >> 1] |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * (e & 1));
+          hw[e] = (uint32_t)__half_as_ushort(__int2half_rn(c0)) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(c1)) << 16);  // exact: |c| <= 127
+        }
+        if (d16) d16[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (c & 1) d8[c >> 1] = make_uint4(b_prev[0], b_prev[1], bw[0], bw[1]);
+        else {
+          b_prev[0] = bw[0];
+          b_prev[1] = bw[1];
         }
       }
-      float amax = 0.0f;
-      int nan = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        nan |= (x[i] != x[i]);
-        amax = fmaxf(amax, fabsf(x[i]));
-      }
-      // the row's eight lanes: lanes 8s .. 8s + 7
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        nan |= __shfl_xor_sync(0xffffffffu, nan, o);
-      }
-      float scale;
-      uint32_t b[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 32 codes, 4 per word
-      uint32_t w[16];                             // 32 fp16 codes, 2 per word
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
-      if (nan) {
-        scale = __int_as_float(0x7fc00000);  // a NaN row: NaN scale, zero codes
-      } else if (amax == 0.0f) {
-        scale = 0.0f;
-      } else {
-        scale = __fdiv_rn(amax, 127.0f);
-        const float inv = __fdiv_rn(127.0f, amax);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          int c = __float2int_rn(__fmul_rn(x[i], inv));
-          c = max(-127, min(127, c));
-          b[i >> 2] |= (uint32_t)(c & 0xff) << (8 * (i & 3));
-          w[i >> 1] |= (uint32_t)__half_as_ushort(__int2half_rn(c)) << (16 * (i & 1));  // exact: |c| <= 127
-        }
-      }
-      if (live_row) {
-        const int64_t pos = p0 + row / a.num_kv_heads;
-        const int h = (int)(row % a.num_kv_heads);
-        const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
-        uint4* d8 = reinterpret_cast<uint4*>(a.k8 + o * kD) + 2 * part;
-        d8[0] = make_uint4(b[0], b[1], b[2], b[3]);
-        d8[1] = make_uint4(b[4], b[5], b[6], b[7]);
-        if (a.k16) {
-          uint4* d16 = reinterpret_cast<uint4*>(a.k16 + o * kD) + 4 * part;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) d16[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-        if (part == 0) a.k8_scale[o] = scale;
-      }
+      if (part == 0) a.k8_scale[o] = scale;
     }
   }
 }
