@@ -5,10 +5,14 @@
 // bf16 scratch holding one block per request (block_size = max_seq, identity block table), so the
 // ordinary bf16 attention runs on it unchanged.
 //
-// One streaming pass, HBM-bound: 1 B read + 2 B written per element for K and for V. Each thread
-// converts 16 e4m3 bytes per step with the hardware conversion (e4m3x2 -> f16x2, exact), widens
-// to fp32, multiplies by the per-tensor scale (fp32, round to nearest) and rounds the product to
-// bf16 (round to nearest even): bit-identical to the definition.
+// One streaming pass, HBM-bound: 1 B read + 2 B written per element for K and for V. One warp per
+// (request, position) at a time: lanes 0-15 take K, lanes 16-31 V, lane q the 16 codes at bytes
+// 16q .. 16q + 15 of every head's row, so each half-warp reads the token's Hkv x 256 codes as
+// coalesced 256-byte rows and writes them as 512-byte bf16 rows. The block id and slot are found
+// once per position; each warp keeps two positions (2 Hkv 16-byte loads a lane) in flight. A code
+// converts with the hardware conversion (e4m3x2 -> f16x2, exact), widens to fp32, is multiplied by
+// the per-tensor scale (fp32, round to nearest) and rounded to bf16 (round to nearest even):
+// bit-identical to the definition.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -20,7 +24,8 @@ namespace pkv {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunksPerThread = 4;  // 16-byte chunks in flight per thread
+constexpr int kMaxHeads = 4;  // kv heads handled per lane step (more heads loop)
+constexpr int kPosPerWarp = 2;
 
 struct DequantArgs {
   const uint8_t* src[2];
@@ -37,51 +42,55 @@ struct DequantArgs {
 
 __global__ void __launch_bounds__(kThreads) kv_fp8_dequant_dense_kernel(const DequantArgs a) {
   const int r = blockIdx.y;
-  const int64_t L = __ldg(a.seq_lens + r);
-  const int chunks_per_row = a.head_dim / 16;                       // 16 codes per chunk
-  const int64_t per_tok = (int64_t)a.num_kv_heads * chunks_per_row;  // chunks per token
-  const int64_t n = 2 * L * per_tok;                                 // K then V
-  const float sk = __ldg(a.scale[0]), sv = __ldg(a.scale[1]);
-  const int64_t stride = (int64_t)gridDim.x * kThreads * kChunksPerThread;
-  for (int64_t base = (int64_t)blockIdx.x * kThreads * kChunksPerThread + threadIdx.x; base < n;
-       base += stride) {
-    uint4 raw[kChunksPerThread];
-    int64_t dsto[kChunksPerThread];
+  const int L = __ldg(a.seq_lens + r);
+  const int lane = threadIdx.x & 31;
+  const int which = lane >> 4;  // 0: K, 1: V
+  const int q = lane & 15;      // 16-byte column chunk of every head's row
+  const uint8_t* src = a.src[which];
+  __nv_bfloat16* dst = a.dst[which];
+  const float sc = __ldg(a.scale[which]);
+  const int H = a.num_kv_heads;
+  const int nw = (int)((gridDim.x * (unsigned)kThreads) >> 5);
+  for (int pos0 = (int)((blockIdx.x * (unsigned)kThreads + threadIdx.x) >> 5); pos0 < L; pos0 += kPosPerWarp * nw) {
+    for (int h0 = 0; h0 < H; h0 += kMaxHeads) {
+      const int nh = min(kMaxHeads, H - h0);
+      uint4 raw[kPosPerWarp][kMaxHeads];
+      bool live[kPosPerWarp];
 #pragma unroll
-    for (int u = 0; u < kChunksPerThread; ++u) {
-      const int64_t i = base + (int64_t)u * kThreads;
-      raw[u] = make_uint4(0, 0, 0, 0);
-      dsto[u] = -1;
-      if (i < n) {
-        const int which = i >= L * per_tok;
-        const int64_t j = which ? i - L * per_tok : i;
-        const int64_t pos = j / per_tok;
-        const int64_t rem = j % per_tok;
-        const int h = (int)(rem / chunks_per_row);
-        const int c = (int)(rem % chunks_per_row);
-        dsto[u] = ((((int64_t)r * a.max_seq + pos) * a.num_kv_heads + h) * a.head_dim + c * 16) |
-                  ((int64_t)which << 62);
-        const int64_t col = pos / a.block_size;
-        const int64_t blk = col < a.max_blocks ? (int64_t)__ldg(a.block_table + (int64_t)r * a.bt_stride + col) : -1;
-        if (blk < 0 || blk >= a.num_blocks) {
-          record_error(a.dev_err, kErrDeviceBounds);
-        } else {
-          const int64_t off = blk * a.stride_blk + (pos % a.block_size) * a.stride_tok +
-                              (int64_t)h * a.stride_head + c * 16;
-          raw[u] = __ldg(reinterpret_cast<const uint4*>(a.src[which] + off));
+      for (int u = 0; u < kPosPerWarp; ++u) {
+        const int pos = pos0 + u * nw;
+        live[u] = pos < L;
+        int64_t base = -1;
+        if (live[u]) {
+          const int col = pos / a.block_size;
+          const int slot = pos - col * a.block_size;
+          const int64_t blk = col < a.max_blocks ? (int64_t)__ldg(a.block_table + (int64_t)r * a.bt_stride + col) : -1;
+          if (blk < 0 || blk >= a.num_blocks) {
+            if (lane == 0) record_error(a.dev_err, kErrDeviceBounds);
+          } else {
+            base = blk * a.stride_blk + (int64_t)slot * a.stride_tok + (int64_t)h0 * a.stride_head + q * 16;
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kMaxHeads; ++t) {
+          raw[u][t] = make_uint4(0, 0, 0, 0);  // a bad block reads as zero codes, written as zeros
+          if (base >= 0 && t < nh) raw[u][t] = __ldg(reinterpret_cast<const uint4*>(src + base + (int64_t)t * a.stride_head));
         }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kChunksPerThread; ++u) {
-      if (dsto[u] < 0) continue;
-      const int which = (int)(dsto[u] >> 62);
-      const int64_t o = dsto[u] & ((1ll << 62) - 1);
-      uint4 hi;
-      const uint4 lo = dequant16_e4m3_bf16(raw[u], which ? sv : sk, hi);
-      uint4* dst = reinterpret_cast<uint4*>(a.dst[which] + o);
-      dst[0] = lo;
-      dst[1] = hi;
+      for (int u = 0; u < kPosPerWarp; ++u) {
+        if (!live[u]) continue;
+        const int64_t row0 = ((int64_t)r * a.max_seq + pos0 + u * nw) * H + h0;
+#pragma unroll
+        for (int t = 0; t < kMaxHeads; ++t) {
+          if (t >= nh) continue;
+          uint4 hi;
+          const uint4 lo = dequant16_e4m3_bf16(raw[u][t], sc, hi);
+          uint4* d = reinterpret_cast<uint4*>(dst + (row0 + t) * a.head_dim + q * 16);
+          d[0] = lo;
+          d[1] = hi;
+        }
+      }
     }
   }
 }
@@ -115,12 +124,11 @@ extern "C" pkv_status pkv_kv_fp8_dequant_dense(const uint8_t* k_fp8, const uint8
                 {k_scale, v_scale},
                 num_blocks, stride_blk, stride_tok, stride_head, block_table, bt_stride, max_blocks, seq_lens,
                 max_seq, block_size, num_kv_heads, head_dim, dev_err};
-  const int64_t chunks = 2ll * max_seq * num_kv_heads * (head_dim / 16);
-  const int64_t per_cta = (int64_t)kThreads * kChunksPerThread;
-  int64_t want = (chunks + per_cta - 1) / per_cta;
-  int64_t cap = ((int64_t)num_sms() * 8 + num_reqs - 1) / num_reqs;
-  if (cap < 1) cap = 1;
-  dim3 grid((unsigned)(want < cap ? want : cap), (unsigned)num_reqs);
+  // one warp per position: a CTA per 8 positions of max_seq (CTAs past a request's seq_len leave at
+  // once; the block scheduler balances the tail). Each warp then takes positions w and w + nw.
+  const int64_t warps_per_cta = kThreads / 32;
+  const int64_t want = ((int64_t)max_seq + kPosPerWarp * warps_per_cta - 1) / (kPosPerWarp * warps_per_cta);
+  dim3 grid((unsigned)want, (unsigned)num_reqs);
   kv_fp8_dequant_dense_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return check_launch("kv_fp8_dequant_dense");
 }

@@ -11,7 +11,9 @@
 // widening each K row once here serves the 64 query tiles that read it.
 //
 // One pass, HBM-bound: 512 B read + 256 B + 4 B written per (token, head) row (+ 512 B with the fp16
-// copy). A warp takes four consecutive rows at a time, eight lanes per row: lane l holds elements
+// copy). CTAs of four warps (so a 2,048-token chunk of four heads spreads over 256 CTAs, past the
+// SM count); row, position and slot arithmetic in 32 bits, once per row. A warp takes four
+// consecutive rows at a time, eight lanes per row: lane l holds elements
 // 32 (l % 8) .. +31 of row l / 8 (four 16-byte loads), the row's absmax is three shuffles among its
 // eight lanes, and the lane stores its 32 codes as two 16-byte words (and their fp16 copy as four);
 // the four rows' scales leave in one store instruction (lanes 0, 8, 16, 24: consecutive floats).
@@ -27,7 +29,7 @@ namespace pkv {
 namespace {
 
 constexpr int kD = 256;
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kQuads = 2;                   // quads of rows in flight per warp
 constexpr int kRowsPerWarpIter = 4 * kQuads;
 
@@ -48,9 +50,10 @@ struct QuantArgs {
 };
 
 // Element offset of K row (request r, position pos, head h), or -1 with an error recorded when
-// the table entry is outside the pool. 64-bit throughout: blk * stride_blk can exceed 2^31.
-__device__ __forceinline__ int64_t row_offset(const QuantArgs& a, int r, int64_t pos, int h) {
-  const int64_t col = pos / a.block_size;
+// the table entry is outside the pool. Positions and rows fit 32 bits (checked on the host), so the
+// divisions are 32-bit; the offset is 64-bit throughout: blk * stride_blk can exceed 2^31.
+__device__ __forceinline__ int64_t row_offset(const QuantArgs& a, int r, int pos, int h) {
+  const int col = pos / a.block_size;
   if (col >= a.max_blocks) {
     record_error(a.dev_err, kErrDeviceBounds);
     return -1;
@@ -60,30 +63,37 @@ __device__ __forceinline__ int64_t row_offset(const QuantArgs& a, int r, int64_t
     record_error(a.dev_err, kErrDeviceBounds);
     return -1;
   }
-  return blk * a.stride_blk + (pos % a.block_size) * a.stride_tok + (int64_t)h * a.stride_head;
+  return blk * a.stride_blk + (int64_t)(pos - col * a.block_size) * a.stride_tok + (int64_t)h * a.stride_head;
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 4) kv_int8_stats_quant_kernel(const QuantArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 8) kv_int8_stats_quant_kernel(const QuantArgs a) {
   const int r = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int sub = lane >> 3;       // the lane's row within a quad
   const int part = lane & 7;       // its 32-element part of the row
-  const int64_t p0 = __ldg(a.pos_begin + r);
-  const int64_t p1 = __ldg(a.pos_end + r);
-  const int64_t nrows = (p1 - p0) * a.num_kv_heads;
-  const int64_t stride = (int64_t)gridDim.x * kWarps * kRowsPerWarpIter;
-  for (int64_t base = ((int64_t)blockIdx.x * kWarps + warp) * kRowsPerWarpIter; base < nrows; base += stride) {
+  const int H = a.num_kv_heads;
+  const int p0 = __ldg(a.pos_begin + r);
+  const int p1 = __ldg(a.pos_end + r);
+  if ((int64_t)(p1 - p0) * H >= (1ll << 31)) {  // rows beyond 32-bit indexing (the host checks max_tokens)
+    if (threadIdx.x == 0) record_error(a.dev_err, kErrDeviceBounds);
+    return;
+  }
+  const int nrows = (p1 - p0) * H;
+  const int stride = (int)gridDim.x * kWarps * kRowsPerWarpIter;
+  for (int base = ((int)blockIdx.x * kWarps + warp) * kRowsPerWarpIter; base < nrows; base += stride) {
     uint4 raw[kQuads][4];
+    int pos_q[kQuads], h_q[kQuads];  // the lane's row of each quad: position and head
 #pragma unroll
     for (int qd = 0; qd < kQuads; ++qd) {
-      const int64_t row = base + 4 * qd + sub;
+      const int row = base + 4 * qd + sub;
+      const int t = row / H;
+      pos_q[qd] = p0 + t;
+      h_q[qd] = row - t * H;
 #pragma unroll
       for (int c = 0; c < 4; ++c) raw[qd][c] = make_uint4(0, 0, 0, 0);
       if (row < nrows) {
-        const int64_t pos = p0 + row / a.num_kv_heads;
-        const int h = (int)(row % a.num_kv_heads);
-        const int64_t off = row_offset(a, r, pos, h);
+        const int64_t off = row_offset(a, r, pos_q[qd], h_q[qd]);
         if (off >= 0) {
           const uint4* src = reinterpret_cast<const uint4*>(a.k_cache + off) + 4 * part;
 #pragma unroll
@@ -94,8 +104,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) kv_int8_stats_quant_kernel(con
 #pragma unroll
     for (int qd = 0; qd < kQuads; ++qd) {
       if (base + 4 * qd >= nrows) break;  // warp-uniform
-      const int64_t row = base + 4 * qd + sub;
-      const bool live_row = row < nrows;
+      const bool live_row = base + 4 * qd + sub < nrows;
       // absmax of the lane's 32 elements on their bit patterns: a bf16 magnitude orders as its low
       // 15 bits, so a packed 16-bit maximum of (bits & 0x7fff) gives it, and a maximum above 0x7f80
       // (infinity) means a NaN is present
@@ -115,10 +124,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) kv_int8_stats_quant_kernel(con
       const bool live = !nan && amax > 0.0f;
       const float scale = nan ? __int_as_float(0x7fc00000) : (amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f);
       const float inv = live ? __fdiv_rn(127.0f, amax) : 0.0f;  // a NaN or all-zero row: zero codes
+      const bool inv_inf = isinf(inv);
       if (!live_row) continue;
-      const int64_t pos = p0 + row / a.num_kv_heads;
-      const int h = (int)(row % a.num_kv_heads);
-      const int64_t o = ((int64_t)r * a.max_ctx + pos) * a.num_kv_heads + h;
+      const int64_t o = ((int64_t)r * a.max_ctx + pos_q[qd]) * H + h_q[qd];
       uint4* d8 = reinterpret_cast<uint4*>(a.k8 + o * kD) + 2 * part;
       uint4* d16 = a.k16 ? reinterpret_cast<uint4*>(a.k16 + o * kD) + 4 * part : nullptr;
       // 8 elements per chunk: their codes (two words) and the codes as fp16 (four words), stored as
@@ -131,10 +139,17 @@ __global__ void __launch_bounds__(kWarps * 32, 4) kv_int8_stats_quant_kernel(con
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __bfloat1622float2(v2[e]);
+          // With inv finite, |x| <= amax and inv = 127 / amax correctly rounded give
+          // |x * inv| <= 127 (1 + 2^-23) < 127.5, so the rounded code is already in [-127, 127] and
+          // the definition's clamp acts only when 127 / amax overflows (amax below ~3.7e-37)
           int c0 = 0, c1 = 0;
           if (live) {
-            c0 = max(-127, min(127, __float2int_rn(__fmul_rn(f.x, inv))));
-            c1 = max(-127, min(127, __float2int_rn(__fmul_rn(f.y, inv))));
+            c0 = __float2int_rn(__fmul_rn(f.x, inv));
+            c1 = __float2int_rn(__fmul_rn(f.y, inv));
+            if (inv_inf) {
+              c0 = max(-127, min(127, c0));
+              c1 = max(-127, min(127, c1));
+            }
           }
           bw[e >> 1] |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * (e & 1));
           hw[e] = (uint32_t)__half_as_ushort(__int2half_rn(c0)) |
@@ -176,6 +191,8 @@ extern "C" pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_b
   PKV_ARG(aligned16(k_cache) && stride_blk % 8 == 0 && stride_tok % 8 == 0 && stride_head % 8 == 0,
           "kv_int8_stats_quant: k_cache rows must be 16-byte aligned");
   PKV_ARG(!k16 || aligned16(k16), "kv_int8_stats_quant: k16 must be 16-byte aligned");
+  PKV_UNSUP((int64_t)max_tokens * num_kv_heads < (1ll << 31) && max_ctx < (1ll << 31),
+            "kv_int8_stats_quant: more than 2^31 rows in one call");
   if (num_reqs == 0 || max_tokens == 0) return PKV_OK;
   QuantArgs a{static_cast<const __nv_bfloat16*>(k_cache), num_blocks, stride_blk, stride_tok, stride_head,
               block_table, bt_stride, max_blocks, pos_begin, pos_end, block_size, num_kv_heads,
@@ -183,9 +200,9 @@ extern "C" pkv_status pkv_kv_int8_stats_quant(const void* k_cache, int64_t num_b
   const int64_t rows = (int64_t)max_tokens * num_kv_heads;
   const int64_t per_cta = (int64_t)kWarps * kRowsPerWarpIter;
   int64_t want = (rows + per_cta - 1) / per_cta;
-  int64_t cap = (int64_t)num_sms() * 8;  // 8 resident CTAs of 256 threads per SM
-  cap = (cap + num_reqs - 1) / num_reqs;
-  if (cap < 1) cap = 1;
+  // one 32-row slice of the range per CTA: the block scheduler balances the tail (the loop
+  // strides only past 2^31 - 1 CTAs)
+  const int64_t cap = (1ll << 31) - 1;
   dim3 grid((unsigned)(want < cap ? want : cap), (unsigned)num_reqs);
   kv_int8_stats_quant_kernel<<<grid, kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return check_launch("kv_int8_stats_quant");

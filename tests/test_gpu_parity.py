@@ -84,6 +84,47 @@ def test_kv_int8_stats_quant_bit_exact(pkv, bs, seqs, begins):
     assert np.array_equal(ks.cpu().numpy().view(np.uint32), rks.view(np.uint32))
 
 
+def test_kv_int8_stats_quant_tiny_rows_bit_exact(pkv):
+    """Rows whose absmax is so small that 127 / absmax overflows to infinity (bf16 subnormals and
+    normals below ~3.7e-37): every nonzero element's product is then infinite and the definition's
+    clamp gives +-127; rows just above that bound, where the quotient stays finite; a normal row.
+    (Zero elements in an overflowing row would multiply 0 by infinity, which the definition leaves
+    undefined; these rows have none.)"""
+    rng = np.random.default_rng(7)
+    bs, H, D = 16, 4, 256
+    rows = []
+    sign = np.where(rng.random(D) < 0.5, -1.0, 1.0).astype(np.float32)
+    rows.append(sign * rng.uniform(1e-38, 3e-37, D).astype(np.float32))            # normals, quotient overflows
+    sub = rng.integers(1, 0x7f, D).astype(np.uint16) | np.where(sign < 0, 0x8000, 0).astype(np.uint16)
+    rows.append(W.bf16_bits_to_f32(sub))                                              # bf16 subnormals
+    mix = sign * np.float32(1e-40)
+    mix[5] = np.float32(3e-37)
+    rows.append(mix.astype(np.float32))                                               # one 3e-37, the rest subnormal
+    rows.append(sign * rng.uniform(1e-37, 5e-37, D).astype(np.float32))              # absmax ~5e-37: finite quotient
+    rows.append(rng.standard_normal(D).astype(np.float32))                            # ordinary
+    n_tok = 2  # 2 tokens x 4 heads = 8 rows; the 5 special rows first, then ordinary ones
+    while len(rows) < n_tok * H:
+        rows.append(rng.standard_normal(D).astype(np.float32))
+    vals = np.stack(rows)
+    bits = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    pool = np.zeros((1, bs, H, D), dtype=np.uint16)
+    pool[0, :n_tok] = bits.reshape(n_tok, H, D)
+    k = torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16).cuda()
+    bt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    pb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pe = torch.full((1,), n_tok, dtype=torch.int32, device="cuda")
+    k8 = torch.zeros((1, n_tok, H, D), dtype=torch.int8, device="cuda")
+    ks = torch.zeros((1, n_tok, H), dtype=torch.float32, device="cuda")
+    err = dev_err()
+    pkv.kv_int8_stats_quant(k, bt, pb, pe, n_tok, k8, ks, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rk8, rks = oracle.kv_int8_stats_quant(pool, np.zeros((1, 1), dtype=np.int32), [0], [n_tok], bs, n_tok)
+    assert (np.abs(rk8[0, 0, :3]) == 127).all()  # the overflowing rows clamp
+    assert np.array_equal(k8.cpu().numpy(), rk8)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), rks.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------------------------
 # A4: fp8 -> dense bf16 - bit exact
 # ---------------------------------------------------------------------------------------------
