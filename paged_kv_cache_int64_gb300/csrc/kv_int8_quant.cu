@@ -130,32 +130,59 @@ __global__ void __launch_bounds__(kWarps * 32, 8) kv_int8_stats_quant_kernel(con
       uint4* d8 = reinterpret_cast<uint4*>(a.k8 + o * kD) + 2 * part;
       uint4* d16 = a.k16 ? reinterpret_cast<uint4*>(a.k16 + o * kD) + 4 * part : nullptr;
       // 8 elements per chunk: their codes (two words) and the codes as fp16 (four words), stored as
-      // soon as a 16-byte word is whole
+      // soon as a 16-byte word is whole.
+      // Rounding. With inv finite and nonzero, |x| <= amax and inv = 127 / amax correctly rounded give
+      // |p| = |x * inv| <= 127 (1 + 2^-23) < 127.5: rint(p) is already in [-127, 127] (the definition's
+      // clamp never acts), and adding 1.5 * 2^23 to p (one correctly rounded add; |p| < 2^22) leaves
+      // rint(p), ties to even, in the sum's low mantissa bits in two's complement - its low byte is
+      // the code. Rows whose 127 / amax overflows (amax below ~3.7e-37) or vanishes (an infinite
+      // element) take the conversion instruction and the clamp instead.
+      const bool fast = live && !inv_inf && inv > 0.0f;
       uint32_t b_prev[2] = {0u, 0u};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&raw[qd][c]);
-        uint32_t bw[2] = {0u, 0u}, hw[4];
+        const uint32_t w[4] = {raw[qd][c].x, raw[qd][c].y, raw[qd][c].z, raw[qd][c].w};
+        uint32_t bw[2];
+        if (fast) {
+          constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+          uint32_t y[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(v2[e]);
-          // With inv finite, |x| <= amax and inv = 127 / amax correctly rounded give
-          // |x * inv| <= 127 (1 + 2^-23) < 127.5, so the rounded code is already in [-127, 127] and
-          // the definition's clamp acts only when 127 / amax overflows (amax below ~3.7e-37)
-          int c0 = 0, c1 = 0;
-          if (live) {
-            c0 = __float2int_rn(__fmul_rn(f.x, inv));
-            c1 = __float2int_rn(__fmul_rn(f.y, inv));
-            if (inv_inf) {
-              c0 = max(-127, min(127, c0));
-              c1 = max(-127, min(127, c1));
-            }
+          for (int e = 0; e < 4; ++e) {
+            y[2 * e] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(w[e] << 16), inv), kMagic));
+            y[2 * e + 1] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(w[e] & 0xffff0000u), inv), kMagic));
           }
-          bw[e >> 1] |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * (e & 1));
-          hw[e] = (uint32_t)__half_as_ushort(__int2half_rn(c0)) |
-                  ((uint32_t)__half_as_ushort(__int2half_rn(c1)) << 16);  // exact: |c| <= 127
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            bw[k] = __byte_perm(__byte_perm(y[4 * k], y[4 * k + 1], 0x0040), __byte_perm(y[4 * k + 2], y[4 * k + 3], 0x0040),
+                                0x5410);
+        } else {
+          bw[0] = bw[1] = 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            int c0 = 0, c1 = 0;
+            if (live) {
+              c0 = max(-127, min(127, __float2int_rn(__fmul_rn(__uint_as_float(w[e] << 16), inv))));
+              c1 = max(-127, min(127, __float2int_rn(__fmul_rn(__uint_as_float(w[e] & 0xffff0000u), inv))));
+            }
+            bw[e >> 1] |= ((uint32_t)(c0 & 0xff) | ((uint32_t)(c1 & 0xff) << 8)) << (16 * (e & 1));
+          }
         }
-        if (d16) d16[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (d16) {
+          // codes -> fp16 integers, exact: bytes (b ^ 0x80) under the fp16 exponent of 1024 give
+          // 1024 + b + 128, and one fp16 subtraction of 1152 leaves b
+          uint32_t hw[4];
+          const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t u = bw[k] ^ 0x80808080u;
+            uint32_t lo = __byte_perm(u, 0x64646464u, 0x5140), hi = __byte_perm(u, 0x64646464u, 0x7362);
+            const __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+            const __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+            hw[2 * k] = *reinterpret_cast<const uint32_t*>(&hl);
+            hw[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+          d16[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
         if (c & 1) d8[c >> 1] = make_uint4(b_prev[0], b_prev[1], bw[0], bw[1]);
         else {
           b_prev[0] = bw[0];
