@@ -862,13 +862,16 @@ __device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barrie
 #pragma unroll
           for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
         }
+        // the masked scores become -inf in place, once, and only in warps that have some (tiles on
+        // the diagonal or at a block's end); the loops below then need no mask
+        if (__any_sync(0xffffffffu, need_mask)) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e > lim) sv[e] = 0xff800000u;  // -inf
+        }
         float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          float v = __uint_as_float(sv[e]);
-          if (need_mask && e > lim) v = -INFINITY;
-          mx = fmaxf(mx, v);
-        }
+        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
         mx *= sc;  // sc > 0 (or NaN for a NaN q row)
         // both halves of a row agree on its maximum through shared memory
         bar.rowmax[g & 1][h][i] = mx;
@@ -895,9 +898,7 @@ __device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barrie
 #pragma unroll
           for (int k = 0; k < n; ++k) {
             const int e = e0 + k;
-            float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
-            if (need_mask && 2 * e > lim) s0 = -INFINITY;
-            if (need_mask && 2 * e + 1 > lim) s1 = -INFINITY;
+            const float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
             if (remainder) {
               const float x0 = ex2_again(fmaf(s0, sc, -m_use)), x1 = ex2_again(fmaf(s1, sc, -m_use));
               pk[k] = pack_bf16x2(x0 - __uint_as_float(pk[k] << 16), x1 - __uint_as_float(pk[k] & 0xffff0000u));
