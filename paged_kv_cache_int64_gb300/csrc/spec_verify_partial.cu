@@ -63,6 +63,7 @@ __host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; } 
 __host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
 constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kOrderMaxReqs = 128;  // batches up to this many requests run longest-first
 
 // shared memory layout (1024-aligned). K and V stages are separate rings, so the K codes of tile
 // j+2 can stream in as soon as tile j's K is widened, without waiting for its V.
@@ -108,6 +109,7 @@ struct Params {
   int64_t bt_stride, num_blocks;
   int32_t max_blocks;
   const int32_t* seq_lens;
+  int32_t num_reqs;
   int32_t T, group, num_q_heads, block_size, seg, split_tokens, max_splits;
   int32_t tpc, n_tg;  // tokens per CTA (tpc * group <= 32 query columns) and CTAs per (split, head)
   float scale_log2;
@@ -209,13 +211,74 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // blockIdx.x = split * n_tg + token group: the CTAs that share a key range are adjacent, so they
-  // run together and the later reads of the same K/V tiles hit L2
-  const int split = blockIdx.x / p.n_tg;
-  const int t_base = (blockIdx.x - split * p.n_tg) * p.tpc;  // first query token of this CTA
-  const int nq = min(p.tpc, p.T - t_base) * p.group;         // live query columns; the rest pad
-  const int kvh = blockIdx.y;
-  const int r = blockIdx.z;
+  // The linear CTA index is (request, split) pair * (KV heads * token groups) + KV head * token
+  // groups + token group: the CTAs that share a key range are adjacent, so they run together and
+  // the later reads of the same K/V tiles hit L2.
+  const int64_t lin = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+  const int units = (int)gridDim.y * p.n_tg;
+  const int64_t pair = lin / units;
+  const int kvh = (int)(lin - pair * units) / p.n_tg;
+  const int t_base = ((int)(lin - pair * units) - kvh * p.n_tg) * p.tpc;  // first query token of this CTA
+  const int nq = min(p.tpc, p.T - t_base) * p.group;                     // live query columns; the rest pad
+  int r, split;
+  if (p.num_reqs <= kOrderMaxReqs) {
+    // Longest first: the CTAs run in launch order, one per SM, so the pairs with a whole
+    // split_tokens keys go first (request by request) and the requests' shorter last splits
+    // follow from the longest down; the short CTAs then fill in behind the long ones instead of
+    // trailing them. Pairs past the last one have nothing to do and leave after one barrier.
+    int* s_rest = reinterpret_cast<int*>(sP);  // scratch before any role starts (P^T buffers)
+    long long* s_wsum = reinterpret_cast<long long*>(s_rest + kOrderMaxReqs);
+    int* s_pick = reinterpret_cast<int*>(s_wsum + kOrderMaxReqs / 32);
+    const int t = threadIdx.x;
+    int n_full = 0, rest = 0;
+    if (t < p.num_reqs) {
+      const int len = max(__ldg(p.seq_lens + t), 0);
+      n_full = min(len / p.split_tokens, p.max_splits);
+      rest = n_full < p.max_splits ? len - n_full * p.split_tokens : 0;  // keys of the last, shorter split
+    }
+    long long inc = n_full;  // inclusive prefix sum of the whole-split counts over requests 0..t
+    if (t < kOrderMaxReqs) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_wsum[warp] = inc;
+      s_rest[t] = rest;
+    }
+    if (t == 0) s_pick[0] = s_pick[1] = -1;
+    const int n_short = __syncthreads_count(rest > 0);
+    long long n_full_pairs = 0;
+#pragma unroll
+    for (int w = 0; w < kOrderMaxReqs / 32; ++w) {
+      if (w < warp) inc += s_wsum[w];
+      n_full_pairs += s_wsum[w];
+    }
+    if (pair >= n_full_pairs + n_short) return;  // CTA-uniform: no pair this far down the order
+    if (t < p.num_reqs) {
+      if (pair < n_full_pairs) {
+        if (pair >= inc - n_full && pair < inc) {
+          s_pick[0] = t;
+          s_pick[1] = (int)(pair - (inc - n_full));
+        }
+      } else if (rest > 0) {
+        int rank = 0;  // shorter last splits ranked by length, longest first (ties: lower request)
+        for (int u = 0; u < p.num_reqs; ++u) rank += s_rest[u] > rest || (s_rest[u] == rest && u < t);
+        if (rank == pair - n_full_pairs) {
+          s_pick[0] = t;
+          s_pick[1] = n_full;
+        }
+      }
+    }
+    __syncthreads();
+    r = s_pick[0];
+    split = s_pick[1];
+    // the scratch is overwritten only after the CTA-wide barrier that follows the tensor-memory
+    // allocation, by which time every thread has read its pick
+  } else {
+    r = (int)(pair / p.max_splits);
+    split = (int)(pair - (int64_t)r * p.max_splits);
+  }
   const int seq_len = __ldg(p.seq_lens + r);
   const int64_t k_begin64 = (int64_t)split * p.split_tokens;
   if (k_begin64 >= seq_len) return;  // CTA-uniform: split past this request's keys
@@ -801,6 +864,7 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   p.num_blocks = num_blocks;
   p.max_blocks = max_blocks;
   p.seq_lens = seq_lens;
+  p.num_reqs = num_reqs;
   p.T = T;
   p.group = group;
   p.tpc = tpc;

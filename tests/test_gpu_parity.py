@@ -495,6 +495,31 @@ def test_verify_other_query_geometries(pkv, T, hq, hkv):
     _partials_close(po, pl, rpo, rpl, p.seq_lens, split, T)
 
 
+@pytest.mark.parametrize("n_req", [7, 130])
+def test_verify_launch_order_covers_every_split(pkv, n_req):
+    """Batches of up to 128 requests run longest first (whole splits, then the requests' shorter
+    last splits by length), larger ones in request order: every live (request, split) partial must
+    match the oracle's wherever it falls in the order (the partials start as NaN). The lengths
+    include exact multiples of the split (no shorter last split), equal last-split lengths, requests
+    shorter than one split and the longest request last."""
+    T, split = 8, 256
+    if n_req == 7:
+        lens = [512, 300, 300, 768, 40, 1000, 2048]
+    else:
+        rng = np.random.default_rng(59)
+        lens = [int(x) for x in rng.integers(T, 420, size=n_req)]
+        lens[3], lens[50], lens[129] = 256, 512, 700
+    p = W.make_problem("vo", seed=59 + n_req, seq_lens=lens, q_lens=[T] * n_req,
+                       num_blocks=sum((L + 63) // 64 for L in lens) + 4, block_size=64, kv_dtype="int8",
+                       softmax_scale=1.0 / 16.0)
+    got, po, pl = _run_verify(pkv, p, split, T)
+    args = _verify_oracle_args(p)
+    ref = oracle.spec_verify_attn(*args, T, p.num_q_heads, p.softmax_scale)
+    _close(got, ref, TOL_BF16)
+    rpo, rpl = oracle.spec_verify_partial(*args, T, p.num_q_heads, p.softmax_scale, split, po.shape[0])
+    _partials_close(po, pl, rpo, rpl, p.seq_lens, split, T)
+
+
 def test_verify_bigpool_top_equals_bottom(pkv):
     """int8 per-token-head cache, 2,600-block pool (bs 880), request of L = 20,000 + 8 tokens on the top
     blocks and on the bottom blocks with identical bytes: bit-identical outputs, and the oracle."""
