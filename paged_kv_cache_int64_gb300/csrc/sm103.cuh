@@ -313,6 +313,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a
 //   dimension byte offset >> 4; 46-47 version (1); 49-51 base offset (0: atoms 1024-B aligned);
 //   61-63 layout (2 = 128-byte swizzle).
 constexpr uint32_t kLayoutSW128 = 2;
+constexpr uint32_t kLayoutSW64 = 4;  // 64-byte swizzle
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t layout = kLayoutSW128) {
   uint64_t d = 0;

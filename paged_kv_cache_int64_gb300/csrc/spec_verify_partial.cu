@@ -57,7 +57,7 @@ constexpr int kGC = 8;                // query columns per softmax warpgroup (4 
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
 constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
-constexpr int kPChunk = kNQ * 128;      // fp16 P^T [32 rows][64 keys] swizzled chunk
+constexpr int kPChunk = kNQ * 128;      // fp16 P^T of 64 keys: [64 keys][32 columns], 64-byte swizzle
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; }    // 2 x 128: fp16 K rows
 __host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // O^T += V_j^T P^T_j, each head_dim half as soon as its V half is widened; a second issuing
     // thread, so the 16 QK and 16 PV MMAs of a tile are issued side by side
     if (lane == 0) {
-      constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, false);
+      constexpr uint32_t id_pv = idesc_f16(128, kNQ, false, true, true);
       const uint32_t v_base = smem_u32(sV16), p_base = smem_u32(sP);
       for (int i = 0; i < n_tiles; ++i) {
         if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort, wl)) break;
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           tc_fence_after();
           for (int ks = 0; ks < 8; ++ks)
             umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
-                        smem_desc(pb + (ks >> 2) * kPChunk + (ks & 3) * 32, 16, 1024), id_pv,
+                        smem_desc(pb + ks * 1024, 0, 512, kLayoutSW64), id_pv,
                         (i > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bar.v_free[hh]);
         }
@@ -665,11 +665,16 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       }
       if (!dead) {  // P^T column for key k (rows c0..c0+7 of buffer j % 2): p * v_scale, fp16
         const float vs = vs_cur;
-        uint8_t* pt = sP + (j & 1) * 2 * kPChunk + (k >> 6) * kPChunk + c0 * 128 + (k & 7) * 2;
-        const uint32_t kc = (uint32_t)(k & 63) >> 3;
+        // row k of the MN-major P^T (64 bytes: 32 columns), the group's 16-byte chunk with the
+        // 64-byte swizzle (chunk index XOR bits 1-2 of the row)
+        uint8_t* pt = sP + (j & 1) * 2 * kPChunk + k * 64 + ((grp ^ ((k >> 1) & 3)) * 16);
+        uint32_t h[kGC / 2];
 #pragma unroll
-        for (int q = 0; q < kGC; ++q)
-          *reinterpret_cast<__half*>(pt + q * 128 + ((kc ^ (uint32_t)(q & 7)) * 16)) = __float2half_rn(e[q] * vs);
+        for (int q = 0; q < kGC / 2; ++q) {
+          const __half2 t = __floats2half2_rn(e[2 * q] * vs, e[2 * q + 1] * vs);
+          h[q] = *reinterpret_cast<const uint32_t*>(&t);
+        }
+        *reinterpret_cast<uint4*>(pt) = make_uint4(h[0], h[1], h[2], h[3]);
       }
       if (!dead) {
         tc_fence_after();
