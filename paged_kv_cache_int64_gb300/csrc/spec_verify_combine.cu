@@ -5,7 +5,8 @@
 // sum_s exp(lse_s - LSE) o_s with LSE = ln sum_s exp(lse_s).
 //
 // One warp per (query row, head): the lanes reduce the split LSEs, then each lane merges 8 of the
-// 256 output elements (two 16-byte loads per split) and writes 16 bytes of bf16.
+// 256 output elements (two 16-byte loads per split) and writes 16 bytes of bf16. With at most 32
+// splits, lane s holds split s's weight, so the partials' loads need no LSE load before them.
 #include <cuda_bf16.h>
 
 #include "host_common.h"
@@ -30,30 +31,49 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int64_t L = __ldg(seq_lens + r);
   int ns = (int)((L + split_tokens - 1) / split_tokens);
   ns = min(ns, max_splits);
-  float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, __ldg(part_lse + (int64_t)s * rows + row));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float sum = 0.0f;
-  if (m != -INFINITY) {
-    for (int s = lane; s < ns; s += 32) {
-      const float l = __ldg(part_lse + (int64_t)s * rows + row);
-      sum += (l == -INFINITY) ? 0.0f : expf(l - m);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (m != -INFINITY && sum > 0.0f) {
-    const float inv = 1.0f / sum;
-    for (int s = 0; s < ns; ++s) {
-      const float l = __ldg(part_lse + (int64_t)s * rows + row);
-      if (l == -INFINITY) continue;
-      const float w = expf(l - m) * inv;
-      const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + row) * head_dim) + lane * 2;
-      const float4 a = __ldg(src), b = __ldg(src + 1);
+  auto add = [&](int s, float w) {  // w == 0: a split with no visible key (its partial is not read)
+    const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + row) * head_dim) + lane * 2;
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    if (w != 0.0f) {
       acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
       acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+  };
+  if (ns <= 32) {
+    // lane s holds split s's LSE and, after the two reductions, its weight; the partials' loads
+    // then carry no dependence on an LSE load and run four splits at a time
+    const float l = lane < ns ? __ldg(part_lse + (int64_t)lane * rows + row) : -INFINITY;
+    float m = l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float e = (m == -INFINITY || l == -INFINITY) ? 0.0f : expf(l - m);
+    float sum = e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float w_lane = sum > 0.0f ? e * (1.0f / sum) : 0.0f;
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) add(s, __shfl_sync(0xffffffffu, w_lane, s));
+  } else {
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32) m = fmaxf(m, __ldg(part_lse + (int64_t)s * rows + row));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.0f;
+    if (m != -INFINITY) {
+      for (int s = lane; s < ns; s += 32) {
+        const float l = __ldg(part_lse + (int64_t)s * rows + row);
+        sum += (l == -INFINITY) ? 0.0f : expf(l - m);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (m != -INFINITY && sum > 0.0f) {
+      const float inv = 1.0f / sum;
+      for (int s = 0; s < ns; ++s) {
+        const float l = __ldg(part_lse + (int64_t)s * rows + row);
+        add(s, l == -INFINITY ? 0.0f : expf(l - m) * inv);
+      }
     }
   }
   uint4 o;

@@ -436,10 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
   } else if (warp >= 8 && warp < 12) {
     // ---------------------------------------------------------------------------- K converter
     // thread k owns key row k of each tile: its int8 (or e4m3) K row -> fp16 into TMEM lane k of the
-    // tile's K buffer; rows outside the split (or in a bad block) are written as zeros (0 * NaN
-    // would not vanish in the MMA). First, Q bf16 -> fp16 in place (32 rows x 256).
+    // tile's K buffer. A row outside the split or in a bad block holds stale stage bytes: int8 codes
+    // widen to finite values whatever they are, and such a key's score is masked (past the split)
+    // or multiplied by a zero scale (bad block), so the row is widened as it is; e4m3 rows are
+    // zeroed first, since a stale NaN code would survive the mask as 0 * NaN in the MMA. First, Q
+    // bf16 -> fp16 in place (32 rows x 256).
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
+    const int kseg = k / G;  // the key's segment within a tile (bad-block bits)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.q_full, 0, abort, wl));
     if (!dead) {  // row k & 31, chunk k >> 5; padding rows (past the CTA's columns) become zeros
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       if (got && j >= 2) got = mbar_wait_suspend(&bar.k_free[st], ((j >> 1) - 1) & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> (k / G)) & 1u);
+      const bool live = k_begin + j * kBN + k < k_end && !((bar.kbad[st] >> kseg) & 1u);
 #pragma unroll 1
       for (int w8 = 0; w8 < 8; ++w8) {  // 32 codes = 16 TMEM columns per step
         uint32_t kv[16];
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           const uint4 v = *reinterpret_cast<const uint4*>(kstage + kStageCodes + (w8 >> 2) * kChunk8 + k * 128 +
                                                           ((q8 ^ (k & 7)) * 16));
           uint32_t o[8];
-          widen16<kFp8>(live ? v : make_uint4(0, 0, 0, 0), o);  // zero codes widen to zeros
+          widen16<kFp8>((kFp8 && !live) ? make_uint4(0, 0, 0, 0) : v, o);  // zero codes widen to zeros
 #pragma unroll
           for (int e = 0; e < 8; ++e) kv[8 * i + e] = o[e];
         }
@@ -492,23 +496,25 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // ---------------------------------------------------------------------------- V converter
     // two warpgroups, one per half of head_dim (warps 12-15: 0-127, warps 20-23: 128-255), each with
     // its own ready / free barriers, so half 0 of V_{j+1} is widened while PV_j still reads half 1.
-    // Thread k owns key row k: its half V row -> fp16 into the MN-major V tile (zeros outside the
-    // split or in a bad block: the codes are zeroed before widening, which maps 0 to 0).
+    // Thread k owns key row k: its half V row -> fp16 into the MN-major V tile. A row outside the
+    // split or in a bad block meets a zero P^T entry: int8 rows are widened as they are (finite
+    // whatever the stale bytes), e4m3 rows are zeroed first (0 * NaN would not vanish).
     const int hv = warp >= 20 ? 1 : 0;  // warps 20-23: the second half
     const int k = (warp & 3) * 32 + lane;
+    const int kseg = k / G;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
       const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
       bool got = j == 0 || mbar_wait_suspend(&bar.v_free[hv], (j - 1) & 1, abort, wl);
       if (got) got = mbar_wait_suspend(&bar.vst_full[st], (j >> 1) & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
-      const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> (k / G)) & 1u);
+      const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> kseg) & 1u);
       const uint8_t* src = vstage + kStageCodes + hv * kChunk8 + k * 128;
       uint8_t* dst = sV16 + 2 * hv * kChunk16 + k * 128;
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
         uint4 v = *reinterpret_cast<const uint4*>(src + ((q8 ^ (k & 7)) * 16));
-        if (!live) v = make_uint4(0, 0, 0, 0);
+        if (kFp8 && !live) v = make_uint4(0, 0, 0, 0);
         uint32_t o[8];
         widen16<kFp8>(v, o);
         uint8_t* row = dst + (q8 >> 2) * kChunk16;
@@ -608,7 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           mbar_arrive(&bar.s_free[st]);  // QK_{j+2} may now overwrite this S^T buffer
         }
         const float f = p.scale_log2 * ks;
-        if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
+        if (!dead && key0 + kBN <= k_end && c0 + kGC <= nq && key0 + kBN - 1 <= prefix) {
+#pragma unroll
+          for (int q = 0; q < kGC; ++q) s[q] = __uint_as_float(v[q]) * f;
+        } else if (key0 + kBN - 1 <= prefix) {  // every key of the tile precedes the first draft token
 #pragma unroll
           for (int q = 0; q < kGC; ++q)
             s[q] = (!dead && in_range && c0 + q < nq) ? __uint_as_float(v[q]) * f : -INFINITY;
