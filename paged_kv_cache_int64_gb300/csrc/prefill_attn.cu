@@ -860,7 +860,12 @@ __device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barrie
         if (kInt8) {  // fold the per-key scales in place: s = S * ks
           named_bar_sync(6 + h, 128);  // this tile's scales of the half's keys, written by the half, are visible
 #pragma unroll
-          for (int e = 0; e < 64; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ks[e]);
+          for (int e = 0; e < 64; e += 2) {
+            float a0, a1;
+            mul2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ks[e], ks[e + 1]);
+            sv[e] = __float_as_uint(a0);
+            sv[e + 1] = __float_as_uint(a1);
+          }
         }
         // the masked scores become -inf in place, once, and only in warps that have some (tiles on
         // the diagonal or at a block's end); the loops below then need no mask
@@ -894,21 +899,21 @@ __device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barrie
         // bf16(P - hi) of a two-part P, from hi in pk (the exp2 recomputed, bit for bit)
         // pairs e0 .. e0 + n - 1 (keys 2e, 2e + 1 of this half) into pk[0 .. n)
         auto pack_p = [&](uint32_t* pk, int e0, int n, bool remainder) -> float {
-          float sum = 0.0f;
+          float sa = 0.0f, sb = 0.0f;
 #pragma unroll
           for (int k = 0; k < n; ++k) {
             const int e = e0 + k;
-            const float s0 = __uint_as_float(sv[2 * e]), s1 = __uint_as_float(sv[2 * e + 1]);
+            float y0, y1;
+            fma2(y0, y1, __uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), sc, sc, -m_use, -m_use);
             if (remainder) {
-              const float x0 = ex2_again(fmaf(s0, sc, -m_use)), x1 = ex2_again(fmaf(s1, sc, -m_use));
+              const float x0 = ex2_again(y0), x1 = ex2_again(y1);
               pk[k] = pack_bf16x2(x0 - __uint_as_float(pk[k] << 16), x1 - __uint_as_float(pk[k] & 0xffff0000u));
             } else {
-              const float x0 = ex2_approx(fmaf(s0, sc, -m_use)), x1 = ex2_approx(fmaf(s1, sc, -m_use));
-              pk[k] = pack_bf16x2(x0, x1);
+              pk[k] = pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
             }
-            sum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
+            add_bf16x2_to(sa, sb, pk[k]);
           }
-          return sum;
+          return sa + sb;
         };
         uint32_t pk[32];
         float lsum = 0.0f;
@@ -947,7 +952,12 @@ __device__ __forceinline__ void cta_roles(const Params& p, uint8_t* smem, Barrie
               tmem_ld_32x32b_x32(oa, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+              for (int e = 0; e < 32; e += 2) {
+                float a0, a1;
+                mul2(a0, a1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), alpha, alpha);
+                v[e] = __float_as_uint(a0);
+                v[e + 1] = __float_as_uint(a1);
+              }
               tmem_st_32x32b_x32(oa, v);
             }
           }

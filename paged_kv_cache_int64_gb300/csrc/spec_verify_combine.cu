@@ -23,6 +23,9 @@ __global__ void __launch_bounds__(kWarps * 32)
                                const int32_t* __restrict__ seq_lens, int32_t T, int32_t num_q_heads,
                                int32_t head_dim, int32_t split_tokens, int32_t max_splits, int64_t rows,
                                __nv_bfloat16* __restrict__ out) {
+  // launched as a programmatic dependent: wait until the previous kernel in the stream (the
+  // partials' launch) has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);  // (token, head)
   if (row >= rows) return;
@@ -100,9 +103,19 @@ extern "C" pkv_status pkv_spec_verify_combine(const float* part_o, const float* 
   PKV_ARG(aligned16(part_o) && aligned16(out), "spec_verify_combine: part_o and out must be 16-byte aligned");
   if (num_reqs == 0) return PKV_OK;
   const int64_t rows = (int64_t)num_reqs * T * num_q_heads;
-  dim3 grid((unsigned)((rows + kWarps - 1) / kWarps));
-  spec_verify_combine_kernel<<<grid, kWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
-      part_o, part_lse, seq_lens, T, num_q_heads, head_dim, split_tokens, max_splits, rows,
-      static_cast<__nv_bfloat16*>(out));
+  // programmatic dependent launch: the blocks may be scheduled while the partials' CTAs finish;
+  // each waits (griddepcontrol.wait) for that grid's completion before its first read
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kWarps - 1) / kWarps));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, spec_verify_combine_kernel, part_o, part_lse, seq_lens, T, num_q_heads, head_dim,
+                     split_tokens, max_splits, rows, static_cast<__nv_bfloat16*>(out));
   return check_launch("spec_verify_combine");
 }
