@@ -51,31 +51,48 @@ namespace {
 
 constexpr int kD = 256;
 constexpr int kBN = 128;  // keys per tile
-constexpr int kNQ = 32;   // query columns (T * group)
-constexpr int kThreads = 1024;
-constexpr int kGC = 8;                // query columns per softmax warpgroup (4 groups)
 constexpr int kChunk8 = 128 * 128;      // int8 [128 rows][128 B] swizzled chunk
 constexpr int kChunk16 = 128 * 128;     // fp16 [128 rows][64] swizzled chunk
-constexpr int kQChunk = kNQ * 128;      // fp16 [32 rows][64] swizzled chunk
-constexpr int kPChunk = kNQ * 128;      // fp16 P^T of 64 keys: [64 keys][32 columns], 64-byte swizzle
 constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_k(int st) { return st ? 128u : 0u; }    // 2 x 128: fp16 K rows
-__host__ __device__ constexpr uint32_t col_s(int st) { return st ? 288u : 256u; }  // 2 x 32: S^T
-constexpr uint32_t kColO = 320;           // 2 x 32 columns: O^T halves (head_dim 0-127, 128-255)
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kOrderMaxReqs = 128;  // batches up to this many requests run longest-first
-
-// shared memory layout (1024-aligned). K and V stages are separate rings, so the K codes of tile
-// j+2 can stream in as soon as tile j's K is widened, without waiting for its V.
-constexpr int kOffQ = 0;                         // 4 x kQChunk = 16 KB
 constexpr int kStageCodes = 0;                   // a K or V stage: [2 chunks][128 rows][128 B] codes
 constexpr int kStageBytes = 2 * kChunk8;         // 32 KB
-constexpr int kOffKStage = kOffQ + 4 * kQChunk;
-constexpr int kOffVStage = kOffKStage + 2 * kStageBytes;
-constexpr int kOffV16 = kOffVStage + 2 * kStageBytes;
-constexpr int kOffP = kOffV16 + 4 * kChunk16;
-constexpr int kTiles = kOffP + 4 * kPChunk;  // P^T: two buffers of [2 chunks] (64 keys each)
 
+// Two CTA shapes. N = 32 query columns: four softmax groups of 8 columns, 1,024 threads, K and V
+// code rings of two stages each. N = 48 (e.g. 8 tokens x 6 heads): three groups of 16 columns,
+// 896 threads, a single V code stage, so that the larger Q and P^T tiles fit in shared memory.
+// Shared memory (1024-aligned): Q [4 chunks][N rows][128 B], the K code ring, the V code ring (K
+// and V rings apart, so the K codes of tile j+2 can stream in as soon as tile j's K is widened,
+// without waiting for its V), the fp16 V tile, two P^T buffers. P^T is MN-major: a key's N fp16
+// weights are one row of 64 B (N = 32, 64-byte swizzle) or 128 B (N = 48 in a 64-column atom,
+// 128-byte swizzle). Tensor memory: K 2 x 128 columns, S^T 2 x N, O^T 2 halves x N.
+template <int kCols>
+struct Geo {
+  static_assert(kCols == 32 || kCols == 48, "two CTA shapes");
+  static constexpr int kNQ = kCols;                      // query columns (tokens x group)
+  static constexpr int kGC = kCols == 32 ? 8 : 16;       // query columns per softmax group
+  static constexpr int kGroups = kNQ / kGC;              // 4 or 3 softmax warpgroups
+  static constexpr int kThreads = kCols == 32 ? 1024 : 896;
+  static constexpr int kVStages = kCols == 32 ? 2 : 1;
+  static constexpr int kQChunk = kNQ * 128;              // fp16 [N rows][64] swizzled chunk
+  static constexpr int kPRow = kCols == 32 ? 64 : 128;   // bytes per key row of P^T
+  static constexpr int kPBuf = kBN * kPRow;              // one P^T buffer (a tile's 128 keys)
+  static constexpr uint32_t kPLayout = kCols == 32 ? kLayoutSW64 : kLayoutSW128;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKStage = kOffQ + 4 * kQChunk;
+  static constexpr int kOffVStage = kOffKStage + 2 * kStageBytes;
+  static constexpr int kOffV16 = kOffVStage + kVStages * kStageBytes;
+  static constexpr int kOffP = kOffV16 + 4 * kChunk16;
+  static constexpr int kTiles = kOffP + 2 * kPBuf;
+  __host__ __device__ static constexpr uint32_t col_s(int st) { return 256u + (uint32_t)(st * kNQ); }
+  static constexpr uint32_t kColO = 256u + 2u * kNQ;     // O^T halves (head_dim 0-127, 128-255)
+  static_assert(kOffKStage % 1024 == 0 && kOffV16 % 1024 == 0 && kOffP % 1024 == 0, "1024-B atoms");
+  static_assert(kColO + 2 * kNQ <= kTmemCols, "tensor memory");
+};
+
+template <int kCols>
 struct alignas(16) Barriers {
   uint64_t q_full, q_ready;
   uint64_t kst_full[2], kst_free[2];  // K stage ring (freed by the K converter)
@@ -94,8 +111,8 @@ struct alignas(16) Barriers {
   uint32_t tmem_base;
   int abort;
   uint32_t kbad[2], vbad[2];        // per stage: segments whose block id was out of range
-  float red[2][kNQ / kGC][4][kGC];  // [tile parity][softmax group][warp][column]: maxima, then the final sums
-  float inv_l[kNQ];      // epilogue: 1 / column sum
+  float red[2][Geo<kCols>::kGroups][4][Geo<kCols>::kGC];  // [tile parity][group][warp][column]: maxima, then the final sums
+  float inv_l[kCols];      // epilogue: 1 / column sum
 };
 
 struct Params {
@@ -200,14 +217,56 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
   return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const __grid_constant__ Params p) {
+// Column maxima of 16 columns without consuming the input (the scores are needed afterwards): the
+// first exchange (lanes 8 apart) writes 8 partial maxima to a scratch array, the rest runs on that.
+__device__ __forceinline__ float reduce_scatter16_max_keep(const float (&v)[16], int lane) {
+  float t[8];
+  const bool upper = (lane & 8) != 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float keep = upper ? v[q + 8] : v[q];
+    const float send = upper ? v[q] : v[q + 8];
+    t[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float keep = up ? t[q + o] : t[q];
+      const float send = up ? t[q] : t[q + o];
+      t[q] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  return fmaxf(t[0], __shfl_xor_sync(0xffffffffu, t[0], 16));
+}
+
+template <int kGC, bool kMax>
+__device__ __forceinline__ float reduce_scatter(float (&v)[kGC], int lane) {
+  if constexpr (kGC == 8) return reduce_scatter8<kMax>(v, lane);
+  else return reduce_scatter16<kMax>(v, lane);
+}
+template <int kGC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kGC]) {
+  if constexpr (kGC == 8) tmem_ld_32x32b_x8(taddr, r);
+  else tmem_ld_32x32b_x16(taddr, r);
+}
+template <int kGC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[kGC]) {
+  if constexpr (kGC == 8) tmem_st_32x32b_x8(taddr, r);
+  else tmem_st_32x32b_x16(taddr, r);
+}
+
+template <bool kFp8, int kCols>
+__global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_kernel(const __grid_constant__ Params p) {
+  using Gm = Geo<kCols>;
+  constexpr int kNQ = Gm::kNQ, kGC = Gm::kGC, kGroups = Gm::kGroups, kVStages = Gm::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sV16 = smem + kOffV16;
-  uint8_t* sP = smem + kOffP;
-  Barriers& bar = *reinterpret_cast<Barriers*>(smem + kTiles);
+  uint8_t* sQ = smem + Gm::kOffQ;
+  uint8_t* sV16 = smem + Gm::kOffV16;
+  uint8_t* sP = smem + Gm::kOffP;
+  Barriers<kCols>& bar = *reinterpret_cast<Barriers<kCols>*>(smem + Gm::kTiles);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -301,14 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       mbar_init(&bar.k_ready[s], 128);
       mbar_init(&bar.k_free[s], 1);
       mbar_init(&bar.s_full[s], 1);
-      mbar_init(&bar.s_free[s], (kNQ / kGC) * 128);
+      mbar_init(&bar.s_free[s], kGroups * 128);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&bar.v_ready[h], 128);
       mbar_init(&bar.v_free[h], 1);
     }
-    mbar_init(&bar.p_full[0], (kNQ / kGC) * 128);  // every softmax thread of the four groups
-    mbar_init(&bar.p_full[1], (kNQ / kGC) * 128);
+    mbar_init(&bar.p_full[0], kGroups * 128);  // every softmax thread of every group
+    mbar_init(&bar.p_full[1], kGroups * 128);
     mbar_init(&bar.pv_done[0], 1);
     mbar_init(&bar.pv_done[1], 1);
     mbar_init(&bar.drain, 2);  // the QK and the PV issuer
@@ -331,14 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 
   if (warp == 0 || warp == 3) {
     // ---------------------------------------------------------------------------- producers
-    // warp 0 streams the K codes, warp 3 the V codes, each through its own two-stage ring; both
-    // read the block table for their tiles
+    // warp 0 streams the K codes, warp 3 the V codes, each through its own ring (K: two stages; V:
+    // two, or one with N = 48); both read the block table for their tiles
     const bool is_k = warp == 0;
+    const int nst = is_k ? 2 : kVStages;
     const int nseg = kBN / G;
     if (is_k && lane == 0) {
       mbar_arm_tx(&bar.q_full, 4u * 128u * (uint32_t)(p.tpc * p.group), &bar.armed[0]);  // the whole box
       for (int c = 0; c < 4; ++c)
-        tma_load_3d(sQ + c * kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T + t_base);
+        tma_load_3d(sQ + c * Gm::kQChunk, &p.qmap, &bar.q_full, c * 64, kvh * p.group, r * p.T + t_base);
     }
     uint64_t* full = is_k ? bar.kst_full : bar.vst_full;
     uint64_t* freeb = is_k ? bar.kst_free : bar.vst_free;
@@ -347,12 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const CUtensorMap* codes = is_k ? &p.k8map : &p.v8map;
     const CUtensorMap* codes_big = is_k ? &p.k8map_big : &p.v8map_big;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      uint8_t* stage = smem + (is_k ? kOffKStage : kOffVStage) + st * kStageBytes;
+      const int st = nst == 2 ? (j & 1) : 0;
+      const int round = nst == 2 ? (j >> 1) : j;  // uses of this stage before tile j
+      uint8_t* stage = smem + (is_k ? Gm::kOffKStage : Gm::kOffVStage) + st * kStageBytes;
       // go / stop is lane 0's wait result, broadcast, so the lanes never part (once any role gives
       // up, every wait returns false promptly)
       bool ok0 = true;
-      if (lane == 0 && j >= 2) ok0 = mbar_wait_suspend(&freeb[st], ((j >> 1) - 1) & 1, abort, wl);
+      if (lane == 0 && round >= 1) ok0 = mbar_wait_suspend(&freeb[st], (round - 1) & 1, abort, wl);
       if (!__shfl_sync(0xffffffffu, ok0, 0)) break;
       const int key0 = k_begin + j * kBN;
       int blk = -1;
@@ -398,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         if (!mbar_wait_suspend(&bar.k_ready[st], (j >> 1) & 1, abort, wl)) break;
         tc_fence_after();
         for (int ks = 0; ks < 16; ++ks)
-          umma_f16_ts(tmem + col_s(st), tmem + col_k(st) + ks * 8,
-                      smem_desc(q_base + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
+          umma_f16_ts(tmem + Gm::col_s(st), tmem + col_k(st) + ks * 8,
+                      smem_desc(q_base + (ks >> 2) * Gm::kQChunk + (ks & 3) * 32, 16, 1024), id_qk, ks > 0);
         umma_commit(&bar.s_full[st]);
         umma_commit(&bar.k_free[st]);
       }
@@ -414,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       const uint32_t v_base = smem_u32(sV16), p_base = smem_u32(sP);
       for (int i = 0; i < n_tiles; ++i) {
         if (!mbar_wait_suspend(&bar.p_full[i & 1], (i >> 1) & 1, abort, wl)) break;
-        const uint32_t pb = p_base + (i & 1) * 2 * kPChunk;
+        const uint32_t pb = p_base + (i & 1) * Gm::kPBuf;
         bool ok = true;
         for (int hh = 0; hh < 2 && ok; ++hh) {
           if (!mbar_wait_suspend(&bar.v_ready[hh], i & 1, abort, wl)) {
@@ -423,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
           }
           tc_fence_after();
           for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ss(tmem + kColO + hh * 32, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
-                        smem_desc(pb + ks * 1024, 0, 512, kLayoutSW64), id_pv,
+            umma_f16_ss(tmem + Gm::kColO + hh * kNQ, smem_desc(v_base + hh * 2 * kChunk16 + ks * 2048, kChunk16, 1024),
+                        smem_desc(pb + ks * 16 * Gm::kPRow, 0, 8 * Gm::kPRow, Gm::kPLayout), id_pv,
                         (i > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&bar.v_free[hh]);
         }
@@ -440,33 +501,35 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     // widen to finite values whatever they are, and such a key's score is masked (past the split)
     // or multiplied by a zero scale (bad block), so the row is widened as it is; e4m3 rows are
     // zeroed first, since a stale NaN code would survive the mask as 0 * NaN in the MMA. First, Q
-    // bf16 -> fp16 in place (32 rows x 256).
+    // bf16 -> fp16 in place (N rows x 256).
     const int quarter = warp & 3;
     const int k = quarter * 32 + lane;
     const int kseg = k / G;  // the key's segment within a tile (bad-block bits)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.q_full, 0, abort, wl));
-    if (!dead) {  // row k & 31, chunk k >> 5; padding rows (past the CTA's columns) become zeros
-      const int row = k & 31, c = k >> 5;
-      const bool live_row = row < nq;
+    if (!dead) {  // (row, chunk) pairs idx = k, k + 128, ...; padding rows (past the CTA's columns) become zeros
+      for (int idx = k; idx < 4 * kNQ; idx += 128) {
+        const int row = idx % kNQ, c = idx / kNQ;
+        const bool live_row = row < nq;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint4* ptr = reinterpret_cast<uint4*>(sQ + c * kQChunk + row * 128 + q * 16);
-        uint4 v = live_row ? *ptr : make_uint4(0, 0, 0, 0);
-        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+        for (int q = 0; q < 8; ++q) {
+          uint4* ptr = reinterpret_cast<uint4*>(sQ + c * Gm::kQChunk + row * 128 + q * 16);
+          uint4 v = live_row ? *ptr : make_uint4(0, 0, 0, 0);
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-          w[e] = pack_f16x2(f.x, f.y);
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            w[e] = pack_f16x2(f.x, f.y);
+          }
+          *ptr = v;
         }
-        *ptr = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(&bar.q_ready);
     }
     for (int j = 0; j < n_tiles && !dead; ++j) {
       const int st = j & 1;
-      const uint8_t* kstage = smem + kOffKStage + st * kStageBytes;
+      const uint8_t* kstage = smem + Gm::kOffKStage + st * kStageBytes;
       bool got = mbar_wait_suspend(&bar.kst_full[st], (j >> 1) & 1, abort, wl);
       if (got && j >= 2) got = mbar_wait_suspend(&bar.k_free[st], ((j >> 1) - 1) & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -503,10 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     const int k = (warp & 3) * 32 + lane;
     const int kseg = k / G;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const uint8_t* vstage = smem + kOffVStage + st * kStageBytes;
+      const int st = kVStages == 2 ? (j & 1) : 0;
+      const int round = kVStages == 2 ? (j >> 1) : j;  // uses of this stage before tile j
+      const uint8_t* vstage = smem + Gm::kOffVStage + st * kStageBytes;
       bool got = j == 0 || mbar_wait_suspend(&bar.v_free[hv], (j - 1) & 1, abort, wl);
-      if (got) got = mbar_wait_suspend(&bar.vst_full[st], (j >> 1) & 1, abort, wl);
+      if (got) got = mbar_wait_suspend(&bar.vst_full[st], round & 1, abort, wl);
       if (!__all_sync(0xffffffffu, got)) break;
       const bool live = k_begin + j * kBN + k < k_end && !((bar.vbad[st] >> kseg) & 1u);
       const uint8_t* src = vstage + kStageCodes + hv * kChunk8 + k * 128;
@@ -528,10 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------------------- softmax
-    // four warpgroups of kGC = 8 query columns (warps 4-7, 16-19, 24-27, 28-31); thread k holds key
-    // k's 8 scores of its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter leaves
-    // column (lane & 7)'s warp maximum in the lane, shared memory combines the four warps; lane l
-    // then keeps column (l & 7)'s running max (the same in all four warps) and hands it to the
+    // warpgroups of kGC query columns (N = 32: four groups of 8, warps 4-7, 16-19, 24-27, 28-31;
+    // N = 48: three groups of 16, warps 4-7, 16-19, 24-27); thread k holds key k's kGC scores of
+    // its group (TMEM lane k of S^T). Column maxima: a shuffle reduce-scatter leaves column
+    // (lane % kGC)'s warp maximum in the lane, shared memory combines the group's four warps; lane l
+    // then keeps column (l % kGC)'s running max (the same in all four warps) and hands it to the
     // other lanes by shuffles. The K scale folds into the scores, the V scale into P^T; each
     // thread reads its key's two scales from the cache itself, two tiles ahead (the block id three
     // tiles ahead), so no stage buffer waits for the softmax and the HBM latency is covered.
@@ -608,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         const float ks = kFp8 ? k_descale : ks_cur;
         if (!dead) {
           tc_fence_after();
-          tmem_ld_32x32b_x8(tmem + lane_off + col_s(st) + c0, v);
+          tmem_ld_cols<kGC>(tmem + lane_off + Gm::col_s(st) + c0, v);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(&bar.s_free[st]);  // QK_{j+2} may now overwrite this S^T buffer
@@ -631,10 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         }
       }
       {
-        float t[kGC];
+        float mine;
+        if constexpr (kGC == 16) {
+          mine = reduce_scatter16_max_keep(s, lane);
+        } else {
+          float t[kGC];
 #pragma unroll
-        for (int q = 0; q < kGC; ++q) t[q] = s[q];
-        const float mine = reduce_scatter8<true>(t, lane);
+          for (int q = 0; q < kGC; ++q) t[q] = s[q];
+          mine = reduce_scatter<kGC, true>(t, lane);
+        }
         if (lane < kGC) bar.red[st][grp][quarter][lane] = mine;
       }
       named_bar_sync(1 + grp, 128);
@@ -660,11 +730,18 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
         dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, wl));
       // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
       // the running column sums and the fp16 P^T stores run as independent batches
-      float e[kGC];
+      // (16 columns: in place over the scores, which keeps the registers within the 896-thread budget)
+      float e_buf[kGC == 16 ? 1 : kGC];
+      float (&e)[kGC] = *reinterpret_cast<float(*)[kGC]>(kGC == 16 ? s : e_buf);
+      if constexpr (kGC == 16) {
 #pragma unroll
-      for (int q = 0; q < kGC; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
+        for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - __shfl_sync(0xffffffffu, mu, q));
+      } else {
 #pragma unroll
-      for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - e[q]);
+        for (int q = 0; q < kGC; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
+#pragma unroll
+        for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - e[q]);
+      }
       if (any_rescale) {
 #pragma unroll
         for (int q = 0; q < kGC; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
@@ -672,18 +749,23 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 #pragma unroll
         for (int q = 0; q < kGC; ++q) l_part[q] += e[q];
       }
-      if (!dead) {  // P^T column for key k (rows c0..c0+7 of buffer j % 2): p * v_scale, fp16
+      if (!dead) {  // P^T for key k (columns c0 .. c0 + kGC - 1 of buffer j % 2): p * v_scale, fp16
         const float vs = vs_cur;
-        // row k of the MN-major P^T (64 bytes: 32 columns), the group's 16-byte chunk with the
-        // 64-byte swizzle (chunk index XOR bits 1-2 of the row)
-        uint8_t* pt = sP + (j & 1) * 2 * kPChunk + k * 64 + ((grp ^ ((k >> 1) & 3)) * 16);
-        uint32_t h[kGC / 2];
+        // row k of the MN-major P^T, the group's 16-byte chunks; the swizzle XORs a chunk index with
+        // the row's bits at 128-byte granularity (64-B rows: bits 1-2 of k; 128-B rows: bits 0-2)
+        uint8_t* prow = sP + (j & 1) * Gm::kPBuf + k * Gm::kPRow;
+        const uint32_t sw = Gm::kPRow == 64 ? ((uint32_t)(k >> 1) & 3u) : ((uint32_t)k & 7u);
 #pragma unroll
-        for (int q = 0; q < kGC / 2; ++q) {
-          const __half2 t = __floats2half2_rn(e[2 * q] * vs, e[2 * q + 1] * vs);
-          h[q] = *reinterpret_cast<const uint32_t*>(&t);
+        for (int cc = 0; cc < kGC / 8; ++cc) {
+          uint32_t h[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __half2 t = __floats2half2_rn(e[8 * cc + 2 * q] * vs, e[8 * cc + 2 * q + 1] * vs);
+            h[q] = *reinterpret_cast<const uint32_t*>(&t);
+          }
+          const uint32_t chunk = (uint32_t)(grp * (kGC / 8) + cc);
+          *reinterpret_cast<uint4*>(prow + ((chunk ^ sw) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
-        *reinterpret_cast<uint4*>(pt) = make_uint4(h[0], h[1], h[2], h[3]);
       }
       if (!dead) {
         tc_fence_after();
@@ -691,12 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[kGC];
-            tmem_ld_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
+            tmem_ld_cols<kGC>(tmem + lane_off + Gm::kColO + hh * kNQ + c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < kGC; ++q)
               v[q] = __float_as_uint(__uint_as_float(v[q]) * __shfl_sync(0xffffffffu, alpha, q));
-            tmem_st_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
+            tmem_st_cols<kGC>(tmem + lane_off + Gm::kColO + hh * kNQ + c0, v);
           }
           tmem_wait_st();
         }
@@ -709,12 +791,12 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
       ks_1 = ks_2;
       vs_1 = vs_2;
     }
-    // epilogue: column sums, O^T / l, log-sum-exp (each group for its 16 columns)
+    // epilogue: column sums, O^T / l, log-sum-exp (each group for its kGC columns)
     bool fin = !dead && !*abort && mbar_wait_suspend(&bar.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort, wl);
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
-      const float sum = reduce_scatter8<false>(l_part, lane);
+      const float sum = reduce_scatter<kGC, false>(l_part, lane);
       if (lane < kGC) bar.red[0][grp][quarter][lane] = sum;
     }
     named_bar_sync(1 + grp, 128);
@@ -736,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_partial_kernel(const 
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[kGC];
-        tmem_ld_32x32b_x8(tmem + lane_off + kColO + hh * 32 + c0, v);
+        tmem_ld_cols<kGC>(tmem + lane_off + Gm::kColO + hh * kNQ + c0, v);
         tmem_wait_ld();
         const int d = hh * 128 + k;
 #pragma unroll
@@ -803,6 +885,17 @@ extern "C" size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t nu
 namespace pkv {
 namespace {
 
+template <bool kFp8, int kCols>
+void launch_shape(const Params& p, dim3 grid, cudaStream_t st) {
+  constexpr int kSmem = 1024 + Geo<kCols>::kTiles + (int)sizeof(Barriers<kCols>);
+  static_assert(kSmem <= 227 * 1024, "dynamic shared memory of one CTA");
+  static std::atomic<uint64_t> attr_done{0};
+  once_per_device(attr_done, [] {
+    cudaFuncSetAttribute(spec_verify_partial_kernel<kFp8, kCols>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  spec_verify_partial_kernel<kFp8, kCols><<<grid, Geo<kCols>::kThreads, kSmem, st>>>(p);
+}
+
 // Shared host path of the int8 (per-token-head scales) and fp8 (per-tensor descales) verify calls.
 template <bool kFp8>
 pkv_status launch_verify(const char* name, const void* q, const void* k_cache, const void* v_cache,
@@ -823,9 +916,14 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
           "%s: bad size argument", name);
   PKV_UNSUP(num_q_heads % num_kv_heads == 0, "%s: num_q_heads %% num_kv_heads != 0", name);
   const int group = num_q_heads / num_kv_heads;
-  PKV_UNSUP(group <= kNQ, "%s: num_q_heads / num_kv_heads must be at most 32 (got %d)", name, group);
-  const int tpc = T < kNQ / group ? T : kNQ / group;  // tokens per CTA
-  const int n_tg = (T + tpc - 1) / tpc;                // CTAs per (split, KV head, request)
+  PKV_UNSUP(group <= 32, "%s: num_q_heads / num_kv_heads must be at most 32 (got %d)", name, group);
+  // CTA shape: N = 48 query columns when that serves a key range with fewer CTAs than N = 32
+  // (e.g. 8 tokens x 6 heads in one CTA instead of two), else N = 32
+  const int tpc32 = T < 32 / group ? T : 32 / group, n32 = (T + tpc32 - 1) / tpc32;
+  const int tpc48 = T < 48 / group ? T : 48 / group, n48 = (T + tpc48 - 1) / tpc48;
+  const bool wide = n48 < n32;
+  const int tpc = wide ? tpc48 : tpc32;  // tokens per CTA
+  const int n_tg = wide ? n48 : n32;     // CTAs per (split, KV head, request)
   PKV_ARG((int64_t)max_splits * n_tg < (1ll << 31), "%s: grid too large", name);
   PKV_UNSUP(block_size % 8 == 0, "%s: block_size must be a multiple of 8", name);
   PKV_UNSUP(split_tokens % kBN == 0, "%s: split_tokens must be a multiple of 128", name);
@@ -894,13 +992,11 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
   p.rows = (int64_t)num_reqs * T * num_q_heads;
   p.dev_err = dev_err;
   p.wait_limit_ns = take_wait_limit_ns();
-  constexpr int kSmem = 1024 + kTiles + (int)sizeof(Barriers);
-  static std::atomic<uint64_t> attr_done{0};
-  once_per_device(attr_done, [] {
-    cudaFuncSetAttribute(spec_verify_partial_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  });
   dim3 grid((unsigned)(max_splits * n_tg), (unsigned)num_kv_heads, (unsigned)num_reqs);
-  spec_verify_partial_kernel<kFp8><<<grid, kThreads, kSmem, static_cast<cudaStream_t>(stream)>>>(p);
+  if (wide)
+    launch_shape<kFp8, 48>(p, grid, static_cast<cudaStream_t>(stream));
+  else
+    launch_shape<kFp8, 32>(p, grid, static_cast<cudaStream_t>(stream));
   return check_launch(name);
 }
 

@@ -481,8 +481,9 @@ def test_verify_partials_and_combine(pkv, split):
 @pytest.mark.parametrize("T,hq,hkv", [(1, 16, 4), (4, 24, 4), (5, 16, 4), (2, 32, 4), (8, 24, 4), (11, 16, 4)])
 def test_verify_other_query_geometries(pkv, T, hq, hkv):
     """T * group other than 32 query columns: a T = 1 decode step; the pages' 24/4 heads with T = 4
-    (24 columns, padded) and T = 8 (48 columns: two CTAs per key range); odd T; T = 11 with 4 heads
-    (44 columns). Padding columns must not leak into live ones, and only live rows are written."""
+    (24 columns, padded) and T = 8 (48 columns: the 48-column CTA shape); odd T; T = 11 with 4 heads
+    (44 columns, 48-column shape, padded); 32/4 heads with T = 2. Padding columns must not leak into
+    live ones, and only live rows are written."""
     p = W.make_problem("vq", seed=53 + T, seq_lens=[L + T for L in (700, 64, 2100)], q_lens=[T] * 3,
                        num_blocks=60, block_size=64, num_q_heads=hq, num_kv_heads=hkv, kv_dtype="int8",
                        softmax_scale=1.0 / 16.0)
@@ -602,20 +603,22 @@ def test_out_of_range_block_id_is_reported_not_read(pkv):
 # verify over a per-tensor fp8 e4m3 cache
 # ---------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("split,bs", [(128, 16), (2048, 880)])
-def test_verify_fp8_partials_and_combine(pkv, split, bs):
+@pytest.mark.parametrize("split,bs,hq", [(128, 16, 16), (2048, 880, 16), (256, 64, 24)])
+def test_verify_fp8_partials_and_combine(pkv, split, bs, hq):
+    """e4m3 cache with per-tensor scales; hq = 24 (8 tokens x 6 heads = 48 query columns) runs the
+    48-column CTA shape."""
     T = 8
     p = W.make_problem("vf8", seed=81, seq_lens=[L + T for L in (100, 3000, 6000, 129)], q_lens=[T] * 4,
                        num_blocks=max(64, 4 * (6008 // bs + 2)), block_size=bs, kv_dtype="e4m3",
-                       softmax_scale=1.0 / 16.0)
+                       num_q_heads=hq, num_kv_heads=4, softmax_scale=1.0 / 16.0)
     k, v = device_pool(p, "k"), device_pool(p, "v")
     bt, sl, _ = device_meta(p)
     q = device_q(p)
     kd = torch.tensor([0.5], dtype=torch.float32, device="cuda")
     vd = torch.tensor([0.75], dtype=torch.float32, device="cuda")
     S = pkv.splits_needed(int(p.seq_lens.max()), split)
-    po = torch.full((S, q.shape[0], 16, 256), float("nan"), dtype=torch.float32, device="cuda")
-    pl = torch.full((S, q.shape[0], 16), float("nan"), dtype=torch.float32, device="cuda")
+    po = torch.full((S, q.shape[0], hq, 256), float("nan"), dtype=torch.float32, device="cuda")
+    pl = torch.full((S, q.shape[0], hq), float("nan"), dtype=torch.float32, device="cuda")
     out = torch.empty_like(q)
     err = dev_err()
     pkv.spec_verify_attn_partial_fp8(q, k, v, kd, vd, bt, sl, T, p.softmax_scale, split, po, pl, dev_err=err)
@@ -623,7 +626,7 @@ def test_verify_fp8_partials_and_combine(pkv, split, bs):
     torch.cuda.synchronize()
     assert err.item() == 0
     args = (p.q, p.pool_numpy("k"), p.pool_numpy("v"), 0.5, 0.75, p.block_table(fill=0), p.seq_lens)
-    ref = oracle.spec_verify_attn_fp8(*args, T, 16, p.softmax_scale)
+    ref = oracle.spec_verify_attn_fp8(*args, T, hq, p.softmax_scale)
     _close(bf16_to_u16(out), ref, TOL_BF16)
-    rpo, rpl = oracle.spec_verify_partial_fp8(*args, T, 16, p.softmax_scale, split, S)
+    rpo, rpl = oracle.spec_verify_partial_fp8(*args, T, hq, p.softmax_scale, split, S)
     _partials_close(po.cpu().numpy(), pl.cpu().numpy(), rpo, rpl, p.seq_lens, split, T)
