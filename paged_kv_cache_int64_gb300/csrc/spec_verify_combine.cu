@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   };
   if (ns <= 32) {
     // lane s holds split s's LSE and, after the two reductions, its weight; the partials' loads
-    // then carry no dependence on an LSE load and run four splits at a time
+    // then carry no dependence on an LSE load and run eight splits at a time (a row of the longest
+    // request has ~20 splits: three memory round trips)
     const float l = lane < ns ? __ldg(part_lse + (int64_t)lane * rows + row) : -INFINITY;
     float m = l;
 #pragma unroll
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float w_lane = sum > 0.0f ? e * (1.0f / sum) : 0.0f;
-#pragma unroll 4
+#pragma unroll 8
     for (int s = 0; s < ns; ++s) add(s, __shfl_sync(0xffffffffu, w_lane, s));
   } else {
     float m = -INFINITY;
