@@ -478,6 +478,22 @@ def test_verify_partials_and_combine(pkv, split):
     _partials_close(po, pl, rpo, rpl, p.seq_lens, split, T)
 
 
+def test_verify_combine_more_than_32_splits(pkv):
+    """A request cut into 40 splits (split 128): the combine's path for more splits than a warp has
+    lanes (the LSEs reduced in strides of 32, then the partials merged one split at a time), next
+    to a short request on the 32-or-fewer path."""
+    T, split = 8, 128
+    p = W.make_problem("vc", seed=61, seq_lens=[5000 + T, 300 + T], q_lens=[T] * 2, num_blocks=90,
+                       block_size=64, kv_dtype="int8", softmax_scale=1.0 / 16.0)
+    got, po, pl = _run_verify(pkv, p, split, T)
+    assert po.shape[0] == 40
+    args = _verify_oracle_args(p)
+    ref = oracle.spec_verify_attn(*args, T, p.num_q_heads, p.softmax_scale)
+    _close(got, ref, TOL_BF16)
+    rpo, rpl = oracle.spec_verify_partial(*args, T, p.num_q_heads, p.softmax_scale, split, po.shape[0])
+    _partials_close(po, pl, rpo, rpl, p.seq_lens, split, T)
+
+
 @pytest.mark.parametrize("T,hq,hkv", [(1, 16, 4), (4, 24, 4), (5, 16, 4), (2, 32, 4), (8, 24, 4), (11, 16, 4)])
 def test_verify_other_query_geometries(pkv, T, hq, hkv):
     """T * group other than 32 query columns: a T = 1 decode step; the pages' 24/4 heads with T = 4
