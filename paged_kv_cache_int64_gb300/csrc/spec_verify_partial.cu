@@ -648,9 +648,12 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
       blk_2 = key_block(2);
       slot_2 = slot_t;
     }
-    float l_part[kGC];
+    // column sums: 8-column groups keep per-key partial sums (reduced once, at the end); 16-column
+    // groups reduce each tile's sums across the warp and keep column (lane % 16)'s in the lane
+    constexpr int kLP = kGC == 16 ? 1 : kGC;
+    float l_part[kLP];
 #pragma unroll
-    for (int q = 0; q < kGC; ++q) l_part[q] = 0.0f;
+    for (int q = 0; q < kLP; ++q) l_part[q] = 0.0f;
     float m_col = -INFINITY;
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
@@ -742,12 +745,14 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
 #pragma unroll
         for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - e[q]);
       }
-      if (any_rescale) {
+      if constexpr (kGC != 16) {
+        if (any_rescale) {
 #pragma unroll
-        for (int q = 0; q < kGC; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
-      } else {
+          for (int q = 0; q < kGC; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
+        } else {
 #pragma unroll
-        for (int q = 0; q < kGC; ++q) l_part[q] += e[q];
+          for (int q = 0; q < kGC; ++q) l_part[q] += e[q];
+        }
       }
       if (!dead) {  // P^T for key k (columns c0 .. c0 + kGC - 1 of buffer j % 2): p * v_scale, fp16
         const float vs = vs_cur;
@@ -766,6 +771,10 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
           const uint32_t chunk = (uint32_t)(grp * (kGC / 8) + cc);
           *reinterpret_cast<uint4*>(prow + ((chunk ^ sw) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
+      }
+      if constexpr (kGC == 16) {  // the weights are stored: reduce them (in place) to the tile's sums
+        const float tsum = reduce_scatter16<false>(e, lane);
+        l_part[0] = (rescale ? l_part[0] * alpha : l_part[0]) + tsum;  // column c0 + cl
       }
       if (!dead) {
         tc_fence_after();
@@ -796,7 +805,9 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
-      const float sum = reduce_scatter<kGC, false>(l_part, lane);
+      float sum;
+      if constexpr (kGC == 16) sum = l_part[0];
+      else sum = reduce_scatter<kGC, false>(l_part, lane);
       if (lane < kGC) bar.red[0][grp][quarter][lane] = sum;
     }
     named_bar_sync(1 + grp, 128);
