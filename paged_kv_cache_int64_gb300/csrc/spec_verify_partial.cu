@@ -37,8 +37,9 @@
 //              group's four warps, after which lane l keeps column (l & 7)'s running max (moved
 //              only when it grows by more than 2^8) and broadcasts it by shuffles; P^T = p * v_scale
 //              in fp16 into one of two buffers, so the softmax waits for the PV two tiles back (and
-//              for the last one only to rescale O^T); at the end, column sums, normalised partial O
-//              and its LSE.
+//              for the last one only to rescale O^T); the stored weights reduced per tile to column
+//              sums that lane l keeps for column (l & 7); at the end, normalised partial O and its
+//              LSE. (The 48-column shape: three groups of 16 columns, see Geo.)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -648,12 +649,9 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
       blk_2 = key_block(2);
       slot_2 = slot_t;
     }
-    // column sums: 8-column groups keep per-key partial sums (reduced once, at the end); 16-column
-    // groups reduce each tile's sums across the warp and keep column (lane % 16)'s in the lane
-    constexpr int kLP = kGC == 16 ? 1 : kGC;
-    float l_part[kLP];
-#pragma unroll
-    for (int q = 0; q < kLP; ++q) l_part[q] = 0.0f;
+    // column sums: each tile's weights are reduced across the warp once they are stored, and lane l
+    // keeps the running sum of column c0 + (l % kGC) (no per-key partial sums in registers)
+    float l_col = 0.0f;
     float m_col = -INFINITY;
     bool dead = false;  // warp-uniform; the named barrier below is reached the same number of times
     for (int j = 0; j < n_tiles; ++j) {
@@ -731,8 +729,8 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
         dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort, wl));
       if (!dead && any_rescale && j >= 1)
         dead = !__all_sync(0xffffffffu, mbar_wait_suspend(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, wl));
-      // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps,
-      // the running column sums and the fp16 P^T stores run as independent batches
+      // P = exp2(s - m): the column maxima are broadcast from their lanes first, then the exps and
+      // the fp16 P^T stores run as independent batches
       // (16 columns: in place over the scores, which keeps the registers within the 896-thread budget)
       float e_buf[kGC == 16 ? 1 : kGC];
       float (&e)[kGC] = *reinterpret_cast<float(*)[kGC]>(kGC == 16 ? s : e_buf);
@@ -744,15 +742,6 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
         for (int q = 0; q < kGC; ++q) e[q] = __shfl_sync(0xffffffffu, mu, q);
 #pragma unroll
         for (int q = 0; q < kGC; ++q) e[q] = ex2_approx(s[q] - e[q]);
-      }
-      if constexpr (kGC != 16) {
-        if (any_rescale) {
-#pragma unroll
-          for (int q = 0; q < kGC; ++q) l_part[q] = l_part[q] * __shfl_sync(0xffffffffu, alpha, q) + e[q];
-        } else {
-#pragma unroll
-          for (int q = 0; q < kGC; ++q) l_part[q] += e[q];
-        }
       }
       if (!dead) {  // P^T for key k (columns c0 .. c0 + kGC - 1 of buffer j % 2): p * v_scale, fp16
         const float vs = vs_cur;
@@ -772,9 +761,9 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
           *reinterpret_cast<uint4*>(prow + ((chunk ^ sw) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
       }
-      if constexpr (kGC == 16) {  // the weights are stored: reduce them (in place) to the tile's sums
-        const float tsum = reduce_scatter16<false>(e, lane);
-        l_part[0] = (rescale ? l_part[0] * alpha : l_part[0]) + tsum;  // column c0 + cl
+      {  // the weights are stored: reduce them (in place) to the tile's column sums
+        const float tsum = reduce_scatter<kGC, false>(e, lane);
+        l_col = (rescale ? l_col * alpha : l_col) + tsum;  // column c0 + cl, with its own factor
       }
       if (!dead) {
         tc_fence_after();
@@ -805,10 +794,7 @@ __global__ void __launch_bounds__(Geo<kCols>::kThreads, 1) spec_verify_partial_k
     fin = __all_sync(0xffffffffu, fin);
     named_bar_sync(1 + grp, 128);  // every warp of the group is past its last read of bar.red
     {
-      float sum;
-      if constexpr (kGC == 16) sum = l_part[0];
-      else sum = reduce_scatter<kGC, false>(l_part, lane);
-      if (lane < kGC) bar.red[0][grp][quarter][lane] = sum;
+      if (lane < kGC) bar.red[0][grp][quarter][lane] = l_col;
     }
     named_bar_sync(1 + grp, 128);
     if (quarter == 0 && lane < kGC) {  // lane q: column c0 + q's sum, 1 / l and log-sum-exp
