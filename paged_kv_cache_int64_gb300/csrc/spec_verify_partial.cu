@@ -6,11 +6,13 @@
 // with the block id widened to int64, and the int8 per-token-head scales are addressed with the
 // same block id; the key range is cut into splits whose partials are merged by log-sum-exp.
 //
-// sm_103a design, one CTA = (split, KV head, request, token group); the tokens x g query heads that
-// share the KV head form N = 32 query columns (floor(32 / g) tokens per CTA: with T * g > 32 the
-// tokens are spread over adjacent CTAs that read the same keys; columns past the CTA's tokens are
-// zero padding, so a T = 1 decode step runs on the same kernel), and the MMAs are "swapped" so the
-// 128 keys of a tile are the M dimension (the verify step is HBM-bound at ~63 flop per cache byte):
+// sm_103a design, one CTA = (split, KV head, request, token group), launched longest first (see
+// the launch order below); the tokens x g query heads that share the KV head form N = 32 query
+// columns (floor(32 / g) tokens per CTA: with T * g > 32 the tokens are spread over adjacent CTAs
+// that read the same keys, or go to the N = 48 shape when that needs fewer CTAs; columns past the
+// CTA's tokens are zero padding, so a T = 1 decode step runs on the same kernel), and the MMAs are
+// "swapped" so the 128 keys of a tile are the M dimension (the verify step is HBM-bound at ~63 flop
+// per cache byte):
 //   warps 0, 3 TMA producers (K and V): Q once; per 128-key tile, the int8 (or e4m3) codes of K
 //              (warp 0) and of V (warp 3) through 4-D maps over the paged pool (block id as a
 //              coordinate), each into its own two-stage ring: 2 copies for a tile inside one
@@ -23,8 +25,9 @@
 //   warps 8-11 K converter: thread k owns key row k and widens it into the tile's tensor-memory K
 //              buffer (two buffers, so tile j+1 is widened while tile j is scored), then releases
 //              the K stage.
-//   warps 12-15 V converter: once the previous PV has read the V tile, thread k widens V row k into
-//              it (shared memory, MN-major) and releases the V stage. No stage waits for the
+//   warps 12-15, 20-23 V converter, one warpgroup per head_dim half: once the previous PV has read
+//              its half of the V tile, thread k widens its half of V row k into it (shared memory,
+//              MN-major) and releases the V stage. No stage waits for the
 //              softmax, and the K side keeps running while the V side waits for PV. int8 -> fp16
 //              by byte permute (fp16 bits 0x6400|(b^0x80) equal 1024 + b + 128, so one
 //              subtraction of 1152 gives b exactly - the int8->fp16 method of Kim et al. 2022,
