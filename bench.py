@@ -60,13 +60,13 @@ def prefill_pairs(seq_len, q_len):
     return q_len * s + q_len * (q_len + 1) // 2
 
 
-def pick_split(seq_lens, n_sms, hkv=HKV):
-    """split_tokens for a verify launch: the largest of 4096, 2048, 1024, 512 that still gives at
-    least two CTAs per SM (larger splits mean fewer partials to write and combine; smaller ones fill
-    the GPU when there are few or short requests)."""
-    split = 4096
-    while split > 512 and hkv * sum(math.ceil(int(s) / split) for s in seq_lens) < 2 * n_sms:
-        split //= 2
+def pick_split(pkv, seq_lens, n_sms, T=None, hq=None, hkv=HKV):
+    """split_tokens for a verify launch: the library's planner (spec_verify_pick_split), which
+    models the launch as a longest-first list schedule of its CTAs over the SMs from the batch's
+    sequence lengths and returns the split with the shortest modelled time."""
+    split = pkv.spec_verify_pick_split(seq_lens, T_VERIFY if T is None else T, HQ if hq is None else hq, hkv, n_sms)
+    if split <= 0:
+        raise ValueError("spec_verify_pick_split rejected the batch")
     return split
 
 
@@ -258,7 +258,7 @@ class Step:
         bt, sl, _ = device_meta(p)
         q = device_q(p)
         out = torch.empty_like(q)
-        split = pick_split(p.seq_lens, torch.cuda.get_device_properties(dev).multi_processor_count)
+        split = pick_split(pkv, p.seq_lens, torch.cuda.get_device_properties(dev).multi_processor_count)
         S = pkv.splits_needed(int(p.seq_lens.max()), split)
         po = torch.empty((S, q.shape[0], HQ, D), dtype=torch.float32, device=dev)
         pl = torch.empty((S, q.shape[0], HQ), dtype=torch.float32, device=dev)
@@ -665,7 +665,7 @@ def run_extras(torch, pkv, st, flush, args, dev):
 
     def verify_rate(pb, kk, vv, kss, vss, bt, q, seq_lens, T, hq):
         sld = torch.from_numpy(np.asarray(seq_lens, dtype=np.int32)).to(dev)
-        split = pick_split(seq_lens, n_sms)
+        split = pick_split(pkv, seq_lens, n_sms, T, hq)
         S = pkv.splits_needed(int(max(seq_lens)), split)
         po = torch.empty((S, q.shape[0], hq, D), dtype=torch.float32, device=dev)
         pl = torch.empty((S, q.shape[0], hq), dtype=torch.float32, device=dev)
@@ -883,7 +883,7 @@ def run_ncu_case(args):
         ks, vs = device_scale_pool(p, "k"), device_scale_pool(p, "v")
         bt, sl, _ = device_meta(p)
         q = device_q(p)
-        split = pick_split(p.seq_lens, torch.cuda.get_device_properties(dev).multi_processor_count)
+        split = pick_split(pkv, p.seq_lens, torch.cuda.get_device_properties(dev).multi_processor_count)
         S = pkv.splits_needed(int(p.seq_lens.max()), split)
         po = torch.empty((S, q.shape[0], HQ, D), dtype=torch.float32, device=dev)
         pl = torch.empty((S, q.shape[0], HQ), dtype=torch.float32, device=dev)

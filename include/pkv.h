@@ -84,7 +84,7 @@ typedef enum pkv_kv_dtype {
 PKV_API const char* pkv_last_error(void);
 
 /* ABI version of this header (incremented on any signature change). */
-#define PKV_ABI_VERSION 6
+#define PKV_ABI_VERSION 7
 PKV_API int32_t pkv_abi_version(void);
 
 /*
@@ -216,14 +216,28 @@ PKV_API size_t pkv_paged_prefill_workspace_bytes(int32_t num_ctas);
  * one allocation). split_tokens must be a positive multiple of 128.
  * Requirements: head_dim == 256; group = num_q_heads / num_kv_heads <= 32. A CTA serves 32 query
  * columns: floor(32 / group) tokens x group heads (the pages' 8 tokens x 4 heads fill it exactly; a
- * one-token decode step runs with padding columns); when T * group > 32 (e.g. 24/4 heads with
- * T = 8) the tokens are spread over adjacent CTAs that read the same keys. block_size a multiple
+ * one-token decode step runs with padding columns), or 48 when that needs fewer CTAs per key range
+ * (e.g. 24/4 heads with T = 8: one CTA instead of two); otherwise the tokens are spread over
+ * adjacent CTAs that read the same keys. block_size a multiple
  * of 8; q, caches and cache strides 16-byte aligned; scale pools 4-byte aligned with
  * scale_stride_tok >= num_kv_heads (head stride 1). Keys in a
  * block whose id is out of range read as zero (k = v = 0) and PKV_ERR_DEVICE_BOUNDS is recorded.
  */
 PKV_API size_t pkv_spec_verify_workspace_bytes(int32_t num_tokens, int32_t num_q_heads, int32_t head_dim,
                                        int32_t max_splits);
+/*
+ * spec_verify_pick_split - host-side planning for pkv_spec_verify_attn_partial: the split_tokens (a
+ * multiple of 512 from 1,024 to 16,384) for which a model of the launch predicts the shortest
+ * time, given the batch's seq_lens in HOST memory (num_reqs of them), T, the head counts and the
+ * device's SM count. The model: the CTAs run longest first, one per SM; each costs a fixed time
+ * plus a time per 128-key tile, each CTA past a request's keys a small fixed time (constants
+ * measured on GB300); the result is the makespan of that list schedule. Larger splits mean fewer
+ * partials and empty CTAs, smaller ones a finer balance over the SMs. Reads nothing on the device.
+ * Returns 0 on a bad argument (null pointer, non-positive count, num_q_heads not a multiple of
+ * num_kv_heads, group above 32).
+ */
+PKV_API int32_t pkv_spec_verify_pick_split(const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                           int32_t num_q_heads, int32_t num_kv_heads, int32_t num_sms);
 PKV_API pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
                                         const float* k_scale, const float* v_scale,
                                         int64_t num_blocks, int64_t stride_blk, int64_t stride_tok,

@@ -19,7 +19,7 @@ from . import _build
 __all__ = [
     "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_CUDA", "PKV_ERR_DEVICE_BOUNDS",
     "PKV_ERR_TIMEOUT", "PKV_QK_BF16", "PKV_QK_INT8", "PKV_KV_BF16", "PKV_KV_INT8", "PKV_KV_FP8", "PkvError", "lib",
-    "library_path", "kv_cache_write", "kv_int8_stats_quant", "paged_prefill_attn_fp8", "kv_fp8_dequant_dense", "paged_prefill_attn", "paged_prefill_workspace_bytes", "spec_verify_workspace_bytes",
+    "library_path", "kv_cache_write", "kv_int8_stats_quant", "paged_prefill_attn_fp8", "kv_fp8_dequant_dense", "paged_prefill_attn", "paged_prefill_workspace_bytes", "spec_verify_workspace_bytes", "spec_verify_pick_split",
     "spec_verify_attn_partial", "spec_verify_attn_partial_fp8", "spec_verify_combine", "EXPORTED_SYMBOLS",
 ]
 
@@ -32,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_prefill_attn", "pkv_spec_verify_workspace_bytes", "pkv_spec_verify_attn_partial",
     "pkv_spec_verify_combine", "pkv_spec_verify_attn_partial_fp8", "pkv_spec_verify_noalloc_capacity_bytes",
     "pkv_spec_verify_attn_noalloc", "pkv_kv_cache_write", "pkv_paged_prefill_attn_fp8",
-    "pkv_paged_prefill_workspace_bytes", "pkv_testing_set_wait_limit_ns",
+    "pkv_paged_prefill_workspace_bytes", "pkv_testing_set_wait_limit_ns", "pkv_spec_verify_pick_split",
 )
 
 library_path = _build.LIB
@@ -64,6 +64,8 @@ def _load():
     L.pkv_paged_prefill_workspace_bytes.restype = sz
     L.pkv_spec_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
     L.pkv_spec_verify_workspace_bytes.restype = sz
+    L.pkv_spec_verify_pick_split.argtypes = [vp, i32, i32, i32, i32, i32]
+    L.pkv_spec_verify_pick_split.restype = i32
     L.pkv_spec_verify_attn_partial.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i32, vp,
                                                i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
     L.pkv_spec_verify_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
@@ -233,6 +235,15 @@ def paged_prefill_workspace_bytes(num_ctas=None) -> int:
 
 def spec_verify_workspace_bytes(num_tokens, num_q_heads, head_dim, max_splits) -> int:
     return int(lib.pkv_spec_verify_workspace_bytes(num_tokens, num_q_heads, head_dim, max_splits))
+
+
+def spec_verify_pick_split(seq_lens, T, num_q_heads, num_kv_heads, num_sms) -> int:
+    """Host-side split_tokens choice for spec_verify_attn_partial from the batch's sequence lengths
+    (host values); 0 on a bad argument."""
+    import numpy as np
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    return int(lib.pkv_spec_verify_pick_split(sl.ctypes.data, int(sl.shape[0]), int(T), int(num_q_heads),
+                                               int(num_kv_heads), int(num_sms)))
 
 
 def spec_verify_attn_partial(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, T, softmax_scale,

@@ -46,6 +46,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <queue>
+#include <utility>
+#include <vector>
+
 #include "host_common.h"
 #include "sm103.cuh"
 
@@ -1002,6 +1007,75 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
 
 }  // namespace
 }  // namespace pkv
+
+// Host-side planning: the launch's CTAs run longest first, one per SM, so the kernel time is about
+// the makespan of a longest-processing-time-first list schedule of its CTAs: every (split, KV head,
+// token group) CTA costs kCtaUs plus kTileUs per 128-key tile (x1.4 for the 48-column shape), and
+// every CTA past a request's keys kEmptyUs (constants fitted to GB300 timings of a 32-request batch
+// swept over ten split sizes, residual 2 us). The whole splits are all alike and go first, so they
+// are dealt round-robin in closed form; the shorter last splits are placed greedily, longest first;
+// the empty CTAs then fill the idle time below the makespan before they extend it.
+extern "C" int32_t pkv_spec_verify_pick_split(const int32_t* seq_lens, int32_t num_reqs, int32_t T,
+                                              int32_t num_q_heads, int32_t num_kv_heads, int32_t num_sms) {
+  using namespace pkv;
+  if (!seq_lens || num_reqs <= 0 || T <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_sms <= 0 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 32) return 0;
+  const int tpc32 = T < 32 / group ? T : 32 / group, n32 = (T + tpc32 - 1) / tpc32;
+  const int tpc48 = T < 48 / group ? T : 48 / group, n48 = (T + tpc48 - 1) / tpc48;
+  const bool wide = n48 < n32;
+  const int64_t units = (int64_t)num_kv_heads * (wide ? n48 : n32);  // CTAs per (request, split)
+  constexpr double kCtaUs = 7.5, kTileUs = 2.08, kEmptyUs = 2.0;
+  const double tile_us = wide ? 1.4 * kTileUs : kTileUs;
+  int64_t max_len = 0;
+  for (int r = 0; r < num_reqs; ++r) max_len = std::max<int64_t>(max_len, std::max(seq_lens[r], 0));
+  if (max_len == 0) return 1024;
+  std::vector<int64_t> rests;
+  std::vector<double> sm(num_sms);
+  int32_t best_split = 0;
+  double best = 0.0;
+  for (int32_t split = 1024; split <= 16384; split += 512) {
+    const int64_t ms = (max_len + split - 1) / split;
+    int64_t n_full = 0;
+    rests.clear();
+    for (int r = 0; r < num_reqs; ++r) {
+      const int64_t len = std::max(seq_lens[r], 0);
+      n_full += len / split;
+      if (len % split) rests.push_back(len % split);
+    }
+    std::sort(rests.begin(), rests.end(), [](int64_t a, int64_t b) { return a > b; });
+    // whole splits: F CTAs of equal cost dealt round-robin
+    const int64_t F = n_full * units;
+    const double full_us = kCtaUs + tile_us * (split / kBN);
+    for (int i = 0; i < num_sms; ++i) sm[i] = (double)(F / num_sms + (i < F % num_sms ? 1 : 0)) * full_us;
+    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<std::pair<double, int>>> pq;
+    for (int i = 0; i < num_sms; ++i) pq.push({sm[i], i});
+    for (const int64_t rest : rests)
+      for (int64_t u = 0; u < units; ++u) {
+        auto top = pq.top();
+        pq.pop();
+        top.first += kCtaUs + tile_us * (double)((rest + kBN - 1) / kBN);
+        pq.push(top);
+      }
+    double makespan = 0.0, total = 0.0;
+    while (!pq.empty()) {
+      makespan = std::max(makespan, pq.top().first);
+      total += pq.top().first;
+      pq.pop();
+    }
+    // empty CTAs: first into the idle time below the makespan, the rest spread over every SM
+    const int64_t empties = (int64_t)num_reqs * ms * units - (n_full + (int64_t)rests.size()) * units;
+    const double idle = makespan * num_sms - total, extra = empties * kEmptyUs - idle;
+    if (extra > 0.0) makespan += extra / num_sms;
+    if (best_split == 0 || makespan < best) {
+      best = makespan;
+      best_split = split;
+    }
+  }
+  return best_split;
+}
 
 extern "C" pkv_status pkv_spec_verify_attn_partial(const void* q, const int8_t* k_cache, const int8_t* v_cache,
                                                    const float* k_scale, const float* v_scale, int64_t num_blocks,

@@ -57,7 +57,7 @@ def test_library_targets_sm103a(libpath):
 
 
 def test_abi_version(pkv):
-    assert pkv.lib.pkv_abi_version() == 6
+    assert pkv.lib.pkv_abi_version() == 7
 
 
 def test_workspace_bytes(pkv):
@@ -191,3 +191,41 @@ def test_noalloc_rejects_sizes_whose_product_wraps(pkv):
                128, splits, 16, None, None)
         assert rc == pkv.PKV_ERR_INVALID_ARG
         assert "scratch" in pkv.lib.pkv_last_error().decode()
+
+
+def test_verify_pick_split(pkv):
+    """The split planner (host code, no device): a multiple of 512 in [1024, 16384]; a batch that
+    cannot fill the SMs is cut fine (one 20k request over 152 SMs); a large batch whose splits fill
+    the SMs many times over gets a large split; its choice agrees with a brute-force evaluation of
+    the same longest-first list-schedule model written out here; bad arguments give 0."""
+    import heapq
+    import numpy as np
+    import workloads as W
+    L = W.verify_batch(distinct=True, with_kv=False).seq_lens
+    for T, hq in ((8, 16), (8, 24), (1, 16)):
+        sp = pkv.spec_verify_pick_split(L, T, hq, 4, 152)
+        assert sp % 512 == 0 and 1024 <= sp <= 16384
+    assert pkv.spec_verify_pick_split([20008], 8, 16, 4, 152) <= 2048
+    assert pkv.spec_verify_pick_split([20008], 8, 16, 4, 0) == 0
+    assert pkv.spec_verify_pick_split([20008], 8, 16, 3, 152) == 0
+    assert pkv.spec_verify_pick_split([20008], 8, 160, 4, 152) == 0
+
+    def model(split, lens, units=4, n_sm=152, cta=7.5, tile=2.08, empty=2.0):
+        ms = max((int(x) + split - 1) // split for x in lens)
+        full = [split] * (sum(int(x) // split for x in lens) * units)
+        part = sorted([int(x) % split for x in lens if int(x) % split] * units, reverse=True)
+        sms = [0.0] * n_sm
+        for k in full + part:
+            t = heapq.heappop(sms)
+            heapq.heappush(sms, t + cta + tile * ((k + 127) // 128))
+        live = len(full) + len(part)
+        for _ in range(len(lens) * ms * units - live):
+            t = heapq.heappop(sms)
+            heapq.heappush(sms, t + empty)
+        return max(sms)
+    rng = np.random.default_rng(3)
+    for lens in (L, rng.integers(1000, 60000, 20), rng.integers(8, 3000, 64)):
+        got = pkv.spec_verify_pick_split(lens, 8, 16, 4, 152)
+        times = {sp: model(sp, lens) for sp in range(1024, 16385, 512)}
+        best = min(times.values())
+        assert times[got] <= best * 1.02, (got, times[got], best)

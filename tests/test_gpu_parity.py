@@ -563,14 +563,18 @@ def _verify_all_requests(p, T):
     return np.concatenate(parts, axis=0)
 
 
-@pytest.mark.parametrize("pool,split", [("distinct", 4096), ("literal", 2048)])
+@pytest.mark.parametrize("pool,split", [("distinct", 4096), ("literal", 2048), ("distinct", "planned")])
 def test_verify_batch_config(pkv, pool, split):
     """32 requests, lognormal prefixes 4k-80k (median 16k), T = 8, int8 KV, bs 880; every request against
-    the oracle. "distinct": a pool of just the blocks the batch needs (split 4,096, the bench's launch);
-    "literal": the pages' 480k-token pool (546 blocks), which cannot hold the batch's ~670 blocks,
-    so the tables walk one permutation cyclically and requests share blocks."""
+    the oracle. "distinct": a pool of just the blocks the batch needs; "literal": the pages'
+    480k-token pool (546 blocks), which cannot hold the batch's ~670 blocks, so the tables walk one
+    permutation cyclically and requests share blocks. "planned": the split the library's planner
+    picks for the batch (the bench's launch; a large split, 6 or fewer per request)."""
     T = 8
     p = W.verify_batch(distinct=pool == "distinct")
+    if split == "planned":
+        split = pkv.spec_verify_pick_split(p.seq_lens, T, 16, 4, torch.cuda.get_device_properties(0).multi_processor_count)
+        assert split % 512 == 0 and split >= 1024
     if pool == "literal":
         assert p.num_blocks == 546 and sum(len(r.blocks) for r in p.requests) > p.num_blocks
     got, _, _ = _run_verify(pkv, p, split, T)
