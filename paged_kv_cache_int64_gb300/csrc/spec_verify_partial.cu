@@ -1013,8 +1013,10 @@ pkv_status launch_verify(const char* name, const void* q, const void* k_cache, c
 // token group) CTA costs kCtaUs plus kTileUs per 128-key tile (x1.4 for the 48-column shape), and
 // every CTA past a request's keys kEmptyUs (constants fitted to GB300 timings of a 32-request batch
 // swept over ten split sizes, residual 2 us). The whole splits are all alike and go first, so they
-// are dealt round-robin in closed form; the shorter last splits are placed greedily, longest first;
-// the empty CTAs then fill the idle time below the makespan before they extend it.
+// are dealt round-robin in closed form; the shorter last splits are placed greedily, longest first
+// (beyond 8 per SM, where the greedy schedule is all but level, the makespan is taken as the mean
+// load plus the largest of them, which keeps the planner linear in the batch); the empty CTAs then
+// fill the idle time below the makespan before they extend it.
 extern "C" int32_t pkv_spec_verify_pick_split(const int32_t* seq_lens, int32_t num_reqs, int32_t T,
                                               int32_t num_q_heads, int32_t num_kv_heads, int32_t num_sms) {
   using namespace pkv;
@@ -1045,25 +1047,40 @@ extern "C" int32_t pkv_spec_verify_pick_split(const int32_t* seq_lens, int32_t n
       n_full += len / split;
       if (len % split) rests.push_back(len % split);
     }
-    std::sort(rests.begin(), rests.end(), [](int64_t a, int64_t b) { return a > b; });
     // whole splits: F CTAs of equal cost dealt round-robin
     const int64_t F = n_full * units;
     const double full_us = kCtaUs + tile_us * (split / kBN);
     for (int i = 0; i < num_sms; ++i) sm[i] = (double)(F / num_sms + (i < F % num_sms ? 1 : 0)) * full_us;
-    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<std::pair<double, int>>> pq;
-    for (int i = 0; i < num_sms; ++i) pq.push({sm[i], i});
-    for (const int64_t rest : rests)
-      for (int64_t u = 0; u < units; ++u) {
-        auto top = pq.top();
-        pq.pop();
-        top.first += kCtaUs + tile_us * (double)((rest + kBN - 1) / kBN);
-        pq.push(top);
-      }
     double makespan = 0.0, total = 0.0;
-    while (!pq.empty()) {
-      makespan = std::max(makespan, pq.top().first);
-      total += pq.top().first;
-      pq.pop();
+    if ((int64_t)rests.size() * units <= 8 * (int64_t)num_sms) {
+      std::sort(rests.begin(), rests.end(), [](int64_t a, int64_t b) { return a > b; });
+      std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>,
+                          std::greater<std::pair<double, int>>> pq;
+      for (int i = 0; i < num_sms; ++i) pq.push({sm[i], i});
+      for (const int64_t rest : rests)
+        for (int64_t u = 0; u < units; ++u) {
+          auto top = pq.top();
+          pq.pop();
+          top.first += kCtaUs + tile_us * (double)((rest + kBN - 1) / kBN);
+          pq.push(top);
+        }
+      while (!pq.empty()) {
+        makespan = std::max(makespan, pq.top().first);
+        total += pq.top().first;
+        pq.pop();
+      }
+    } else {
+      for (int i = 0; i < num_sms; ++i) {
+        total += sm[i];
+        makespan = std::max(makespan, sm[i]);
+      }
+      double largest = 0.0;
+      for (const int64_t rest : rests) {
+        const double d = kCtaUs + tile_us * (double)((rest + kBN - 1) / kBN);
+        total += d * (double)units;
+        largest = std::max(largest, d);
+      }
+      makespan = std::max(makespan, total / num_sms + largest);
     }
     // empty CTAs: first into the idle time below the makespan, the rest spread over every SM
     const int64_t empties = (int64_t)num_reqs * ms * units - (n_full + (int64_t)rests.size()) * units;
